@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the MSA decode step over a paged NVFP4 cache (one layer-step per step).
+
+Default workload: speculative decode, B=64 sequences of 131,072 tokens (1,024 blocks), 8 query
+tokens each, hot blocks planted, random paging (the configuration the headline metric is
+quoted on). One step = indexer -> top-k -> sparse attention -> merge over the whole batch
+(msa_decode_step), inputs resident in HBM, L2 flushed by a 256 MB write between timed steps.
+
+Prints one JSON line. `value` is microseconds per layer-step (lower is better, max over
+ranks); the roofline object reports the dominant kernel (the indexer) against the measured
+HBM peak; `e2e` repeats the measurement through host buffers (pinned H2D of the step's
+queries and metadata, D2H of the output) inside the timed region; `cpu_baseline` times the
+oracle on a bounded sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config spec] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "MSA decode µs/layer-step & achieved HBM TB/s (indexer+topk+attn), B=64 @128K"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def index_bytes(w: W.Workload, layer: int) -> int:
+    """Algorithmic bytes of the index scan: every valid token's index key once (shared pages
+    once), plus the index queries."""
+    per_tok = 72 if w.layers[layer].index_dtype == W.INDEX_NVFP4 else 128
+    toks = 0
+    seen = set()
+    for b in range(w.B):
+        if w.q_lens[b] == 0:
+            continue
+        L = w.seq_lens[b]
+        for k in range((L + 127) // 128):
+            pg = int(w.block_table[b, k])
+            if pg in seen:
+                continue
+            seen.add(pg)
+            toks += min(128, L - 128 * k)
+    return toks * per_tok + w.T * 512
+
+
+def step_bytes(w: W.Workload, layer: int, sel: np.ndarray) -> int:
+    """Algorithmic bytes of one layer-step: the index scan, each (sequence, group)'s distinct
+    selected valid tokens x 144 B (K and V codes + scales), and per query token its Q (8,192
+    B), index query (512 B, counted in index_bytes) and bf16 output (16,384 B)."""
+    qsl = w.query_start_loc()
+    kv = 0
+    for b in range(w.B):
+        ql, L = w.q_lens[b], w.seq_lens[b]
+        if ql == 0:
+            continue
+        for g in range(4):
+            blocks = set(int(x) for x in sel[qsl[b]:qsl[b] + ql, g].ravel() if x >= 0)
+            kv += sum(min(128, L - 128 * k) for k in blocks if 128 * k < L) * 144
+    return index_bytes(w, layer) + kv + w.T * (8192 + 16384)
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        mhz, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def recorded_traffic(kernel: str, source: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when the
+    kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    h = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:16]
+    return d.get("bytes_per_launch") if d.get("source_sha") == h else None
+
+
+# ---------------------------------------------------------------------------- oracle leg
+def oracle_sample(w: W.Workload, layer: int, b: int, device: str):
+    """Time the oracle (indexer + selection + attention) on sequence b; the inputs are
+    quantised outside the timed region (the caches are resident state)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from parity import OracleSeq
+
+    oracle.build()
+    ref = OracleSeq(w, layer, b, device, kv_blocks=None)
+    t0 = time.perf_counter()
+    s = ref.scores()
+    sel = oracle.select_seq(s, ref.L, ref.q_len)
+    ref.attention(sel, 1.0 / math.sqrt(128))
+    dt = time.perf_counter() - t0
+    return dt, oracle.hardware_threads()
+
+
+def run_reference(args, w: W.Workload, rank: int):
+    if rank != 0:
+        return
+    device = "cuda" if _cuda_ok() else "cpu"
+    active = [b for b in range(w.B) if w.q_lens[b] > 0]
+    times = []
+    cores = 0
+    for i in range(args.warmup + args.steps):
+        b = active[i % len(active)]
+        dt, cores = oracle_sample(w, 0, b, device)
+        if i >= args.warmup:
+            times.append(dt)
+    per_step_s = statistics.mean(times) * len(active)
+    v = per_step_s * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/layer-step", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "seq_len": max(w.seq_lens), "q_len": max(w.q_lens),
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": v, "unit": "us/layer-step", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: one of {len(active)} sequences (all its query tokens, 4 groups,"
+                                       f" 64 heads), oracle wall time x {len(active)}"},
+            "e2e": {"value": v, "unit": "us/layer-step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _cuda_ok():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# ---------------------------------------------------------------------------- GPU leg
+def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_kv_cache_gb300 as msa
+    from workloads.device import DeviceLayer
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    dl = DeviceLayer(w, 0, device=dev)
+    o = dl.outputs()
+    ws = dl.workspace()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    B, T = w.B, w.T
+
+    def step():
+        msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if msa.msa_read_device_status(ws) != msa.MSA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- headline: K timed steps of the fused call, L2 flushed between them
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop() if clocks else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+
+    # ---- per-stage breakdown: the same three calls with events between them
+    o2 = dl.outputs()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    aws_n = msa.msa_attn_workspace_size(B, T, 0)
+    aws = torch.empty(max(aws_n, 256), dtype=torch.uint8, device=dev)
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e = st_ev[i]
+        e[0].record(stream)
+        msa.msa_indexer_decode(dl.batch, dl.cache, dl.iq8, o2["scores"], status)
+        e[1].record(stream)
+        msa.msa_topk_blocks(dl.batch, o2["scores"], o2["sel"], status)
+        e[2].record(stream)
+        msa.msa_sparse_attn_decode(dl.batch, dl.cache, dl.q8, o2["sel"], dl.softmax_scale, o2["out"], 0, aws, status)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    stage_ms = [statistics.mean(st_ev[i][j].elapsed_time(st_ev[i][j + 1]) for i in range(args.steps))
+                for j in range(3)]
+    assert msa.status_bits(status) == 0
+    sel = o2["sel"].cpu().numpy()
+
+    # ---- end to end through host buffers: pinned H2D of the step's inputs, D2H of the output
+    q_h = dl.q8.cpu().pin_memory()
+    iq_h = dl.iq8.cpu().pin_memory()
+    meta = [dl.batch.query_start_loc, dl.batch.seq_lens, dl.batch.block_table]
+    meta_h = [m.cpu().pin_memory() for m in meta]
+    out_h = torch.empty(o["out"].shape, dtype=o["out"].dtype).pin_memory()
+    h2d = q_h.numel() + iq_h.numel() + sum(m.numel() * m.element_size() for m in meta_h)
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        dl.q8.copy_(q_h, non_blocking=True)
+        dl.iq8.copy_(iq_h, non_blocking=True)
+        for m, mh in zip(meta, meta_h):
+            m.copy_(mh, non_blocking=True)
+        step()
+        out_h.copy_(o["out"], non_blocking=True)
+        e2e_ev[i][1].record(stream)
+        e2e_ev[i][1].synchronize()
+    barrier()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    t2 = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+    e2e_ms = float(t2.item())
+
+    if rank != 0:
+        return
+    peak_gbs, peak_kind = peaks()
+    idx_bytes = index_bytes(w, 0)
+    total_bytes = step_bytes(w, 0, sel)
+    idx_gbs = idx_bytes / (stage_ms[0] * 1e-3) / 1e9
+    launches_per_step = 3 + (1 if aws_n > 0 else 0)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        dt, cores = oracle_sample(w, 0, 0, dev)
+        active = sum(1 for q in w.q_lens if q > 0)
+        cpu = {"value": dt * active * 1e6, "unit": "us/layer-step", "cores": cores, "kind": "oracle",
+               "sample": f"sequence 0 of {active} (all {w.q_lens[0]} query tokens, 4 groups, 64 heads): oracle "
+                         f"indexer+selection+attention wall time x {active}"}
+    line = {
+        "metric": METRIC, "value": ms_max * 1e3, "unit": "us/layer-step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 MMA, fp32 accumulate/softmax, f16 PV", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "seq_len": max(w.seq_lens), "q_len": max(w.q_lens), "T": T,
+                   "index_dtype": "nvfp4" if w.layers[0].index_dtype == 0 else "fp8", "layers": 1,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed by a 256 MB write before every timed step"},
+        "achieved_tbps": total_bytes / (ms_max * 1e-3) / 1e12,
+        "step_bytes": total_bytes, "step_frac_of_hbm_peak": total_bytes / (ms_max * 1e-3) / 1e9 / peak_gbs,
+        "stages_us": {"indexer": stage_ms[0] * 1e3, "topk": stage_ms[1] * 1e3, "attention": stage_ms[2] * 1e3},
+        "roofline": {"kernel": "k_indexer (msa_indexer_decode)", "bound": "hbm", "achieved": idx_gbs,
+                     "peak": peak_gbs, "unit": "GB/s", "frac": idx_gbs / peak_gbs,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes": idx_bytes,
+                     "traffic": recorded_traffic("k_indexer", "nvfp4_kv_cache_gb300/csrc/msa_indexer.cu")},
+        "e2e": {"value": e2e_ms * 1e3, "unit": "us/layer-step", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="spec", choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.CONFIGS[args.config]()
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", init_method="env://")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+/*
+ * msa.h — C ABI of the MiniMax Sparse Attention (MSA) decode step over a paged NVFP4 cache,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources named by page title and section):
+ *  - "vLLM ofrece soporte en día 0 para MiniMax-M3.1-Flash", section "MSA primer": the KV
+ *    cache is split into 128-token blocks; a light indexer scores every key of the context
+ *    with one index query per GQA group against one shared index-key head and max-pools the
+ *    scores to one per block; main attention then runs exactly over the top 16 blocks, the
+ *    most recent block always kept, so each query sees at most 2,048 keys.
+ *  - same page, "NVIDIA Blackwell optimizado kernes MSA": the KV cache is NVFP4 while the
+ *    queries stay FP8, so the kernels dequantise the cache to FP8 and run FP8 MMAs.
+ *  - "MiniMax M3 in vLLM: Day-0 Serving for 1M-Token Multimodal Reasoning", sections
+ *    "MSA 机制详解" (mechanism: init_blocks = 0, local_blocks = 1, partial last block masked,
+ *    causal boundary inside a block, local block not counted twice, per-request block
+ *    ranges), "解码执行" (decode: score, local window, top-k, sparse GQA, merge of split
+ *    partial outputs) and "解码内核中的推测解码" (uniform decode query length, tokens flattened
+ *    request-major, each mapped back to its request, sequence length, block table and causal
+ *    position; shape-stable launch grids for CUDA graphs).
+ *  - "MiniMax-M3.1-Flash serving notes", "The architecture, in operator terms" (64 query
+ *    heads, 4 KV heads, head dim 128) and "The capacity numbers" (NVFP4 = 4-bit values plus
+ *    one FP8 scale per 16 values, 4.5 bits per element).
+ *
+ * Conventions for every function:
+ *  - Pointers named device are CUDA device pointers; structs are passed by host pointer and
+ *    read during the call only. The caller allocates and owns every buffer; the library
+ *    allocates no memory and keeps no state between calls (it is re-entrant). Buffers must
+ *    not alias unless stated.
+ *  - Every call is asynchronous on the given stream and never synchronises the host, except
+ *    msa_read_device_status.
+ *  - Problems found on the host (null pointers, sizes, alignment, unsupported geometry)
+ *    return an error before anything is launched. A failed launch returns MSA_ERR_CUDA.
+ *    Problems only the device can see (a page id outside the cache, an inconsistent batch
+ *    description, a wait that ran out) set bits in a caller-provided device status word
+ *    (bit 1 << code, see msa_status) and never trap; the affected outputs are zero-filled
+ *    where stated.
+ *  - Launch grids depend only on the integer arguments (B, T, max_blocks_per_seq, sizes)
+ *    and on the device's SM count, never on device data, so a call can be captured in a CUDA
+ *    graph and replayed with new device contents.
+ *
+ * Byte layouts (this library's; the pages fix none):
+ *  - NVFP4 row of C elements (C % 16 == 0): C/2 code bytes and C/16 E4M3 scale bytes; scale
+ *    k covers elements 16k..16k+15 with value E2M1(code) * E4M3(scale). The code bytes are
+ *    little-endian 32-bit words; word w holds elements 8w..8w+7: element 8w+j keeps its three
+ *    E2M1 magnitude bits at bits 4j..4j+2 and its sign bit at bit 4*s(j)+3, with
+ *    s = (1, 3, 5, 7, 0, 2, 4, 6). (Every nibble still holds three magnitude bits and one
+ *    sign bit; placing the signs this way lets the dequantiser produce FP8 bytes in element
+ *    order with one byte-permute and one masked xor per four elements.)
+ *  - Index page (NVFP4): 128 rows x 64 code bytes, then 128 rows x 8 scale bytes = 9,216 B.
+ *    Index page (FP8): 128 rows x 128 E4M3 bytes = 16,384 B.
+ *  - KV page: [4 KV heads][K, V][128 rows x 64 code bytes, then 128 rows x 8 scale bytes]
+ *    = 73,728 B. Index and KV pages share the physical page id of the block table.
+ *  - Page arrays must be 256-byte aligned. Several block-table entries may name one page.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_ABI_VERSION 1
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or batch description */
+  MSA_ERR_UNSUPPORTED = 2,  /* a geometry or dtype this build does not implement */
+  MSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MSA_ERR_TIMEOUT = 4,      /* a device-side wait ran out of its time budget */
+  MSA_ERR_DEVICE_FAULT = 5  /* the device found a page id outside [0, num_pages) or an
+                               out-of-range selected block */
+} msa_status;
+
+/* Index-key cache dtypes: NVFP4 (72 B/token) or FP8 E4M3 (128 B/token, no scales). */
+enum { MSA_INDEX_NVFP4 = 0, MSA_INDEX_FP8 = 1 };
+
+/* The fixed MSA geometry of the method ("MSA primer"; "The architecture, in operator terms";
+ * "MSA 机制详解"): 64 query heads, 4 KV heads, head and index dim 128, 128-token blocks,
+ * 16 selected blocks of which 1 local block and 0 initial blocks. Any other value is
+ * rejected with MSA_ERR_UNSUPPORTED. */
+typedef struct msa_geometry {
+  int32_t num_q_heads;   /* 64 */
+  int32_t num_kv_heads;  /* 4 (= GQA groups; query head h belongs to group h / 16) */
+  int32_t head_dim;      /* 128 */
+  int32_t index_dim;     /* 128 */
+  int32_t block_size;    /* 128 */
+  int32_t topk;          /* 16, local block included */
+  int32_t local_blocks;  /* 1 */
+  int32_t init_blocks;   /* 0 */
+} msa_geometry;
+
+#define MSA_GEOMETRY_DEFAULT {64, 4, 128, 128, 128, 16, 1, 0}
+
+/* One decode batch, query tokens flattened request-major ("解码内核中的推测解码").
+ * Sequence b owns query tokens query_start_loc[b] .. query_start_loc[b+1]-1; its cache
+ * holds seq_lens[b] tokens including those query tokens, and its i-th query token sits at
+ * position seq_lens[b] - q_len_b + i and attends causally up to that position.
+ * All pointers are device pointers (int32). A sequence with q_len 0 (a padded request row)
+ * is skipped; a sequence with q_len > 0 needs seq_lens[b] >= q_len. */
+typedef struct msa_batch {
+  int32_t B;                       /* sequences */
+  int32_t T;                       /* query tokens, = query_start_loc[B] */
+  const int32_t* query_start_loc;  /* [B+1], device */
+  const int32_t* seq_lens;         /* [B], device */
+  const int32_t* block_table;      /* [B][max_blocks_per_seq] physical page ids, device */
+  int32_t max_blocks_per_seq;      /* row stride of block_table; seq_lens[b] <= 128 * this */
+  int32_t max_q_len;               /* upper bound on q_len, 1..8 */
+} msa_batch;
+
+/* The paged caches of one layer. */
+typedef struct msa_cache {
+  const uint8_t* kv_pages;     /* [num_pages][73,728 B], device, 256-B aligned */
+  const uint8_t* index_pages;  /* [num_pages][9,216 B (NVFP4) | 16,384 B (FP8)], device */
+  int32_t index_dtype;         /* MSA_INDEX_NVFP4 or MSA_INDEX_FP8 */
+  int32_t num_pages;           /* valid page ids are 0 .. num_pages-1 */
+} msa_cache;
+
+const char* msa_status_string(msa_status s);
+int32_t msa_abi_version(void);
+
+/* ---------------------------------------------------------------- cache producers ---- */
+
+/* NVFP4 quantisation ("The capacity numbers": 4-bit values plus one FP8 scale per 16).
+ * For each run of 16 elements of a row: s = E4M3 round-to-nearest-even, saturating, of
+ * amax/6 (fp32 division); S = E4M3 value of s; code_i = E2M1 round-to-nearest-even,
+ * saturating at 6, of x_i / S (fp32 division), zero magnitudes coded +0; S == 0 gives all
+ * codes 0. The amax/6 rule and the rounding modes are this library's reading (the pages
+ * leave them open).
+ *   x       [rows][cols] fp32, device, 16-B aligned, row stride cols; finite values
+ *   cols    multiple of 16
+ *   vals    device; row r's codes at vals + r * vals_row_stride (cols/2 bytes, stride % 4 == 0,
+ *           4-B aligned)
+ *   scales  device; row r's scales at scales + r * scales_row_stride (cols/16 bytes) */
+msa_status msa_quantize_nvfp4(const float* x, int64_t rows, int32_t cols, uint8_t* vals,
+                              int64_t vals_row_stride, uint8_t* scales,
+                              int64_t scales_row_stride, cudaStream_t stream);
+
+/* FP8 (E4M3) cast, round to nearest even, saturating to +-448, sign of zero kept.
+ * Used for queries, index queries and the FP8 index-key cache. x, out: [n], device. */
+msa_status msa_quantize_fp8(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
+
+/* Dequantise NVFP4 rows to the FP8 operand the MMAs see ("NVIDIA Blackwell optimizado
+ * kernes MSA"; the E4M3 re-rounding is the one "NVIDIA Rubin MSA optimizado" contrasts with
+ * exact FP16 scores): out = E4M3_rne_sat(E2M1(code) * E4M3(scale)), sign = sign(code) xor
+ * sign(scale), NaN scale -> 0x7F with that sign.
+ *   vals [rows] x (cols/2) bytes at vals_row_stride, scales [rows] x (cols/16) at
+ *   scales_row_stride, out [rows][cols] E4M3; all device; cols % 16 == 0. */
+msa_status msa_dequant_nvfp4(const uint8_t* vals, int64_t vals_row_stride,
+                             const uint8_t* scales, int64_t scales_row_stride, int64_t rows,
+                             int32_t cols, uint8_t* out, cudaStream_t stream);
+
+/* Paged cache insert: quantise n new tokens straight into their pages (the KV-insert step
+ * of "QKV GEMM + norm + RoPE + KV inserción fusión", without the GEMM, norm and RoPE).
+ *   k, v      [n][4][128] fp32, device, contiguous
+ *   ik        [n][128] fp32, device (index keys), may be NULL to skip the index cache
+ *   slots     [n] int64 device: physical page * 128 + row in page; -1 skips the token
+ *   kv_pages, index_pages: the caches (index_pages may be NULL when ik is NULL)
+ * Slots outside [0, num_pages * 128) set MSA_ERR_DEVICE_FAULT in *status (nullable) and
+ * are skipped. Two tokens must not name the same slot. */
+msa_status msa_kv_insert(const float* k, const float* v, const float* ik, int64_t n,
+                         const int64_t* slots, uint8_t* kv_pages, uint8_t* index_pages,
+                         int32_t index_dtype, int32_t num_pages, uint32_t* status,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------- the decode step ---- */
+
+/* Indexer score and block max-pool ("MSA primer"; "解码执行").
+ * block_scores[t][g][k] = max over the cache positions j of block k with j <= p_t of
+ * sum_d index_q[t][g][d] * ik_fp8[j][d], where ik_fp8 is the index key dequantised to E4M3
+ * as in msa_dequant_nvfp4 (the FP8 index cache is used as is) and p_t is token t's position;
+ * -inf for a block with no such j. Products are exact, sums are fp32.
+ *   index_q       [T][4][128] E4M3, device
+ *   block_scores  [T][4][max_blocks_per_seq] fp32, device; entries k >= the sequence's
+ *                 block count are not written
+ *   status        device uint32, nullable: bad page ids set bit MSA_ERR_DEVICE_FAULT (the
+ *                 page is then scored -inf), an inconsistent batch sets MSA_ERR_INVALID_ARG */
+msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch,
+                              const msa_cache* cache, const uint8_t* index_q,
+                              float* block_scores, uint32_t* status, cudaStream_t stream);
+
+/* Per-group block selection ("MSA primer"; "MSA 机制详解"). For token t at position p_t,
+ * local = p_t / 128. sel[t][g][0] = local; sel[t][g][1..15] = the 15 highest-scoring blocks
+ * among 0 .. local-1, in descending score order, equal scores ordered by lower block id
+ * first (NaN ranks as -inf, -0 equals +0); -1 pads when fewer than 15 exist.
+ *   block_scores  [T][4][max_blocks_per_seq] fp32, device (as written by the indexer)
+ *   sel           [T][4][16] int32, device */
+msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* batch,
+                           const float* block_scores, int32_t* sel, uint32_t* status,
+                           cudaStream_t stream);
+
+/* Workspace bytes msa_sparse_attn_decode needs for num_splits partial results per token
+ * (num_splits 0 = the automatic choice, which never exceeds 16). */
+size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, int32_t num_splits);
+
+/* Exact sparse GQA attention over the selected blocks ("MSA primer": exact attention over
+ * the selected blocks; "解码执行": split work merged from partial outputs). For query head h
+ * of token t (group g = h / 16): the keys are the cache positions j <= p_t of the distinct
+ * blocks listed in sel[t][g][0..15] (entries < 0 ignored); z_j = softmax_scale * q . k_j with
+ * K dequantised to E4M3; out = sum_j softmax(z)_j v_j with V dequantised to E4M3; written
+ * as bf16. QK^T runs as an FP8 MMA with fp32 accumulation; the softmax is fp32; PV runs
+ * with P in f16 and V widened exactly from E4M3 to f16.
+ *   q          [T][64][128] E4M3, device
+ *   sel        [T][4][16] int32, device
+ *   num_splits 0 = automatic; else 1..16 splits of each (sequence, group)'s block list,
+ *              merged by log-sum-exp
+ *   workspace  device, >= msa_attn_workspace_size(...) bytes (may be NULL when that is 0)
+ *   out        [T][64][128] bf16 (uint16 bit patterns), device
+ *   status     nullable; a selected block beyond the sequence or a bad page id sets
+ *              MSA_ERR_DEVICE_FAULT and the affected tokens' outputs are zero-filled */
+msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_batch* batch,
+                                  const msa_cache* cache, const uint8_t* q, const int32_t* sel,
+                                  float softmax_scale, int32_t num_splits, void* workspace,
+                                  size_t workspace_bytes, uint16_t* out, uint32_t* status,
+                                  cudaStream_t stream);
+
+/* Workspace bytes msa_decode_step needs (depends only on its arguments). */
+size_t msa_decode_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
+                                 int32_t max_blocks_per_seq);
+
+/* The whole decode step of one layer: indexer -> top-k -> sparse attention -> merge, all
+ * on `stream`. The workspace starts with the device status word, which the call clears
+ * first; read it with msa_read_device_status.
+ *   q, index_q        as for msa_sparse_attn_decode / msa_indexer_decode
+ *   dbg_block_scores  nullable [T][4][max_blocks_per_seq] fp32: when given, the scores are
+ *                     written there instead of into the workspace
+ *   dbg_sel           nullable [T][4][16] int32: likewise for the selection
+ *   workspace         device, >= msa_decode_workspace_size(...) bytes, 256-B aligned
+ *   out               [T][64][128] bf16, device */
+msa_status msa_decode_step(const msa_geometry* geo, const msa_batch* batch,
+                           const msa_cache* cache, const uint8_t* q, const uint8_t* index_q,
+                           float softmax_scale, float* dbg_block_scores, int32_t* dbg_sel,
+                           void* workspace, size_t workspace_bytes, uint16_t* out,
+                           cudaStream_t stream);
+
+/* Test and debugging helper: waits for `stream`, then returns the most severe code whose
+ * bit is set in the status word at the start of `workspace` (MSA_OK when none). */
+msa_status msa_read_device_status(const void* workspace, cudaStream_t stream);
+
+/* Self-test of the bounded device waits: launches one CTA that waits on a shared-memory
+ * barrier nobody arrives on, gives up after limit_ns nanoseconds of %globaltimer, sets
+ * MSA_ERR_TIMEOUT in *status (device) and returns. Faults nothing. */
+msa_status msa_selftest_wait_timeout(uint32_t* status, int64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -1,0 +1,239 @@
+"""Python binding of libmsa.so: the MSA decode step over a paged NVFP4 cache on GB300.
+
+Argument marshalling only: every function forwards torch tensors' device pointers and the
+current CUDA stream to the C ABI of the same name (include/msa.h), and raises MsaError on a
+non-OK status. All arithmetic runs in the library's CUDA kernels. There is no fallback:
+importing this package fails if libmsa.so has not been built (``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmsa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libmsa.so is not built ({LIB_PATH}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MSA_OK = 0
+MSA_ERR_INVALID_ARG = 1
+MSA_ERR_UNSUPPORTED = 2
+MSA_ERR_CUDA = 3
+MSA_ERR_TIMEOUT = 4
+MSA_ERR_DEVICE_FAULT = 5
+MSA_INDEX_NVFP4 = 0
+MSA_INDEX_FP8 = 1
+
+HEAD_DIM = 128
+GROUPS = 4
+Q_HEADS = 64
+BLOCK = 128
+K_SEL = 16
+INDEX_PAGE_BYTES = {MSA_INDEX_NVFP4: 9216, MSA_INDEX_FP8: 16384}
+KV_PAGE_BYTES = 73728
+
+
+class msa_geometry(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_q_heads", "num_kv_heads", "head_dim", "index_dim",
+                                               "block_size", "topk", "local_blocks", "init_blocks")]
+
+
+class msa_batch(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("query_start_loc", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("max_blocks_per_seq", ctypes.c_int32), ("max_q_len", ctypes.c_int32)]
+
+
+class msa_cache(ctypes.Structure):
+    _fields_ = [("kv_pages", ctypes.c_void_p), ("index_pages", ctypes.c_void_p), ("index_dtype", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
+
+
+GEOMETRY = msa_geometry(64, 4, 128, 128, 128, 16, 1, 0)
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_GP = ctypes.POINTER(msa_geometry)
+_BP = ctypes.POINTER(msa_batch)
+_CP = ctypes.POINTER(msa_cache)
+
+_SIGS = {
+    "msa_status_string": (ctypes.c_char_p, [_I32]),
+    "msa_abi_version": (_I32, []),
+    "msa_quantize_nvfp4": (_I32, [_P, _I64, _I32, _P, _I64, _P, _I64, _P]),
+    "msa_quantize_fp8": (_I32, [_P, _I64, _P, _P]),
+    "msa_dequant_nvfp4": (_I32, [_P, _I64, _P, _I64, _I64, _I32, _P, _P]),
+    "msa_kv_insert": (_I32, [_P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _P, _P]),
+    "msa_indexer_decode": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
+    "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
+    "msa_attn_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
+    "msa_sparse_attn_decode": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _SZ, _P, _P, _P]),
+    "msa_decode_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
+    "msa_decode_step": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
+    "msa_read_device_status": (_I32, [_P, _P]),
+    "msa_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class MsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {_lib.msa_status_string(code).decode()}")
+
+
+def _check(code: int, where: str) -> None:
+    if code != MSA_OK:
+        raise MsaError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+# ------------------------------------------------------------------ descriptors ----------
+class Batch:
+    """Decode batch: device int32 tensors + the msa_batch struct (keeps the tensors alive)."""
+
+    def __init__(self, query_start_loc: torch.Tensor, seq_lens: torch.Tensor, block_table: torch.Tensor,
+                 max_q_len: int, T: Optional[int] = None):
+        for n, t in (("query_start_loc", query_start_loc), ("seq_lens", seq_lens), ("block_table", block_table)):
+            _need(t, torch.int32, n)
+        self.query_start_loc, self.seq_lens, self.block_table = query_start_loc, seq_lens, block_table
+        self.B = int(seq_lens.numel())
+        self.T = int(T) if T is not None else int(query_start_loc[-1].item())
+        self.max_blocks = int(block_table.shape[1]) if block_table.dim() == 2 else 1
+        self.max_q_len = int(max_q_len)
+        self.c = msa_batch(self.B, self.T, query_start_loc.data_ptr(), seq_lens.data_ptr(), block_table.data_ptr(),
+                           self.max_blocks, self.max_q_len)
+
+
+class Cache:
+    """One layer's paged caches (uint8 device tensors) + the msa_cache struct."""
+
+    def __init__(self, kv_pages: torch.Tensor, index_pages: torch.Tensor, index_dtype: int, num_pages: int):
+        _need(kv_pages, torch.uint8, "kv_pages")
+        _need(index_pages, torch.uint8, "index_pages")
+        self.kv_pages, self.index_pages = kv_pages, index_pages
+        self.index_dtype, self.num_pages = int(index_dtype), int(num_pages)
+        self.c = msa_cache(kv_pages.data_ptr(), index_pages.data_ptr(), self.index_dtype, self.num_pages)
+
+    @staticmethod
+    def empty(num_pages: int, index_dtype: int, device="cuda") -> "Cache":
+        kv = torch.zeros(num_pages * KV_PAGE_BYTES, dtype=torch.uint8, device=device)
+        ix = torch.zeros(num_pages * INDEX_PAGE_BYTES[index_dtype], dtype=torch.uint8, device=device)
+        return Cache(kv, ix, index_dtype, num_pages)
+
+
+# ------------------------------------------------------------------ the C ABI ------------
+def msa_abi_version() -> int:
+    return int(_lib.msa_abi_version())
+
+
+def msa_status_string(code: int) -> str:
+    return _lib.msa_status_string(code).decode()
+
+
+def msa_quantize_nvfp4(x: torch.Tensor, vals: torch.Tensor, scales: torch.Tensor,
+                       vals_row_stride: Optional[int] = None, scales_row_stride: Optional[int] = None) -> None:
+    _need(x, torch.float32, "x")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    _check(_lib.msa_quantize_nvfp4(_ptr(x), rows, cols, _ptr(vals), vals_row_stride or cols // 2, _ptr(scales),
+                                   scales_row_stride or cols // 16, _stream()), "msa_quantize_nvfp4")
+
+
+def msa_quantize_fp8(x: torch.Tensor, out: torch.Tensor) -> None:
+    _need(x, torch.float32, "x")
+    _check(_lib.msa_quantize_fp8(_ptr(x), x.numel(), _ptr(out), _stream()), "msa_quantize_fp8")
+
+
+def msa_dequant_nvfp4(vals: torch.Tensor, scales: torch.Tensor, out: torch.Tensor) -> None:
+    cols = vals.shape[-1] * 2
+    rows = vals.numel() // vals.shape[-1]
+    _check(_lib.msa_dequant_nvfp4(_ptr(vals), cols // 2, _ptr(scales), cols // 16, rows, cols, _ptr(out), _stream()),
+           "msa_dequant_nvfp4")
+
+
+def msa_kv_insert(k: torch.Tensor, v: torch.Tensor, ik: Optional[torch.Tensor], slots: torch.Tensor, cache: Cache,
+                  status: Optional[torch.Tensor] = None) -> None:
+    _need(k, torch.float32, "k")
+    _need(v, torch.float32, "v")
+    _need(slots, torch.int64, "slots")
+    n = int(slots.numel())
+    _check(_lib.msa_kv_insert(_ptr(k), _ptr(v), _ptr(ik), n, _ptr(slots), _ptr(cache.kv_pages),
+                              _ptr(cache.index_pages), cache.index_dtype, cache.num_pages, _ptr(status), _stream()),
+           "msa_kv_insert")
+
+
+def msa_indexer_decode(batch: Batch, cache: Cache, index_q: torch.Tensor, block_scores: torch.Tensor,
+                       status: Optional[torch.Tensor] = None) -> None:
+    _check(_lib.msa_indexer_decode(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                   _ptr(index_q), _ptr(block_scores), _ptr(status), _stream()),
+           "msa_indexer_decode")
+
+
+def msa_topk_blocks(batch: Batch, block_scores: torch.Tensor, sel: torch.Tensor,
+                    status: Optional[torch.Tensor] = None) -> None:
+    _check(_lib.msa_topk_blocks(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(block_scores), _ptr(sel),
+                                _ptr(status), _stream()), "msa_topk_blocks")
+
+
+def msa_attn_workspace_size(B: int, T: int, num_splits: int = 0) -> int:
+    return int(_lib.msa_attn_workspace_size(ctypes.byref(GEOMETRY), B, T, num_splits))
+
+
+def msa_sparse_attn_decode(batch: Batch, cache: Cache, q: torch.Tensor, sel: torch.Tensor, softmax_scale: float,
+                           out: torch.Tensor, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.msa_sparse_attn_decode(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(q),
+                                       _ptr(sel), float(softmax_scale), num_splits, _ptr(workspace), ws_bytes,
+                                       _ptr(out), _ptr(status), _stream()), "msa_sparse_attn_decode")
+
+
+def msa_decode_workspace_size(B: int, T: int, max_blocks_per_seq: int) -> int:
+    return int(_lib.msa_decode_workspace_size(ctypes.byref(GEOMETRY), B, T, max_blocks_per_seq))
+
+
+def msa_decode_step(batch: Batch, cache: Cache, q: torch.Tensor, index_q: torch.Tensor, softmax_scale: float,
+                    workspace: torch.Tensor, out: torch.Tensor, dbg_block_scores: Optional[torch.Tensor] = None,
+                    dbg_sel: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.msa_decode_step(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(q),
+                                _ptr(index_q), float(softmax_scale), _ptr(dbg_block_scores), _ptr(dbg_sel),
+                                _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)), "msa_decode_step")
+
+
+def msa_read_device_status(workspace: torch.Tensor) -> int:
+    return int(_lib.msa_read_device_status(_ptr(workspace), _stream()))
+
+
+def msa_selftest_wait_timeout(status: torch.Tensor, limit_ns: int) -> None:
+    _check(_lib.msa_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream()), "msa_selftest_wait_timeout")
+
+
+def status_bits(status: torch.Tensor) -> int:
+    """Bits of a device status word (1 << msa_status code)."""
+    return int(status.view(torch.int32)[0].item()) & 0xFFFFFFFF

@@ -1,0 +1,116 @@
+// msa_api.cu — the fused decode step, workspace sizing, device status and self-test entry
+// points of the C ABI (include/msa.h).
+//
+// msa_decode_step runs the three stages of the MSA decode step ("vLLM ofrece soporte en día 0
+// para MiniMax-M3.1-Flash", "MSA primer"; "MiniMax M3 in vLLM ...", "解码执行": score the
+// candidate blocks, apply the local window, select the top blocks, run sparse GQA decode and
+// merge split partial outputs) on one stream, with every intermediate in the caller's
+// workspace and launch shapes that depend only on the integer arguments (CUDA-graph safe,
+// "解码内核中的推测解码").
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+#include "msa_device.cuh"
+#include "msa_host.h"
+
+namespace msa {
+namespace {
+
+__global__ void k_wait_selftest(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nobody ever arrives on `bar`: the bounded wait must give up and report it
+    if (!mbar_wait_bounded(&bar, 0u, limit_ns, &abort_flag)) set_status(status, MSA_ERR_TIMEOUT);
+  }
+}
+
+struct WsLayout {
+  size_t scores, sel, attn, total;
+};
+
+WsLayout decode_layout(int B, int T, int maxb) {
+  using msa_host::align256;
+  WsLayout w;
+  w.scores = 256;
+  w.sel = w.scores + align256(static_cast<size_t>(T) * 4 * maxb * sizeof(float));
+  w.attn = w.sel + align256(static_cast<size_t>(T) * 4 * kSel * sizeof(int32_t));
+  msa_geometry geo = MSA_GEOMETRY_DEFAULT;
+  w.total = w.attn + msa_attn_workspace_size(&geo, B, T, 0);
+  return w;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+using namespace msa_host;
+
+extern "C" const char* msa_status_string(msa_status s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARG: return "MSA_ERR_INVALID_ARG: bad pointer, size, alignment or batch description";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED: geometry or dtype not implemented";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA: a CUDA call or launch failed";
+    case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT: a device-side wait ran out of time";
+    case MSA_ERR_DEVICE_FAULT: return "MSA_ERR_DEVICE_FAULT: page id or selected block out of range";
+  }
+  return "unknown msa_status";
+}
+
+extern "C" int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+extern "C" size_t msa_decode_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
+                                            int32_t max_blocks_per_seq) {
+  if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || max_blocks_per_seq < 1) return 0;
+  return decode_layout(B, T, max_blocks_per_seq).total;
+}
+
+extern "C" msa_status msa_decode_step(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                      const uint8_t* q, const uint8_t* index_q, float softmax_scale,
+                                      float* dbg_block_scores, int32_t* dbg_sel, void* workspace,
+                                      size_t workspace_bytes, uint16_t* out, cudaStream_t stream) {
+  msa_status st = check_geometry(geo);
+  if (st != MSA_OK) return st;
+  if ((st = check_batch(batch)) != MSA_OK) return st;
+  if ((st = check_cache(cache, true, true)) != MSA_OK) return st;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MSA_ERR_INVALID_ARG;
+  const WsLayout w = decode_layout(batch->B, batch->T, batch->max_blocks_per_seq);
+  if (workspace_bytes < w.total) return MSA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return MSA_ERR_CUDA;
+  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  float* scores = dbg_block_scores != nullptr ? dbg_block_scores : reinterpret_cast<float*>(ws + w.scores);
+  int32_t* sel = dbg_sel != nullptr ? dbg_sel : reinterpret_cast<int32_t*>(ws + w.sel);
+  if ((st = msa_indexer_decode(geo, batch, cache, index_q, scores, status, stream)) != MSA_OK) return st;
+  if ((st = msa_topk_blocks(geo, batch, scores, sel, status, stream)) != MSA_OK) return st;
+  return msa_sparse_attn_decode(geo, batch, cache, q, sel, softmax_scale, 0, ws + w.attn, w.total - w.attn, out,
+                                status, stream);
+}
+
+extern "C" msa_status msa_read_device_status(const void* workspace, cudaStream_t stream) {
+  if (workspace == nullptr) return MSA_ERR_INVALID_ARG;
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_ERR_CUDA;
+  const msa_status order[] = {MSA_ERR_DEVICE_FAULT, MSA_ERR_TIMEOUT, MSA_ERR_INVALID_ARG, MSA_ERR_CUDA,
+                              MSA_ERR_UNSUPPORTED};
+  for (msa_status s : order)
+    if (bits & (1u << s)) return s;
+  return MSA_OK;
+}
+
+extern "C" msa_status msa_selftest_wait_timeout(uint32_t* status, int64_t limit_ns, cudaStream_t stream) {
+  if (status == nullptr || limit_ns < 0 || !aligned(status, 4)) return MSA_ERR_INVALID_ARG;
+  k_wait_selftest<<<1, 32, 0, stream>>>(status, static_cast<unsigned long long>(limit_ns));
+  return launch_status();
+}

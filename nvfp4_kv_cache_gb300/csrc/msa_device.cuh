@@ -1,0 +1,265 @@
+// msa_device.cuh — device-side building blocks of the MSA decode kernels (sm_103a).
+//
+// PTX wrappers (mbarrier, 1-D bulk async copies, mma.sync, ldmatrix, FP8 converts), the
+// bounded waits every kernel uses, and the NVFP4 -> E4M3 dequantiser: a 2 KB shared-memory
+// table of pre-rounded FP8 values indexed by (scale byte, E2M1 magnitude) — the table idea
+// of "vLLM ofrece soporte en día 0 para MiniMax-M3.1-Flash", section "NVFP4 MSA kernel" —
+// read with one byte-permute per four elements and a masked xor for the signs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+// ------------------------------------------------------------------ fixed geometry ----
+constexpr int kD = 128;          // head dim = index dim
+constexpr int kGroups = 4;       // KV heads
+constexpr int kHPG = 16;         // query heads per group
+constexpr int kQHeads = 64;
+constexpr int kBS = 128;         // tokens per block = page rows
+constexpr int kSel = 16;         // selected blocks per (token, group)
+constexpr int kMaxQLen = 8;
+constexpr int kRowCodes = kD / 2;    // 64 B
+constexpr int kRowScales = kD / 16;  // 8 B
+constexpr int kRegion = kBS * (kRowCodes + kRowScales);  // 9,216 B: codes of 128 rows, scales
+constexpr int kScaleOff = kBS * kRowCodes;               // 8,192: scales start in a region
+constexpr int kIdxPageNv = kRegion;
+constexpr int kIdxPageFp8 = kBS * kD;                    // 16,384 B
+constexpr int kKvPage = kGroups * 2 * kRegion;           // 73,728 B
+constexpr int kMaxSplits = 16;
+constexpr int kMaxB = 4096;      // sequences per call (shared-memory prefix sums)
+
+// Default budget of every device-side wait; a correct run never gets near it.
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ void set_status(uint32_t* status, int code) {
+  if (status != nullptr) atomicOr(status, 1u << code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier ----------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete. Gives up (returns false)
+// after limit_ns of %globaltimer, or early when *abort becomes non-zero.
+static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
+                                               volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ bulk copies -------
+// 1-D bulk copy global -> shared, completing `bytes` of transaction count on `bar`.
+// src and dst 16-B aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 evict-first hint for data streamed exactly once.
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ------------------------------------------------------------------ loads -------------
+// Shared-memory loads as plain C++ so the compiler orders them against barriers and can
+// still schedule them freely around the (non-volatile) MMAs.
+__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+
+__device__ __forceinline__ uint2 ldg_nc64(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ MMAs --------------
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col)
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p))
+               : "memory");
+}
+
+// ------------------------------------------------------------------ conversions -------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two fp32 -> two E4M3 bytes (round to nearest even, saturating): lo in bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 bytes (bits 0..15) -> f16x2, exact.
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t in = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+  return r;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  const uint32_t h2 = cvt_f16x2_e4m3x2(byte & 0xFFu);
+  float f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ NVFP4 codec -------
+// E2M1 magnitudes by code 0..7 (the FP4 format definition).
+__device__ __forceinline__ float e2m1_mag(int c) {
+  return c < 4 ? 0.5f * static_cast<float>(c) : (c == 4 ? 2.0f : (c == 5 ? 3.0f : (c == 6 ? 4.0f : 6.0f)));
+}
+
+// E2M1 magnitude code of a >= 0: round to nearest, ties to the even code, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1_code(float a) {
+  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) + static_cast<uint32_t>(a > 1.25f) +
+         static_cast<uint32_t>(a >= 1.75f) + static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
+         static_cast<uint32_t>(a > 5.0f);
+}
+
+// Sign slot of element j (0..7) inside its 32-bit code word.
+__host__ __device__ constexpr int sign_slot(int j) { return j < 4 ? 2 * j + 1 : 2 * (j - 4); }
+
+// Fill the 256-entry dequant table: lut[s] holds, for magnitudes 0..7, the E4M3 byte of
+// |E2M1(m)| * |E4M3(s)| rounded to nearest even with saturation, with the sign of s in
+// bit 7 (0x7F for a NaN scale). One 8-byte entry per scale byte: 2 KB.
+__device__ __forceinline__ void build_dequant_lut(uint2* lut, int tid, int nthreads) {
+  for (int s = tid; s < 256; s += nthreads) {
+    const uint32_t mag = static_cast<uint32_t>(s) & 0x7Fu;
+    const uint32_t sgn = (static_cast<uint32_t>(s) & 0x80u) ? 0x80808080u : 0u;
+    uint32_t lo, hi;
+    if (mag == 0x7Fu) {
+      lo = hi = 0x7F7F7F7Fu;
+    } else {
+      const float S = e4m3_to_f32(mag);
+      lo = cvt_e4m3x2(e2m1_mag(0) * S, e2m1_mag(1) * S) | (cvt_e4m3x2(e2m1_mag(2) * S, e2m1_mag(3) * S) << 16);
+      hi = cvt_e4m3x2(e2m1_mag(4) * S, e2m1_mag(5) * S) | (cvt_e4m3x2(e2m1_mag(6) * S, e2m1_mag(7) * S) << 16);
+    }
+    lut[s] = make_uint2(lo | sgn, hi | sgn);
+  }
+}
+
+// Dequantise one code word (8 elements, this library's layout) with the table entry of
+// its scale: lo = E4M3 bytes of elements 0..3, hi = elements 4..7, in element order.
+__device__ __forceinline__ void dq8(uint32_t w, uint2 e, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w & 0x77777777u;
+  lo = prmt(e.x, e.y, x) ^ (w & 0x80808080u);
+  hi = prmt(e.x, e.y, x >> 16) ^ ((w << 4) & 0x80808080u);
+}
+
+// ------------------------------------------------------------------ misc ---------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace msa

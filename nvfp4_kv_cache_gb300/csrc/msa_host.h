@@ -1,0 +1,71 @@
+// msa_host.h — host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa_host {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Status of the launches issued since the last check.
+inline msa_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+inline msa_status check_geometry(const msa_geometry* g) {
+  if (g == nullptr) return MSA_ERR_INVALID_ARG;
+  if (g->num_q_heads != 64 || g->num_kv_heads != 4 || g->head_dim != 128 || g->index_dim != 128 ||
+      g->block_size != 128 || g->topk != 16 || g->local_blocks != 1 || g->init_blocks != 0)
+    return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+inline msa_status check_batch(const msa_batch* b) {
+  if (b == nullptr) return MSA_ERR_INVALID_ARG;
+  if (b->B < 0 || b->T < 0 || b->B > 4096) return MSA_ERR_INVALID_ARG;
+  if (b->max_q_len < 1 || b->max_q_len > 8) return MSA_ERR_INVALID_ARG;
+  if (b->max_blocks_per_seq < 1 || b->max_blocks_per_seq > (1 << 20)) return MSA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(b->T) > static_cast<int64_t>(b->B) * b->max_q_len) return MSA_ERR_INVALID_ARG;
+  if (b->B > 0 && (b->query_start_loc == nullptr || b->seq_lens == nullptr || b->block_table == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned(b->query_start_loc, 4) || !aligned(b->seq_lens, 4) || !aligned(b->block_table, 4))
+    return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+inline msa_status check_cache(const msa_cache* c, bool need_index, bool need_kv) {
+  if (c == nullptr) return MSA_ERR_INVALID_ARG;
+  if (c->num_pages < 0) return MSA_ERR_INVALID_ARG;
+  if (c->index_dtype != MSA_INDEX_NVFP4 && c->index_dtype != MSA_INDEX_FP8) return MSA_ERR_UNSUPPORTED;
+  if (need_index && (c->index_pages == nullptr || !aligned(c->index_pages, 256))) return MSA_ERR_INVALID_ARG;
+  if (need_kv && (c->kv_pages == nullptr || !aligned(c->kv_pages, 256))) return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Splits of the attention work per (sequence, group) chosen from B alone (so workspace sizes
+// are a pure function of the arguments): enough CTAs for about two per SM of a 152-SM GB300.
+inline int auto_splits(int B) {
+  const int items = 4 * B;
+  if (items <= 0 || items >= 152) return 1;
+  int s = (304 + items - 1) / items;
+  return s > 16 ? 16 : s;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace msa_host
+
+// Launchers implemented in the kernel translation units.
+msa_status msa_launch_attn_merge(const float* part_o, const float* part_lse, int32_t splits, int32_t T,
+                                 uint16_t* out, cudaStream_t stream);

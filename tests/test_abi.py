@@ -1,0 +1,73 @@
+"""The C-ABI library loads and exports every function include/msa.h declares; host-side
+argument checks reject bad calls before anything is launched (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_kv_cache_gb300 import _build
+
+    return ctypes.CDLL(_build.build())
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("msa_quantize_nvfp4", "msa_indexer_decode", "msa_topk_blocks", "msa_sparse_attn_decode",
+              "msa_decode_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.msa_status_string.restype = ctypes.c_char_p
+    for code in range(6):
+        assert lib.msa_status_string(code).startswith(b"MSA_")
+    assert lib.msa_abi_version() == 1
+
+
+def test_host_checks_without_gpu(lib):
+    # rows < 0, cols not a multiple of 16, null pointers: rejected before any CUDA call
+    f = lib.msa_quantize_nvfp4
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    assert f(None, -1, 128, None, 64, None, 8, None) == 1
+    assert f(None, 4, 100, None, 64, None, 8, None) == 1
+    assert f(None, 4, 128, None, 64, None, 8, None) == 1
+    assert f(None, 0, 128, None, 64, None, 8, None) == 0  # nothing to do
+
+    class Geo(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int32) for n in "abcdefgh"]
+
+    bad = Geo(64, 8, 128, 128, 128, 16, 1, 0)  # 8 KV heads: not this method's geometry
+    good = Geo(64, 4, 128, 128, 128, 16, 1, 0)
+    ws = lib.msa_decode_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.POINTER(Geo), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+    assert ws(ctypes.byref(bad), 4, 4, 32) == 0
+    n = ws(ctypes.byref(good), 64, 512, 1024)
+    # header + scores [T,4,maxb] f32 + sel [T,4,16] i32 (+ no split partials at B=64)
+    assert n == 256 + 512 * 4 * 1024 * 4 + 512 * 4 * 16 * 4
+    n1 = ws(ctypes.byref(good), 1, 1, 32)
+    assert n1 > 256 + 1 * 4 * 32 * 4  # B=1 splits its work: partials need room
+    g = lib.msa_topk_blocks
+    g.argtypes = [ctypes.POINTER(Geo), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    assert g(ctypes.byref(bad), None, None, None, None, None) == 2
+    assert g(ctypes.byref(good), None, None, None, None, None) == 1

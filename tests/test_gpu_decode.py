@@ -1,0 +1,199 @@
+"""GPU parity of the decode step (indexer -> top-k -> sparse attention) on small cases the
+oracle finishes in seconds: ragged lengths with partial last blocks, 1..8 query tokens per
+sequence, hot blocks, both index-cache dtypes, padded request rows, and every split count."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity import OracleSeq, check_attention, check_scores, check_selection
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "ragged": dict(seq_lens=[1000, 4096 + 77, 300], q_lens=[1, 8, 3], seed=21),
+    "hot": dict(seq_lens=[6000, 9000 + 5], q_lens=[8, 2], seed=22, hot=12),
+    "fp8_index": dict(seq_lens=[3000, 5000, 129], q_lens=[4, 1, 2], seed=23, index_dtype=1),
+    "dense": dict(seq_lens=[2048, 1500, 130], q_lens=[1, 5, 2], seed=24),
+    "padded": dict(seq_lens=[4000, 0, 2500, 700, 1], q_lens=[2, 0, 0, 1, 1], seed=25),
+    "many": dict(seq_lens=[129 * k + 17 for k in range(1, 20)], q_lens=[(k % 8) + 1 for k in range(19)], seed=26),
+}
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import nvfp4_kv_cache_gb300 as m
+
+    return m
+
+
+def run_step(msa, dl, num_splits=None):
+    o = dl.outputs()
+    ws = dl.workspace()
+    msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"], o["scores"], o["sel"])
+    st = msa.msa_read_device_status(ws)
+    return o, st
+
+
+def compare_case(w, dl, o, device="cuda", seqs=None):
+    from workloads.device import bf16_to_f32
+
+    qsl = w.query_start_loc()
+    scores = o["scores"].cpu().numpy()
+    sel = o["sel"].cpu().numpy()
+    out = bf16_to_f32(o["out"]).cpu().numpy()
+    stats = []
+    for b in (range(w.B) if seqs is None else seqs):
+        ql, L = w.q_lens[b], w.seq_lens[b]
+        if ql == 0:
+            continue
+        nb = (L + 127) // 128
+        rows = slice(qsl[b], qsl[b] + ql)
+        gsel = sel[rows]
+        ref = OracleSeq(w, 0, b, device, kv_blocks=np.unique(gsel[gsel >= 0]))
+        rs = ref.scores()
+        gs = scores[rows, :, :nb]
+        check_scores(gs, rs, f"seq {b}")
+        check_selection(gsel, gs, rs, L, ql, f"seq {b}")
+        ro = ref.attention(gsel, 1.0 / np.sqrt(128.0))
+        stats.append(check_attention(out[rows], ro, f"seq {b}"))
+    return stats
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_decode_step_matches_oracle(msa, case):
+    from workloads.device import DeviceLayer
+
+    w = W.small(case, **CASES[case])
+    dl = DeviceLayer(w, 0)
+    o, st = run_step(msa, dl)
+    assert st == msa.MSA_OK
+    compare_case(w, dl, o)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
+def test_standalone_stages_and_splits(msa, splits):
+    """indexer, top-k and attention called one by one (any split count) == the fused step."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("ragged", **CASES["ragged"])
+    dl = DeviceLayer(w, 0)
+    o, st = run_step(msa, dl)
+    assert st == msa.MSA_OK
+    T = w.T
+    scores = torch.full((T, 4, dl.batch.max_blocks), float("nan"), device="cuda")
+    sel = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((T, 64, 128), dtype=torch.uint16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_indexer_decode(dl.batch, dl.cache, dl.iq8, scores, status)
+    msa.msa_topk_blocks(dl.batch, scores, sel, status)
+    nbytes = msa.msa_attn_workspace_size(w.B, T, splits)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    msa.msa_sparse_attn_decode(dl.batch, dl.cache, dl.q8, sel, dl.softmax_scale, out, splits, ws, status)
+    torch.cuda.synchronize()
+    assert msa.status_bits(status) == 0
+    qsl = w.query_start_loc()
+    for b in range(w.B):
+        nb = (w.seq_lens[b] + 127) // 128
+        r = slice(qsl[b], qsl[b + 1])
+        assert torch.equal(scores[r, :, :nb], o["scores"][r, :, :nb])
+    assert torch.equal(sel, o["sel"])
+    a, b_ = bf16_to_f32(out), bf16_to_f32(o["out"])
+    rel = (a - b_).norm() / b_.norm()
+    assert rel < 2e-3, float(rel)  # splits change only the summation order (and bf16 rounding)
+    compare_case(w, dl, dict(out=out, scores=o["scores"], sel=sel))
+
+
+def test_topk_on_crafted_scores(msa):
+    """Ties, NaN, -inf, -0/+0, fewer than 15 candidates: GPU == the oracle's stable sort."""
+    rng = np.random.default_rng(5)
+    seq_lens = [128 * 700 + 3, 128 * 3 + 1, 128 * 16, 5, 128 * 4096]
+    q_lens = [3, 1, 2, 1, 1]
+    B = len(seq_lens)
+    maxb = 4096
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(qsl[-1])
+    scores = rng.integers(-4, 5, size=(T, 4, maxb)).astype(np.float32)
+    scores[0, 0, rng.integers(0, 700, 50)] = np.nan
+    scores[0, 1, rng.integers(0, 700, 50)] = -np.inf
+    scores[1, 2, :] = 0.0
+    scores[1, 2, ::2] = -0.0
+    scores[2, 3, :] = rng.standard_normal(maxb)
+    scores[5:, :, :] = rng.standard_normal((T - 5, 4, maxb))
+    scores[7, 0, :] = 7.0  # all equal over 4,095 candidates
+    bt = torch.zeros((B, maxb), dtype=torch.int32, device="cuda")
+    batch = msa.Batch(torch.from_numpy(qsl).cuda(), torch.tensor(seq_lens, dtype=torch.int32, device="cuda"), bt,
+                      max_q_len=8)
+    sd = torch.from_numpy(scores).cuda()
+    sel = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+    msa.msa_topk_blocks(batch, sd, sel)
+    got = sel.cpu().numpy()
+    for b in range(B):
+        L, ql = seq_lens[b], q_lens[b]
+        for i in range(ql):
+            t = qsl[b] + i
+            local = (L - ql + i) // 128
+            for g in range(4):
+                want = oracle.select_row(scores[t, g].astype(np.float64), local)
+                assert np.array_equal(got[t, g], want), (b, i, g)
+
+
+def test_paging_invariance(msa):
+    """Identity vs permuted block tables: bit-identical scores, selection and output."""
+    from workloads.device import DeviceLayer
+
+    kw = dict(seq_lens=[5000, 3000 + 11, 777], q_lens=[4, 8, 1], seed=31, hot=8)
+    outs = []
+    for identity in (True, False):
+        w = W.small("paging", identity=identity, **kw)
+        dl = DeviceLayer(w, 0)
+        o, st = run_step(msa, dl)
+        assert st == msa.MSA_OK
+        outs.append(o)
+    for key in ("sel", "out"):
+        assert torch.equal(outs[0][key], outs[1][key]), key
+
+
+def test_shared_prefix_pages(msa):
+    """Sequences sharing the physical pages of a prefix read the same bytes."""
+    from workloads.device import DeviceLayer
+
+    w = W.small("prefix", [16384 + 1000, 16384 + 5, 20000], [3, 1, 2], seed=32, prefix_len=16384, prefix_seqs=2)
+    dl = DeviceLayer(w, 0)
+    o, st = run_step(msa, dl)
+    assert st == msa.MSA_OK
+    compare_case(w, dl, o)
+
+
+def test_cuda_graph_replay(msa):
+    """The decode step captured once replays with new device contents."""
+    from workloads.device import DeviceLayer
+
+    w = W.small("graph", [3000, 4100], [2, 5], seed=33)
+    dl = DeviceLayer(w, 0)
+    o = dl.outputs()
+    ws = dl.workspace()
+    msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"], o["scores"], o["sel"])
+    torch.cuda.synchronize()
+    eager = o["out"].clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"], o["scores"],
+                                o["sel"])
+    torch.cuda.current_stream().wait_stream(s)
+    o["out"].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o["out"], eager)
+    # new query contents, same graph
+    dl.q8.copy_(torch.roll(dl.q8, 1, dims=1))
+    g.replay()
+    torch.cuda.synchronize()
+    o2 = dl.outputs()
+    msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, dl.workspace(), o2["out"])
+    torch.cuda.synchronize()
+    assert torch.equal(o["out"], o2["out"])

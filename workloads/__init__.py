@@ -204,13 +204,14 @@ def make(name: str, seq_lens, q_lens, seed: int, index_dtype: int = INDEX_NVFP4,
     q_lens = [int(x) for x in q_lens]
     nb = [(L + BLOCK - 1) // BLOCK for L in seq_lens]
     assert prefix_len % BLOCK == 0
-    table, total = _paging(nb, rng, identity, prefix_len // BLOCK, prefix_seqs)
+    # content choices first, so the block table (identity or permuted) changes nothing else
     hot_blocks = _hot(nb, q_lens, seq_lens, hot, rng) if hot else [np.zeros(0, np.int64)] * len(nb)
     ko = vo = None
     if outlier_frac > 0:
         n = int(round(outlier_frac * GROUPS * HEAD_DIM))
         ko = np.sort(rng.choice(GROUPS * HEAD_DIM, size=n, replace=False))
         vo = np.sort(rng.choice(GROUPS * HEAD_DIM, size=n, replace=False))
+    table, total = _paging(nb, rng, identity, prefix_len // BLOCK, prefix_seqs)
     dtypes = layer_dtypes or [index_dtype] * n_layers
     seeds = layer_seeds or [seed + 1000 * l for l in range(n_layers)]
     layers = [Layer(seed=int(s), index_dtype=int(d)) for s, d in zip(seeds, dtypes)]

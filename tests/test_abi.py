@@ -18,9 +18,9 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from nvfp4_kv_cache_gb300 import _build
+    import __graft_entry__
 
-    return ctypes.CDLL(_build.build())
+    return ctypes.CDLL(__graft_entry__._load_builder().build())
 
 
 def test_header_declares_the_boundary():

@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import workloads as W
+from parity import OracleSeq, check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -53,10 +54,14 @@ def test_bad_page_id_is_reported_and_zero_filled(msa):
     assert np.isneginf(s[0:2, :, 3]).all()
     out = bf16_to_f32(o["out"])
     assert (out[2] == 0).all(), "tokens whose selected page is bad are zero-filled"
-    # sequence 0 never selects the -inf block, so its output is unchanged
+    # sequence 0 never selects the -inf block; its other scores are unchanged and its output
+    # is the oracle's attention over its (new) selection
     sel0 = o["sel"][0:2].cpu().numpy()
     assert not (sel0 == 3).any()
-    assert torch.equal(o["out"][0:2], good["out"][0:2])
+    keep = [k for k in range(24) if k != 3]
+    assert torch.equal(o["scores"][0:2, :, keep], good["scores"][0:2, :, keep])
+    ref = OracleSeq(w, 0, 0, "cuda", kv_blocks=np.unique(sel0))
+    check_attention(out[0:2].cpu().numpy(), ref.attention(sel0, dl.softmax_scale), "seq 0")
 
 
 def test_selected_block_out_of_range(msa):

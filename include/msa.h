@@ -218,6 +218,31 @@ msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_batch* batc
                                   size_t workspace_bytes, uint16_t* out, uint32_t* status,
                                   cudaStream_t stream);
 
+/* Allocation-free form of msa_sparse_attn_decode (no counterpart on the pages; this is an
+ * interface addition for callers that cannot allocate device memory, e.g. a host runtime
+ * whose memory is planned once with no allocator to hand down, or code running inside
+ * another library's callback where a cudaMalloc would synchronise the device). Same
+ * arguments and results as msa_sparse_attn_decode without the workspace: the split partial
+ * results go to one file-scope device array of msa_noalloc_scratch_bytes() bytes (16 MiB),
+ * which every GPU that loads the library keeps until the process exits.
+ *  - Needs at most splits * T * 64 * 129 * 4 bytes (rounded up to 256-B pieces); larger
+ *    requests return MSA_ERR_INVALID_ARG before anything is launched (num_splits = 1 needs
+ *    no scratch at all).
+ *  - Calls no cudaMalloc / cudaFree. The first call on a device looks up the array's device
+ *    address (cudaGetSymbolAddress) once for that device, so make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents (nothing in it
+ *    needs to start at zero: each call writes every partial it reads). Calls whose kernels
+ *    overlap on the GPU (other streams, other threads) race on it and must be serialised by
+ *    the caller. */
+msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_batch* batch,
+                                          const msa_cache* cache, const uint8_t* q, const int32_t* sel,
+                                          float softmax_scale, int32_t num_splits, uint16_t* out,
+                                          uint32_t* status, cudaStream_t stream);
+
+/* Size in bytes of the device array msa_sparse_attn_decode_noalloc uses. */
+size_t msa_noalloc_scratch_bytes(void);
+
 /* Workspace bytes msa_decode_step needs (depends only on its arguments). */
 size_t msa_decode_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
                                  int32_t max_blocks_per_seq);

@@ -76,6 +76,8 @@ _SIGS = {
     "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
     "msa_attn_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_sparse_attn_decode": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _SZ, _P, _P, _P]),
+    "msa_sparse_attn_decode_noalloc": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _P, _P]),
+    "msa_noalloc_scratch_bytes": (_SZ, []),
     "msa_decode_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_decode_step": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
     "msa_read_device_status": (_I32, [_P, _P]),
@@ -211,6 +213,20 @@ def msa_sparse_attn_decode(batch: Batch, cache: Cache, q: torch.Tensor, sel: tor
     _check(_lib.msa_sparse_attn_decode(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(q),
                                        _ptr(sel), float(softmax_scale), num_splits, _ptr(workspace), ws_bytes,
                                        _ptr(out), _ptr(status), _stream()), "msa_sparse_attn_decode")
+
+
+def msa_sparse_attn_decode_noalloc(batch: Batch, cache: Cache, q: torch.Tensor, sel: torch.Tensor,
+                                   softmax_scale: float, out: torch.Tensor, num_splits: int = 0,
+                                   status: Optional[torch.Tensor] = None) -> None:
+    """msa_sparse_attn_decode for callers that cannot allocate: split partials go to the
+    library's own device array (msa_noalloc_scratch_bytes() bytes); calls must not overlap."""
+    _check(_lib.msa_sparse_attn_decode_noalloc(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                               _ptr(q), _ptr(sel), float(softmax_scale), num_splits, _ptr(out),
+                                               _ptr(status), _stream()), "msa_sparse_attn_decode_noalloc")
+
+
+def msa_noalloc_scratch_bytes() -> int:
+    return int(_lib.msa_noalloc_scratch_bytes())
 
 
 def msa_decode_workspace_size(B: int, T: int, max_blocks_per_seq: int) -> int:

@@ -28,6 +28,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "msa.h"
 #include "msa_device.cuh"
 #include "msa_host.h"
@@ -545,6 +547,90 @@ extern "C" msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_
     return MSA_ERR_CUDA;
   const int grid = batch->B * 4 * splits;
   k_attn<<<grid, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
+  if ((st = launch_status()) != MSA_OK) return st;
+  if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
+  return MSA_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free variant of msa_sparse_attn_decode.
+//
+// Some callers cannot allocate device memory: a host runtime whose memory is laid out once
+// by a static planner and that has no allocator to hand down to this library, or code that
+// runs inside another library's callback, where a cudaMalloc would synchronise the device
+// and break the caller's stream ordering. For them the split partial results live in one
+// file-scope device array of kNoAllocScratchBytes bytes, which every GPU that loads this
+// library holds until the process exits. The caller still passes inputs and outputs.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
+__device__ __align__(256) uint8_t g_attn_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_attn_scratch on the current device, looked up once per device (the
+// name is a host-side stand-in, not a device address).
+msa_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) return MSA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t msa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_batch* batch,
+                                                     const msa_cache* cache, const uint8_t* q, const int32_t* sel,
+                                                     float softmax_scale, int32_t num_splits, uint16_t* out,
+                                                     uint32_t* status, cudaStream_t stream) {
+  msa_status st = check_geometry(geo);
+  if (st != MSA_OK) return st;
+  if ((st = check_batch(batch)) != MSA_OK) return st;
+  if ((st = check_cache(cache, false, true)) != MSA_OK) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits) return MSA_ERR_INVALID_ARG;
+  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
+    return MSA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
+  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->B);
+  const size_t need = attn_ws_bytes(batch->T, splits);
+  if (need > kNoAllocScratchBytes) return MSA_ERR_INVALID_ARG;  // too many tokens x splits for the array
+  void* scratch = nullptr;
+  if (need > 0 && (st = scratch_address(&scratch)) != MSA_OK) return st;
+  AttnParams p;
+  p.B = batch->B;
+  p.T = batch->T;
+  p.maxb = batch->max_blocks_per_seq;
+  p.max_q_len = batch->max_q_len;
+  p.num_pages = cache->num_pages;
+  p.splits = splits;
+  p.qsl = batch->query_start_loc;
+  p.seq_lens = batch->seq_lens;
+  p.block_table = batch->block_table;
+  p.kv_pages = cache->kv_pages;
+  p.q = q;
+  p.sel = sel;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = out;
+  p.part_o = splits > 1 ? static_cast<float*>(scratch) : nullptr;
+  p.part_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                                     align256(static_cast<size_t>(splits) * batch->T * kQHeads * kD * 4))
+                          : nullptr;
+  p.status = status;
+  if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
+      cudaSuccess)
+    return MSA_ERR_CUDA;
+  k_attn<<<batch->B * 4 * splits, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
   if ((st = launch_status()) != MSA_OK) return st;
   if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
   return MSA_OK;

@@ -10,20 +10,21 @@
 // f16, because P rounded to E4M3 (3 mantissa bits) would cost several percent of relative
 // error.
 //
-// GB300 design (one CTA per (sequence, group, split)):
-//  * The query tokens of a sequence (1..8, speculative decoding) mostly pick the same blocks,
-//    so the CTA walks the union of their selections once ("KV-block-major" reuse): each union
-//    block's K and V (2 x 9,216 B, contiguous in the page) arrive with one 1-D bulk copy into a
-//    double-buffered stage, are dequantised once by all 256 threads into swizzled shared memory
-//    (K as E4M3 rows, V as f16 rows), and every warp whose token selected the block consumes it.
-//  * Warps split as tokens x key slices (8 / q_len warps per token), each with its own online
-//    softmax state; the states are merged in shared memory at the end.
-//  * QK^T: mma.sync.m16n8k32.e4m3 with the 16 heads of the group on M; the K operand is one
-//    8-byte shared load per lane (8-byte-slot xor swizzle: conflict-free). PV:
-//    mma.sync.m16n8k16.f16 with P taken straight from the QK^T accumulators and V fragments
-//    from ldmatrix.trans (16-byte-chunk xor swizzle: conflict-free).
-//  * Splits of the union list raise the CTA count when B * 4 is small; partial (lse, o) pairs
-//    are merged by log-sum-exp in a second kernel.
+// GB300 design: one CTA of 8 warps per (query token, group, split); a warp owns whole
+// selected blocks (16 query heads x 128 keys):
+//  * its block's K and V regions (2 x 9,216 B, contiguous in the page) arrive with one 1-D
+//    bulk copy (cp.async.bulk + mbarrier) into the warp's own shared-memory stage;
+//  * K is dequantised register-direct into the B fragments of mma.sync.m16n8k32.e4m3 (the
+//    16 heads of the group on M), 32 keys at a time, the same lane/dim mapping as the indexer;
+//  * V of those 32 keys is dequantised once into a private swizzled f16 tile and read back
+//    transposed with ldmatrix.trans for mma.sync.m16n8k16.f16 (P straight from the QK^T
+//    accumulators);
+//  * online softmax per warp; O is rescaled only when some row maximum moved; the 8 warps'
+//    states are merged in shared memory at the end.
+//  * Splits of a (token, group)'s 16 blocks raise the CTA count when T * 4 is small; the
+//    partial (lse, o) pairs are merged by log-sum-exp in a second kernel.
+// The next block's copy is issued as soon as the last V chunk of the current block has been
+// dequantised, so it overlaps the remaining MMAs.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -40,6 +41,8 @@ namespace {
 constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = 32 * kAttnWarps;
 constexpr int kStageBytes = 2 * kRegion;  // K region then V region of one (page, group)
+constexpr int kChunkKeys = 32;
+constexpr int kVTileBytes = kChunkKeys * kD * 2;  // 32 keys x 128 dims f16
 
 struct AttnParams {
   int32_t B, T, maxb, max_q_len, num_pages, splits;
@@ -57,22 +60,18 @@ struct AttnParams {
 };
 
 struct AttnSmem {
-  static constexpr size_t kOffStage = 0;                                  // 2 x 18,432
-  static constexpr size_t kOffK = kOffStage + 2 * kStageBytes;            // 128 x 128 B
-  static constexpr size_t kOffV = kOffK + kBS * kD;                       // 128 x 256 B
-  static constexpr size_t kOffLut = kOffV + kBS * kD * 2;                 // 2 KB
-  static constexpr size_t kOffBar = kOffLut + 256 * 8;
-  static constexpr size_t kOffUblk = kOffBar + 64;                        // 128 int
-  static constexpr size_t kOffUmask = kOffUblk + 4 * 128;                 // 128 u32
-  static constexpr size_t kOffUphys = kOffUmask + 4 * 128;                // 128 int
-  static constexpr size_t kOffVals = kOffUphys + 4 * 128;                 // 128 int
-  static constexpr size_t kOffFirst = kOffVals + 4 * 128;                 // 128 u32
-  static constexpr size_t kOffMisc = kOffFirst + 4 * 128;
+  static constexpr size_t kOffStage = 0;                                        // 8 x 18,432
+  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kAttnWarps) * kStageBytes;  // 8 x 8,192
+  static constexpr size_t kOffLut = kOffV + static_cast<size_t>(kAttnWarps) * kVTileBytes;    // 2 KB
+  static constexpr size_t kOffBar = kOffLut + 256 * 8;                          // 8 mbarriers
+  static constexpr size_t kOffBlk = kOffBar + 8 * kAttnWarps;                   // 16 block ids
+  static constexpr size_t kOffPhys = kOffBlk + 4 * kSel;                        // 16 page ids
+  static constexpr size_t kOffMisc = kOffPhys + 4 * kSel;
   static constexpr size_t kBytes = kOffMisc + 64;
-  // after the block loop, the stage / K / V area holds each warp's final state
-  static constexpr size_t kWarpState = 16 * 4 * 2 + 16 * kD * 4;          // m, l, O[16][128]
+  // after the block loop, the stage area holds each warp's final state
+  static constexpr size_t kWarpState = 16 * 4 * 2 + 16 * kD * 4;  // m, l, O[16][128]
 };
-static_assert(AttnSmem::kOffLut >= kAttnWarps * AttnSmem::kWarpState, "merge area too small");
+static_assert(AttnSmem::kOffV >= kAttnWarps * AttnSmem::kWarpState, "merge area too small");
 
 __device__ __forceinline__ float quad_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
@@ -89,200 +88,231 @@ struct WarpState {
   float o[16][4];  // 16 n-tiles of 8 dims: (head gid, dims 8j+2t..+1), (head gid+8, ...)
 };
 
-// Attend to NJ*8 keys starting at key `k0` of the staged block (K, V in shared memory).
-template <int NJ>
-__device__ __forceinline__ void attend_keys(WarpState& st, const uint32_t (&qa)[4][4], const uint8_t* Ks,
-                                            const uint8_t* Vs, int k0, int blk_pos0, int p_tok, float scale_log2,
-                                            int lane) {
+// Dequantise keys r0 + gid + 8i (i = 0..3), dims 32t .. 32t+31, of a staged NVFP4 region into
+// the f16 tile `vt` (32 rows x 256 B, 16-byte chunk c of row r stored at chunk c ^ (r & 7)).
+__device__ __forceinline__ void dequant_v_chunk(const uint8_t* vr, int r0, const uint2* lut, uint8_t* vt, int lane) {
   const int gid = lane >> 2, t = lane & 3;
-  float x[NJ][4];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    x[j][0] = x[j][1] = x[j][2] = x[j][3] = 0.f;
-    const int key = k0 + 8 * j + gid;
-    const uint8_t* row = Ks + key * kD;
+  for (int i = 0; i < 4; ++i) {
+    const int rl = gid + 8 * i;  // row inside the tile
+    const int r = r0 + rl;       // row inside the block
+    const uint4 c = lds128(vr + r * kRowCodes + 16 * t);
+    const uint32_t sc = *reinterpret_cast<const uint16_t*>(vr + kScaleOff + r * kRowScales + 2 * t);
+    const uint2 e0 = lut[sc & 0xFFu], e1 = lut[sc >> 8];
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint2 b = lds64(row + (((4 * t + s) ^ (key & 3)) << 3));
-      mma_e4m3(x[j], qa[s][0], qa[s][1], qa[s][2], qa[s][3], b.x, b.y);
+    for (int q = 0; q < 4; ++q) {  // word q = dims 32t + 8q .. +7 = f16 chunk 4t + q
+      uint32_t lo, hi;
+      dq8(w[q], q < 2 ? e0 : e1, lo, hi);
+      const uint4 v = make_uint4(cvt_f16x2_e4m3x2(lo), cvt_f16x2_e4m3x2(lo >> 16), cvt_f16x2_e4m3x2(hi),
+                                 cvt_f16x2_e4m3x2(hi >> 16));
+      *reinterpret_cast<uint4*>(vt + rl * (2 * kD) + (((4 * t + q) ^ (rl & 7)) << 4)) = v;
     }
   }
-  // scale, causal mask, row max
-  const bool need_mask = blk_pos0 + k0 + 8 * NJ - 1 > p_tok;
-  float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+}
+
+// Copy of the next block into this warp's stage: src == nullptr means a bad page id (the
+// barrier phase still completes, with no bytes).
+__device__ __forceinline__ void issue_stage(uint8_t* stage, const uint8_t* src, uint64_t* bar) {
+  if (src != nullptr) {
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    bulk_g2s(stage, src, kStageBytes, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+// One block of 128 keys (K, V staged at kr, kr + kRegion) for the 16 heads of this warp.
+// Once every key and value of the stage has been read, lane 0 starts the copy of the warp's
+// next block (has_next; next_src as for issue_stage) into the same stage.
+__device__ __forceinline__ void attend_block(WarpState& st, const uint32_t (&qa)[4][4], uint8_t* kr,
+                                             const uint2* lut, uint8_t* vt, int blk_pos0, int p_tok, float scale_log2,
+                                             int lane, bool has_next, const uint8_t* next_src, uint64_t* bar) {
+  const int gid = lane >> 2, t = lane & 3;
+  const uint8_t* vr = kr + kRegion;
+  bool issued = !has_next;
+#pragma unroll 1
+  for (int c = 0; c < kBS / kChunkKeys; ++c) {
+    const int k0 = c * kChunkKeys;
+    if (blk_pos0 + k0 > p_tok) break;  // every remaining key lies after the query position
+    // ---- S = Q K^T for keys k0 .. k0+31 (4 n-tiles of 8 keys)
+    float x[4][4];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
+    for (int j = 0; j < 4; ++j) {
+      const int key = k0 + 8 * j + gid;
+      const uint4 cw = lds128(kr + key * kRowCodes + 16 * t);
+      const uint32_t sc = *reinterpret_cast<const uint16_t*>(kr + kScaleOff + key * kRowScales + 2 * t);
+      const uint2 e0 = lut[sc & 0xFFu], e1 = lut[sc >> 8];
+      uint32_t b[4][2];
+      dq8(cw.x, e0, b[0][0], b[0][1]);
+      dq8(cw.y, e0, b[1][0], b[1][1]);
+      dq8(cw.z, e1, b[2][0], b[2][1]);
+      dq8(cw.w, e1, b[3][0], b[3][1]);
+      mma_e4m3_zc(x[j], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b[0][0], b[0][1]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float v = x[j][i] * scale_log2;
-      if (need_mask && blk_pos0 + k0 + 8 * j + 2 * t + (i & 1) > p_tok) v = -CUDART_INF_F;
-      x[j][i] = v;
+      for (int s = 1; s < 4; ++s) mma_e4m3(x[j], qa[s][0], qa[s][1], qa[s][2], qa[s][3], b[s][0], b[s][1]);
     }
-    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][1]));
-    mx1 = fmaxf(mx1, fmaxf(x[j][2], x[j][3]));
-  }
-  mx0 = quad_max(mx0);
-  mx1 = quad_max(mx1);
-  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-  const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
-  const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
-  const float c0 = fast_exp2(st.m[0] - mu0), c1 = fast_exp2(st.m[1] - mu1);
-  st.m[0] = mn0;
-  st.m[1] = mn1;
-  float ls0 = 0.f, ls1 = 0.f;
+    // ---- V of these keys -> f16 tile; after the last chunk the stage is fully read
+    dequant_v_chunk(vr, k0, lut, vt, lane);
+    if (!issued && (c == kBS / kChunkKeys - 1 || blk_pos0 + k0 + kChunkKeys > p_tok)) {
+      __syncwarp();
+      if (lane == 0) issue_stage(kr, next_src, bar);
+      issued = true;
+    }
+    // ---- scale, causal mask, online softmax
+    const bool need_mask = blk_pos0 + k0 + kChunkKeys - 1 > p_tok;
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    x[j][0] = fast_exp2(x[j][0] - mu0);
-    x[j][1] = fast_exp2(x[j][1] - mu0);
-    x[j][2] = fast_exp2(x[j][2] - mu1);
-    x[j][3] = fast_exp2(x[j][3] - mu1);
-    ls0 += x[j][0] + x[j][1];
-    ls1 += x[j][2] + x[j][3];
-  }
-  st.l[0] = st.l[0] * c0 + ls0;
-  st.l[1] = st.l[1] * c1 + ls1;
+    for (int j = 0; j < 4; ++j) {
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    st.o[n][0] *= c0;
-    st.o[n][1] *= c0;
-    st.o[n][2] *= c1;
-    st.o[n][3] *= c1;
-  }
-  // PV: 16 keys per k-step
+      for (int i = 0; i < 4; ++i) {
+        float v = x[j][i] * scale_log2;
+        if (need_mask && blk_pos0 + k0 + 8 * j + 2 * t + (i & 1) > p_tok) v = -CUDART_INF_F;
+        x[j][i] = v;
+      }
+      mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(x[j][2], x[j][3]));
+    }
+    mx0 = quad_max(mx0);
+    mx1 = quad_max(mx1);
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+    const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+    if (__any_sync(0xffffffffu, mn0 != st.m[0] || mn1 != st.m[1])) {
+      const float c0 = fast_exp2(st.m[0] - mu0), c1 = fast_exp2(st.m[1] - mu1);
+      st.l[0] *= c0;
+      st.l[1] *= c1;
 #pragma unroll
-  for (int kk = 0; kk < NJ / 2; ++kk) {
-    const uint32_t a0 = pack_f16x2(x[2 * kk][0], x[2 * kk][1]);
-    const uint32_t a1 = pack_f16x2(x[2 * kk][2], x[2 * kk][3]);
-    const uint32_t a2 = pack_f16x2(x[2 * kk + 1][0], x[2 * kk + 1][1]);
-    const uint32_t a3 = pack_f16x2(x[2 * kk + 1][2], x[2 * kk + 1][3]);
+      for (int n = 0; n < 16; ++n) {
+        st.o[n][0] *= c0;
+        st.o[n][1] *= c0;
+        st.o[n][2] *= c1;
+        st.o[n][3] *= c1;
+      }
+      st.m[0] = mn0;
+      st.m[1] = mn1;
+    }
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[j][0] = fast_exp2(x[j][0] - mu0);
+      x[j][1] = fast_exp2(x[j][1] - mu0);
+      x[j][2] = fast_exp2(x[j][2] - mu1);
+      x[j][3] = fast_exp2(x[j][3] - mu1);
+      ls0 += x[j][0] + x[j][1];
+      ls1 += x[j][2] + x[j][3];
+    }
+    st.l[0] += ls0;
+    st.l[1] += ls1;
+    __syncwarp();  // the V tile is complete
+    // ---- O += P V: 2 k-steps of 16 keys, 8 pairs of 8-dim n-tiles
     const int mi = lane >> 3, ri = lane & 7;
-    const int key = k0 + 16 * kk + (mi & 1) * 8 + ri;
-    const uint8_t* vrow = Vs + key * (kD * 2);
 #pragma unroll
-    for (int dn = 0; dn < 8; ++dn) {
-      const int chunk = 2 * dn + (mi >> 1);
-      uint32_t r[4];
-      ldmatrix_x4_trans(r, vrow + ((chunk ^ (key & 7)) << 4));
-      mma_f16(st.o[2 * dn], a0, a1, a2, a3, r[0], r[1]);
-      mma_f16(st.o[2 * dn + 1], a0, a1, a2, a3, r[2], r[3]);
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t a0 = pack_f16x2(x[2 * kk][0], x[2 * kk][1]);
+      const uint32_t a1 = pack_f16x2(x[2 * kk][2], x[2 * kk][3]);
+      const uint32_t a2 = pack_f16x2(x[2 * kk + 1][0], x[2 * kk + 1][1]);
+      const uint32_t a3 = pack_f16x2(x[2 * kk + 1][2], x[2 * kk + 1][3]);
+      const int rl = 16 * kk + (mi & 1) * 8 + ri;
+      const uint8_t* vrow = vt + rl * (2 * kD);
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn) {
+        const int chunk = 2 * dn + (mi >> 1);
+        uint32_t r[4];
+        ldmatrix_x4_trans(r, vrow + ((chunk ^ (rl & 7)) << 4));
+        mma_f16(st.o[2 * dn], a0, a1, a2, a3, r[0], r[1]);
+        mma_f16(st.o[2 * dn + 1], a0, a1, a2, a3, r[2], r[3]);
+      }
     }
+    __syncwarp();  // before the next chunk overwrites the V tile
+  }
+  if (!issued) {  // (not reached: the first chunk always holds a valid key)
+    __syncwarp();
+    if (lane == 0) issue_stage(kr, next_src, bar);
   }
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p) {
   using S = AttnSmem;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stage = smem + S::kOffStage;
-  uint8_t* Ks = smem + S::kOffK;
-  uint8_t* Vs = smem + S::kOffV;
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  int* ublk = reinterpret_cast<int*>(smem + S::kOffUblk);
-  uint32_t* umask = reinterpret_cast<uint32_t*>(smem + S::kOffUmask);
-  int* uphys = reinterpret_cast<int*>(smem + S::kOffUphys);
-  int* vals = reinterpret_cast<int*>(smem + S::kOffVals);
-  uint32_t* first = reinterpret_cast<uint32_t*>(smem + S::kOffFirst);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
-  uint32_t* tokbad = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 4);
-  int* nunion = reinterpret_cast<int*>(smem + S::kOffMisc + 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
+  int* blk = reinterpret_cast<int*>(smem + S::kOffBlk);
+  int* phys = reinterpret_cast<int*>(smem + S::kOffPhys);
+  int* nblk = reinterpret_cast<int*>(smem + S::kOffMisc);
+  int* bad = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x % p.splits;
-  const int bg = blockIdx.x / p.splits;
-  const int g = bg & 3, b = bg >> 2;
+  const int tg = blockIdx.x / p.splits;
+  const int t = tg >> 2, g = tg & 3;
 
-  const int q0 = p.qsl[b];
-  const int ql = p.qsl[b + 1] - q0;
+  // the sequence of token t (largest b with qsl[b] <= t)
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
   const int L = p.seq_lens[b];
-  if (ql <= 0) return;  // padded request row
-  const bool batch_ok = ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS && q0 >= 0 && q0 + ql <= p.T;
-  if (!batch_ok) {
+  if (!(t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) {
     if (tid == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
     return;
   }
   const int nb = ceil_div(L, kBS);
+  const int p_tok = L - ql + (t - q0);
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int w = 0; w < kAttnWarps; ++w) mbar_init(&bars[w], 1);
     fence_mbar_init();
     *abort_flag = 0;
-    *tokbad = 0;
+    *bad = 0;
   }
   build_dequant_lut(lut, tid, kAttnThreads);
-  // ---- the union of the tokens' selected blocks (distinct, ascending) -----------------
-  if (tid < 128) {
-    const int tok = tid >> 4, slot = tid & 15;
-    int v = 0x7FFFFFFF;
-    if (tok < ql) {
-      const int blk = p.sel[(static_cast<int64_t>(q0 + tok) * 4 + g) * kSel + slot];
-      if (blk >= nb) {
-        atomicOr(tokbad, 1u << tok);
-        set_status(p.status, MSA_ERR_DEVICE_FAULT);
-      } else if (blk >= 0) {
-        v = blk;
-      }
-    }
-    vals[tid] = v;
-  }
-  __syncthreads();
-  if (tid < 128) {
-    const int v = vals[tid];
-    bool is_first = v != 0x7FFFFFFF;
-    uint32_t m = 0;
-    for (int j = 0; j < 128; ++j) {
-      if (vals[j] == v) {
-        m |= 1u << (j >> 4);
-        if (j < tid) is_first = false;
-      }
-    }
-    first[tid] = is_first ? m : 0u;
-  }
-  __syncthreads();
-  if (tid < 128) {
-    const int v = vals[tid];
-    const uint32_t m = first[tid];
-    if (m != 0u) {
-      int rank = 0;
-      for (int j = 0; j < 128; ++j) rank += (first[j] != 0u && vals[j] < v) ? 1 : 0;
-      ublk[rank] = v;
-      umask[rank] = m;
-    }
-  }
-  const int U = __syncthreads_count(tid < 128 && first[tid] != 0u);
-  if (tid < U) {
-    const int phys = p.block_table[static_cast<int64_t>(b) * p.maxb + ublk[tid]];
-    const bool ok = phys >= 0 && phys < p.num_pages;
-    uphys[tid] = ok ? phys : -1;
-    if (!ok) {
-      atomicOr(tokbad, umask[tid]);
+  // ---- the distinct selected blocks of (t, g), in slot order, and their pages
+  if (warp == 0) {
+    const int v = lane < kSel ? p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + lane] : -1;
+    bool keep = v >= 0 && v < nb;
+    if (lane < kSel && v >= nb) {
       set_status(p.status, MSA_ERR_DEVICE_FAULT);
+      atomicOr(bad, 1);
     }
+    // drop repeats of an earlier slot
+    for (int j = 0; j < kSel; ++j) {
+      const int vj = __shfl_sync(0xffffffffu, v, j);
+      if (j < lane && vj == v) keep = false;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, keep && lane < kSel);
+    const int pos = __popc(m & ((1u << lane) - 1u));
+    if (keep && lane < kSel) {
+      blk[pos] = v;
+      const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
+      const bool ok = ph >= 0 && ph < p.num_pages;
+      phys[pos] = ok ? ph : -1;
+      if (!ok) {
+        set_status(p.status, MSA_ERR_DEVICE_FAULT);
+        atomicOr(bad, 1);
+      }
+    }
+    if (lane == 0) *nblk = __popc(m);
   }
-  if (tid == 0) *nunion = U;
   __syncthreads();
+  const int n = *nblk;
+  const bool is_bad = *bad != 0;
+  const int i0 = (n * split) / p.splits, i1 = (n * (split + 1)) / p.splits;
 
-  const int u0 = (U * split) / p.splits, u1 = (U * (split + 1)) / p.splits;
-  const uint32_t bad = *tokbad;
-
-  // ---- warp roles -----------------------------------------------------------------
-  const int wpt = kAttnWarps / ql;  // 8, 4, 2, 2, 1, 1, 1, 1
-  const int my_tok = warp / wpt;
-  const int slice = warp % wpt;
-  const bool active = my_tok < ql;
-  const int nk = kBS / wpt;
-  const int kbase = slice * nk;
-  const int p_tok = L - ql + my_tok;
-  const int gid = lane >> 2, t = lane & 3;
-
-  uint32_t qa[4][4];
+  // ---- per-warp blocks i0 + warp, i0 + warp + 8, ...
+  const int gid = lane >> 2, tq = lane & 3;
   WarpState st;
   st.m[0] = st.m[1] = -CUDART_INF_F;
   st.l[0] = st.l[1] = 0.f;
 #pragma unroll
-  for (int n = 0; n < 16; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
-  if (active) {
-    const uint8_t* qrow0 = p.q + (static_cast<int64_t>(q0 + my_tok) * kQHeads + g * kHPG + gid) * kD + 32 * t;
+  for (int k = 0; k < 16; ++k) st.o[k][0] = st.o[k][1] = st.o[k][2] = st.o[k][3] = 0.f;
+  uint32_t qa[4][4];
+  {
+    const uint8_t* qrow0 = p.q + (static_cast<int64_t>(t) * kQHeads + g * kHPG + gid) * kD + 32 * tq;
     const uint8_t* qrow1 = qrow0 + 8 * kD;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -294,139 +324,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p) {
       qa[s][3] = x1.y;
     }
   }
-
-  // ---- block loop ------------------------------------------------------------------
-  auto issue = [&](int u, int buf) {
-    const int phys = uphys[u];
-    if (phys >= 0) {
-      mbar_arrive_expect_tx(&full[buf], kStageBytes);
-      bulk_g2s(stage + buf * kStageBytes, p.kv_pages + static_cast<int64_t>(phys) * kKvPage + (2 * g) * kRegion,
-               kStageBytes, &full[buf]);
-    } else {
-      mbar_arrive(&full[buf]);
-    }
+  uint8_t* stage = smem + S::kOffStage + static_cast<size_t>(warp) * kStageBytes;
+  uint8_t* vt = smem + S::kOffV + static_cast<size_t>(warp) * kVTileBytes;
+  uint64_t* bar = &bars[warp];
+  auto src_of = [&](int i) -> const uint8_t* {
+    const int ph = phys[i];
+    return ph >= 0 ? p.kv_pages + static_cast<int64_t>(ph) * kKvPage + (2 * g) * kRegion : nullptr;
   };
-  if (tid == 0) {
-    if (u0 < u1) issue(u0, 0);
-    if (u0 + 1 < u1) issue(u0 + 1, 1);
+  int it = 0;
+  bool inflight = false;
+  if (!is_bad && i0 + warp < i1) {
+    if (lane == 0) issue_stage(stage, src_of(i0 + warp), bar);
+    inflight = true;
   }
-  int issued_hi = min(u1, u0 + 2);  // meaningful in thread 0 only
-  bool aborted = false;
-  int u_stop = u1;
-  for (int u = u0; u < u1; ++u) {
-    const int it = u - u0, buf = it & 1;
-    if (!mbar_wait_bounded(&full[buf], static_cast<uint32_t>(it >> 1) & 1u, kWaitLimitNs, abort_flag)) {
-      if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      aborted = true;
-    }
-    if (__syncthreads_or(aborted ? 1 : 0)) {
-      aborted = true;
-      u_stop = u;
-      break;
-    }
-    const bool page_ok = uphys[u] >= 0;
-    if (page_ok) {
-      // dequantise K -> E4M3 rows, V -> f16 rows (row r, dims 64h .. 64h+63 per thread)
-      const uint8_t* kr = stage + buf * kStageBytes;
-      const uint8_t* vr = kr + kRegion;
-      const int r = tid >> 1, h = tid & 1;
-      {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(kr + r * kRowCodes + 32 * h);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(kr + r * kRowCodes + 32 * h + 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(kr + kScaleOff + r * kRowScales + 4 * h);
-        const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const int m = r & 3;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 16-byte chunk c of this thread = words 2c, 2c+1
-          const uint2 e = lut[(sc >> (8 * c)) & 0xFFu];
-          uint32_t l0, h0, l1, h1;
-          dq8(w[2 * c], e, l0, h0);
-          dq8(w[2 * c + 1], e, l1, h1);
-          const int slot = 8 * h + 2 * c;        // logical 8-byte slot of word 2c
-          const int phys = slot ^ m;
-          uint4 v = (m & 1) ? make_uint4(l1, h1, l0, h0) : make_uint4(l0, h0, l1, h1);
-          *reinterpret_cast<uint4*>(Ks + r * kD + ((phys & ~1) << 3)) = v;
-        }
+  for (int i = i0 + warp; !is_bad && i < i1; i += kAttnWarps, ++it) {
+    if (!mbar_wait_bounded(bar, static_cast<uint32_t>(it) & 1u, kWaitLimitNs, abort_flag)) {
+      if (lane == 0) {
+        if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+        *abort_flag = 1;
       }
-      {
-        const uint4 c0 = *reinterpret_cast<const uint4*>(vr + r * kRowCodes + 32 * h);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(vr + r * kRowCodes + 32 * h + 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(vr + kScaleOff + r * kRowScales + 4 * h);
-        const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {  // word i = dims 64h + 8i .. +7 = f16 chunk 8h + i
-          const uint2 e = lut[(sc >> (8 * (i >> 1))) & 0xFFu];
-          uint32_t lo, hi;
-          dq8(w[i], e, lo, hi);
-          const uint4 v = make_uint4(cvt_f16x2_e4m3x2(lo), cvt_f16x2_e4m3x2(lo >> 16), cvt_f16x2_e4m3x2(hi),
-                                     cvt_f16x2_e4m3x2(hi >> 16));
-          const int chunk = (8 * h + i) ^ (r & 7);
-          *reinterpret_cast<uint4*>(Vs + r * (2 * kD) + (chunk << 4)) = v;
-        }
-      }
+      break;  // inflight stays true: drained below
     }
-    __syncthreads();  // K, V ready; stage[buf] free
-    if (tid == 0 && u + 2 < u1) {
-      issue(u + 2, buf);
-      issued_hi = u + 3;
-    }
-    if (page_ok && active && ((umask[u] >> my_tok) & 1u) && !((bad >> my_tok) & 1u)) {
-      const int blk_pos0 = ublk[u] * kBS;
-      if (nk == 16) {
-        attend_keys<2>(st, qa, Ks, Vs, kbase, blk_pos0, p_tok, p.scale_log2, lane);
-      } else {
-        for (int kc = 0; kc < nk; kc += 32)
-          attend_keys<4>(st, qa, Ks, Vs, kbase + kc, blk_pos0, p_tok, p.scale_log2, lane);
-      }
-    }
-    __syncthreads();  // before the next block overwrites K, V
+    const bool has_next = i + kAttnWarps < i1;
+    // the copy of the next block starts inside, once this stage has been fully read
+    attend_block(st, qa, stage, lut, vt, blk[i] * kBS, p_tok, p.scale_log2, lane, has_next,
+                 has_next ? src_of(i + kAttnWarps) : nullptr, bar);
+    inflight = has_next;
   }
-  if (aborted && tid == 0) {
-    // wait (bounded) for the copies not yet consumed, which may still be in flight into this
-    // CTA's shared memory (at most the two stages from u_stop on)
-    for (int u = u_stop; u < issued_hi; ++u) {
-      const int it = u - u0;
-      mbar_wait_bounded(&full[it & 1], static_cast<uint32_t>(it >> 1) & 1u, kWaitLimitNs, nullptr);
-    }
+  if (inflight && lane == 0) {
+    // a copy into this warp's stage may still be in flight: wait for it (bounded)
+    mbar_wait_bounded(bar, static_cast<uint32_t>(it) & 1u, kWaitLimitNs, nullptr);
   }
   __syncthreads();
 
-  // ---- merge the warps of each token, write the output or the split partial ----------
-  uint8_t* ws = smem;  // reuse stage / K / V
-  if (active) {
+  // ---- merge the 8 warps' states, write the output or this split's partial --------------
+  uint8_t* ws = smem;  // reuse the stages
+  {
     float* mw = reinterpret_cast<float*>(ws + warp * S::kWarpState);
     float* lw = mw + 16;
     float* ow = lw + 16;
     const float l0 = quad_sum(st.l[0]), l1 = quad_sum(st.l[1]);
-    if (t == 0) {
+    if (tq == 0) {
       mw[gid] = st.m[0];
       mw[gid + 8] = st.m[1];
       lw[gid] = l0;
       lw[gid + 8] = l1;
     }
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      *reinterpret_cast<float2*>(ow + gid * kD + 8 * n + 2 * t) = make_float2(st.o[n][0], st.o[n][1]);
-      *reinterpret_cast<float2*>(ow + (gid + 8) * kD + 8 * n + 2 * t) = make_float2(st.o[n][2], st.o[n][3]);
+    for (int k = 0; k < 16; ++k) {
+      *reinterpret_cast<float2*>(ow + gid * kD + 8 * k + 2 * tq) = make_float2(st.o[k][0], st.o[k][1]);
+      *reinterpret_cast<float2*>(ow + (gid + 8) * kD + 8 * k + 2 * tq) = make_float2(st.o[k][2], st.o[k][3]);
     }
   }
   __syncthreads();
-  const int nelem = ql * kHPG * (kD / 4);  // float4 granules
-  for (int e = tid; e < nelem; e += kAttnThreads) {
+  for (int e = tid; e < kHPG * (kD / 4); e += kAttnThreads) {
     const int d4 = e % (kD / 4);
-    const int hh = (e / (kD / 4)) % kHPG;
-    const int tok = e / (kD / 4) / kHPG;
+    const int hh = e / (kD / 4);
     float M = -CUDART_INF_F;
-    for (int sl = 0; sl < wpt; ++sl) {
-      const float* mw = reinterpret_cast<const float*>(ws + (tok * wpt + sl) * S::kWarpState);
-      M = fmaxf(M, mw[hh]);
-    }
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(ws + w * S::kWarpState)[hh]);
     float Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -CUDART_INF_F) {
-      for (int sl = 0; sl < wpt; ++sl) {
-        const float* mw = reinterpret_cast<const float*>(ws + (tok * wpt + sl) * S::kWarpState);
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float* mw = reinterpret_cast<const float*>(ws + w * S::kWarpState);
         const float f = fast_exp2(mw[hh] - M);
         Lsum += mw[16 + hh] * f;
         const float4 o = *reinterpret_cast<const float4*>(mw + 32 + hh * kD + 4 * d4);
@@ -436,9 +398,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p) {
         acc.w += o.w * f;
       }
     }
-    const bool zero = (M == -CUDART_INF_F) || Lsum <= 0.f || ((bad >> tok) & 1u);
+    const bool zero = (M == -CUDART_INF_F) || Lsum <= 0.f || is_bad;
     const float inv = zero ? 0.f : 1.0f / Lsum;
-    const int64_t orow = static_cast<int64_t>(q0 + tok) * kQHeads + g * kHPG + hh;
+    const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + hh;
     if (p.splits == 1) {
       const uint2 v = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
       *reinterpret_cast<uint2*>(p.out + orow * kD + 4 * d4) = v;
@@ -494,7 +456,7 @@ using namespace msa_host;
 
 extern "C" size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, int32_t num_splits) {
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || num_splits < 0 || num_splits > kMaxSplits) return 0;
-  const int s = num_splits > 0 ? num_splits : auto_splits(B);
+  const int s = num_splits > 0 ? num_splits : auto_splits(T);
   return attn_ws_bytes(T, s);
 }
 
@@ -518,7 +480,7 @@ extern "C" msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
     return MSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->B);
+  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->T);
   const size_t need = attn_ws_bytes(batch->T, splits);
   if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned(workspace, 256))))
     return MSA_ERR_INVALID_ARG;
@@ -545,7 +507,7 @@ extern "C" msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_
   if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
-  const int grid = batch->B * 4 * splits;
+  const int grid = batch->T * 4 * splits;
   k_attn<<<grid, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
   if ((st = launch_status()) != MSA_OK) return st;
   if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
@@ -602,7 +564,7 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, co
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
     return MSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->B);
+  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->T);
   const size_t need = attn_ws_bytes(batch->T, splits);
   if (need > kNoAllocScratchBytes) return MSA_ERR_INVALID_ARG;  // too many tokens x splits for the array
   void* scratch = nullptr;
@@ -630,7 +592,7 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, co
   if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
-  k_attn<<<batch->B * 4 * splits, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
+  k_attn<<<batch->T * 4 * splits, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
   if ((st = launch_status()) != MSA_OK) return st;
   if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
   return MSA_OK;

@@ -53,11 +53,12 @@ inline int num_sms() {
   return n;
 }
 
-// Splits of the attention work per (sequence, group) chosen from B alone (so workspace sizes
-// are a pure function of the arguments): enough CTAs for about two per SM of a 152-SM GB300.
-inline int auto_splits(int B) {
-  const int items = 4 * B;
-  if (items <= 0 || items >= 152) return 1;
+// Splits of each (query token, group)'s selected blocks, chosen from T alone (so workspace
+// sizes are a pure function of the arguments): enough CTAs for about two per SM of a 152-SM
+// GB300, at most 16 (one block per split).
+inline int auto_splits(int T) {
+  const int items = 4 * T;
+  if (items <= 0 || items >= 304) return 1;
   int s = (304 + items - 1) / items;
   return s > 16 ? 16 : s;
 }

@@ -35,21 +35,27 @@
 namespace msa {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kIdxThreads = 32 * (kConsumerWarps + 1);
-
+// Stage ring: consumer warp w owns slots w, w + W, ..., w + W*(D-1) and its j-th page lives
+// in slot w + W*(j % D). Each slot thus serves one warp, in order, so a warp only ever waits
+// for the phase right after the one it consumed itself (an mbarrier's parity cannot tell a
+// phase from the one two steps earlier).
 template <int DT>
 struct IdxCfg;
 template <>
 struct IdxCfg<MSA_INDEX_NVFP4> {
   static constexpr int kPage = kIdxPageNv;
-  static constexpr int kStages = 16;
+  static constexpr int kWarps = 8;  // consumer warps
+  static constexpr int kDepth = 2;  // pages in flight per consumer warp
+  static constexpr int kStages = kWarps * kDepth;
 };
 template <>
 struct IdxCfg<MSA_INDEX_FP8> {
   static constexpr int kPage = kIdxPageFp8;
-  static constexpr int kStages = 10;
+  static constexpr int kWarps = 6;
+  static constexpr int kDepth = 2;
+  static constexpr int kStages = kWarps * kDepth;
 };
+constexpr int kMaxIdxThreads = 32 * (8 + 1);
 
 struct IdxParams {
   int32_t B, T, maxb, max_q_len, num_pages;
@@ -93,16 +99,16 @@ __device__ __forceinline__ int seq_pages(const IdxParams& p, int b, bool* bad) {
 }
 
 // Score one staged page for the N tiles of the current sequence and write its block scores.
-// NT = number of 8-column tiles (columns = q_len * 4).
-template <int DT, int NT>
+// NT = number of 8-column tiles (columns = q_len * 4). MASK: the page holds rows after a query
+// position (only the last page or two of a sequence), so rows are masked per column.
+template <int DT, int NT, bool MASK>
 __device__ __forceinline__ void score_page(const uint8_t* pg, const uint2* lut, const uint32_t (&bfrag)[4][4][2],
                                            int lane, int k, int p0, int ncol, int q0, const IdxParams& p) {
   const int gid = lane >> 2, t = lane & 3;
   float mx[NT][2];
 #pragma unroll
   for (int j = 0; j < NT; ++j) mx[j][0] = mx[j][1] = -CUDART_INF_F;
-  const bool need_mask = (k + 1) * kBS - 1 > p0;  // some row may lie after a query position
-#pragma unroll 2
+#pragma unroll 1
   for (int tile = 0; tile < kBS / 16; ++tile) {
     const int r0 = tile * 16 + gid, r1 = r0 + 8;
     uint32_t a[4][4];
@@ -137,10 +143,11 @@ __device__ __forceinline__ void score_page(const uint8_t* pg, const uint2* lut, 
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4];
+      mma_e4m3_zc(acc, a[0][0], a[0][1], a[0][2], a[0][3], bfrag[j][0][0], bfrag[j][0][1]);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) mma_e4m3(acc, a[s][0], a[s][1], a[s][2], a[s][3], bfrag[j][s][0], bfrag[j][s][1]);
-      if (need_mask) {
+      for (int s = 1; s < 4; ++s) mma_e4m3(acc, a[s][0], a[s][1], a[s][2], a[s][3], bfrag[j][s][0], bfrag[j][s][1]);
+      if constexpr (MASK) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = (i < 2) ? r0 : r1;
@@ -167,21 +174,34 @@ __device__ __forceinline__ void score_page(const uint8_t* pg, const uint2* lut, 
   }
 }
 
-template <int DT>
-__device__ __forceinline__ void score_page_any(int nt, const uint8_t* pg, const uint2* lut,
-                                               const uint32_t (&bfrag)[4][4][2], int lane, int k, int p0, int ncol,
-                                               int q0, const IdxParams& p) {
+template <int DT, bool MASK>
+__device__ __forceinline__ void score_page_nt(int nt, const uint8_t* pg, const uint2* lut,
+                                              const uint32_t (&bfrag)[4][4][2], int lane, int k, int p0, int ncol,
+                                              int q0, const IdxParams& p) {
   switch (nt) {
-    case 1: score_page<DT, 1>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    case 2: score_page<DT, 2>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    case 3: score_page<DT, 3>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    default: score_page<DT, 4>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
+    case 1: score_page<DT, 1, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
+    case 2: score_page<DT, 2, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
+    case 3: score_page<DT, 3, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
+    default: score_page<DT, 4, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
   }
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p) {
+__device__ __forceinline__ void score_page_any(int nt, const uint8_t* pg, const uint2* lut,
+                                               const uint32_t (&bfrag)[4][4][2], int lane, int k, int p0, int ncol,
+                                               int q0, const IdxParams& p) {
+  if ((k + 1) * kBS - 1 > p0)  // some row lies after a query position: mask per column
+    score_page_nt<DT, true>(nt, pg, lut, bfrag, lane, k, p0, ncol, q0, p);
+  else
+    score_page_nt<DT, false>(nt, pg, lut, bfrag, lane, k, p0, ncol, q0, p);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxIdxThreads, 1) k_indexer(const IdxParams p) {
   using S = IdxSmem<DT>;
+  constexpr int kConsumerWarps = IdxCfg<DT>::kWarps;
+  constexpr int kDepth = IdxCfg<DT>::kDepth;
+  constexpr int kIdxThreads = 32 * (kConsumerWarps + 1);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffFull);
@@ -212,7 +232,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p) {
     bool bad = false;
     for (int b = tid * per; b < min(p.B, (tid + 1) * per); ++b) local += seq_pages(p, b, &bad);
     if (bad) *bad_batch = 1;
-    __shared__ int partial[kIdxThreads + 1];
+    __shared__ int partial[kMaxIdxThreads + 1];
     partial[tid] = local;
     __syncthreads();
     if (tid == 0) {
@@ -258,8 +278,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p) {
         const int gp = start + n;
         while (prefix[b + 1] <= gp) ++b;
         const int k = gp - prefix[b];
-        const int slot = n % S::kStages;
-        const uint32_t ph = static_cast<uint32_t>(n / S::kStages) & 1u;
+        const int j = n / kConsumerWarps;  // the consumer's j-th page
+        const int slot = (n % kConsumerWarps) + kConsumerWarps * (j % kDepth);
+        const uint32_t ph = static_cast<uint32_t>(j / kDepth) & 1u;
         if (!mbar_wait_bounded(&empty[slot], ph ^ 1u, kWaitLimitNs, abort_flag)) {
           if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
           *abort_flag = 1;
@@ -280,11 +301,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p) {
         }
         issued = n + 1;
       }
-      // Never leave while a copy into this CTA's shared memory may still be in flight.
+      // Never leave while a copy into this CTA's shared memory may still be in flight: wait
+      // for the last page issued into every slot (in a normal run they have all landed).
       const int first = issued > S::kStages ? issued - S::kStages : 0;
       for (int n = first; n < issued; ++n) {
-        if (!mbar_wait_bounded(&full[n % S::kStages], static_cast<uint32_t>(n / S::kStages) & 1u, kWaitLimitNs,
-                               nullptr)) {
+        const int j = n / kConsumerWarps;
+        const int slot = (n % kConsumerWarps) + kConsumerWarps * (j % kDepth);
+        if (!mbar_wait_bounded(&full[slot], static_cast<uint32_t>(j / kDepth) & 1u, kWaitLimitNs, nullptr)) {
           set_status(p.status, MSA_ERR_TIMEOUT);
         }
       }
@@ -297,8 +320,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p) {
   uint32_t bfrag[4][4][2];
   int cur_b = -1, q0 = 0, ncol = 0, nt = 0, p0 = 0;
   for (int n = cw; n < npages; n += kConsumerWarps) {
-    const int slot = n % S::kStages;
-    const uint32_t ph = static_cast<uint32_t>(n / S::kStages) & 1u;
+    const int j = n / kConsumerWarps;
+    const int slot = cw + kConsumerWarps * (j % kDepth);
+    const uint32_t ph = static_cast<uint32_t>(j / kDepth) & 1u;
     if (!mbar_wait_bounded(&full[slot], ph, kWaitLimitNs, abort_flag)) {
       if (lane == 0) {
         if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
@@ -374,13 +398,13 @@ extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batc
     if (cudaFuncSetAttribute(k_indexer<MSA_INDEX_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MSA_ERR_CUDA;
-    k_indexer<MSA_INDEX_NVFP4><<<sms, kIdxThreads, smem, stream>>>(p);
+    k_indexer<MSA_INDEX_NVFP4><<<sms, 32 * (IdxCfg<MSA_INDEX_NVFP4>::kWarps + 1), smem, stream>>>(p);
   } else {
     const size_t smem = IdxSmem<MSA_INDEX_FP8>::bytes(p.B);
     if (cudaFuncSetAttribute(k_indexer<MSA_INDEX_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MSA_ERR_CUDA;
-    k_indexer<MSA_INDEX_FP8><<<sms, kIdxThreads, smem, stream>>>(p);
+    k_indexer<MSA_INDEX_FP8><<<sms, 32 * (IdxCfg<MSA_INDEX_FP8>::kWarps + 1), smem, stream>>>(p);
   }
   return launch_status();
 }

@@ -178,7 +178,9 @@ msa_status msa_kv_insert(const float* k, const float* v, const float* ik, int64_
  *   block_scores  [T][4][max_blocks_per_seq] fp32, device; entries k >= the sequence's
  *                 block count are not written
  *   status        device uint32, nullable: bad page ids set bit MSA_ERR_DEVICE_FAULT (the
- *                 page is then scored -inf), an inconsistent batch sets MSA_ERR_INVALID_ARG */
+ *                 page is then scored -inf), an inconsistent batch sets MSA_ERR_INVALID_ARG
+ * Returns MSA_ERR_UNSUPPORTED when cache->num_pages exceeds 2^24 (the index pool is read as
+ * one tensor of 128-byte rows). */
 msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch,
                               const msa_cache* cache, const uint8_t* index_q,
                               float* block_scores, uint32_t* status, cudaStream_t stream);

@@ -6,27 +6,38 @@
 // k with j <= p_t of  index_q[t][g] . ik_fp8[j], where ik_fp8 is the NVFP4 index key dequantised
 // to E4M3 ("NVIDIA Blackwell optimizado kernes MSA") — or the FP8 index key as is.
 //
-// GB300 design:
-//  * The whole index cache is streamed once per step (9,216 B per NVFP4 page): the kernel is
-//    HBM-bound. One persistent CTA per SM; the flattened (sequence, block) page list is split
-//    evenly over CTAs, so ragged batches stay balanced at page granularity.
-//  * Warp 0 lane 0 is the producer: one 1-D bulk async copy (cp.async.bulk, 16-B aligned,
-//    whole page) per page into a ring of shared-memory stages, completion tracked by an
-//    mbarrier transaction count; L2 evict-first since every byte is read once.
-//  * Warps 1..8 consume whole pages (8 tiles of 16 tokens): register-direct dequant (LUT in
-//    shared memory, one prmt per 4 values) straight into the A fragments of
-//    mma.sync.m16n8k32.e4m3 with tokens on M and (query token, group) columns on N — so a
-//    page's A fragments are reused by all N tiles — and the block max is kept in registers and
-//    finished with three shuffles. No block score ever leaves the SM before it is final.
-//  * The head-dim order inside an MMA is free (a dot product does not care) as long as A and B
-//    use the same one: thread t of a quad owns dims 32t..32t+31 (two scale groups, 16 code
-//    bytes), k-step s covers dims 32t+8s..32t+8s+7, so the dequantised bytes land in the A
-//    registers in element order and the B fragment is one 8-byte load of index_q.
-//  * Every wait is bounded (MSA_ERR_TIMEOUT) and every page id is checked (MSA_ERR_DEVICE_FAULT,
-//    the block is scored -inf); nothing traps.
+// GB300 design: one persistent CTA per SM; the flattened (sequence, block) page list is split
+// evenly over CTAs, so ragged batches balance at page granularity. Inside a CTA the work is a
+// warp-specialised pipeline; every hand-off is an mbarrier ring, so each role runs at its own
+// pace and the latency of one stage hides behind the depth of the rings:
+//  * producer warp: resolves 32 pages' (sequence, block, page id) at a time, the next batch's
+//    block-table loads in flight while lane 0 issues one 2-D tensor copy per 128-token index
+//    page into the stage ring (L2 evict-first: every byte is read once). The copy applies the
+//    128-byte swizzle, so the per-row loads below are free of bank conflicts;
+//  * two dequant groups of four warps take alternate pages, thread = key row = TMEM lane. An
+//    NVFP4 row becomes 128 E4M3 bytes (LUT + byte-permute) stored straight into a TMEM key
+//    tile (tcgen05.st): the tile never makes a round trip through shared memory. An FP8 page
+//    is already the tensor core's swizzled K-major tile and stays in its stage. The groups
+//    also keep each tile slot's copy of the sequence's index queries (a 32 x 128 B swizzled
+//    shared tile) current;
+//  * one MMA thread: four tcgen05.mma kind::f8f6f4 per page (M = 128 keys, N = 16 or 32
+//    (token, group) columns, K = 4 x 32) into a ring of TMEM accumulators, then commits that
+//    free the key tile and publish the scores;
+//  * two max-pool groups of four warps take alternate pages: the 16x256b TMEM load hands every
+//    thread four keys of eight columns, so a warp needs a 4-key register max and a 3-step
+//    shuffle transpose-reduce; the four warps' partial maxima meet in shared memory behind one
+//    group barrier, and 32 threads store the block scores. Keys after a query position are
+//    masked on the (rare) pages that hold them.
+// Every wait is bounded (MSA_ERR_TIMEOUT); a max-pool group leaves its loop only on a barrier
+// that reports the same decision to all its threads; every page id is checked
+// (MSA_ERR_DEVICE_FAULT, the block is scored -inf); nothing traps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "msa.h"
 #include "msa_device.cuh"
@@ -35,34 +46,43 @@
 namespace msa {
 namespace {
 
-// Stage ring: consumer warp w owns slots w, w + W, ..., w + W*(D-1) and its j-th page lives
-// in slot w + W*(j % D). Each slot thus serves one warp, in order, so a warp only ever waits
-// for the phase right after the one it consumed itself (an mbarrier's parity cannot tell a
-// phase from the one two steps earlier).
+constexpr int kDqGroups = 3;                     // dequant groups (4 warps each)
+constexpr int kEpGroups = 2;                     // max-pool groups (4 warps each)
+constexpr int kMmaWarps = 3;                     // MMA-issuing warps (pages in turn)
+constexpr int kWarpDq = 1 + kMmaWarps;           // first dequant warp
+constexpr int kWarpEp = kWarpDq + 4 * kDqGroups; // first max-pool warp
+constexpr int kIdxThreads = 32 * (kWarpEp + 4 * kEpGroups);
+constexpr int kATiles = 6;                       // TMEM key tiles (32 columns each)
+constexpr int kDTiles = 6;                       // TMEM accumulators (32 columns each)
+constexpr int kTmemCols = 512;
+constexpr int kBTile = 32 * kD;                  // 32 query rows x 128 B
+static_assert(kATiles % kDqGroups == 0 && kDTiles % kEpGroups == 0, "a ring slot serves one group");
+static_assert(kIdxThreads <= 1024, "one CTA");
+static_assert(kATiles % kMmaWarps == 0 && kDTiles % kMmaWarps == 0, "a ring slot serves one MMA warp");
+static_assert(32 * (kATiles + kDTiles) <= kTmemCols, "TMEM budget");
+
+// Page n of a CTA lives in stage n % kStages, key tile n % kATiles and accumulator
+// n % kDTiles; the ring sizes are multiples of the group counts, so every slot is used by one
+// group, in page order, and nobody ever waits on an mbarrier phase two steps ahead of the one
+// it last saw (parity cannot tell those apart).
 template <int DT>
 struct IdxCfg;
 template <>
 struct IdxCfg<MSA_INDEX_NVFP4> {
   static constexpr int kPage = kIdxPageNv;
-  static constexpr int kWarps = 8;  // consumer warps
-  static constexpr int kDepth = 2;  // pages in flight per consumer warp
-  static constexpr int kStages = kWarps * kDepth;
+  static constexpr int kStages = 18;
 };
 template <>
 struct IdxCfg<MSA_INDEX_FP8> {
   static constexpr int kPage = kIdxPageFp8;
-  static constexpr int kWarps = 6;
-  static constexpr int kDepth = 2;
-  static constexpr int kStages = kWarps * kDepth;
+  static constexpr int kStages = 9;
 };
-constexpr int kMaxIdxThreads = 32 * (8 + 1);
 
 struct IdxParams {
   int32_t B, T, maxb, max_q_len, num_pages;
   const int32_t* qsl;
   const int32_t* seq_lens;
   const int32_t* block_table;
-  const uint8_t* index_pages;
   const uint8_t* index_q;
   float* block_scores;
   uint32_t* status;
@@ -76,14 +96,26 @@ template <int DT>
 struct IdxSmem {
   static constexpr int kStages = IdxCfg<DT>::kStages;
   static constexpr int kPage = IdxCfg<DT>::kPage;
-  static constexpr size_t kStageBytes = static_cast<size_t>(kStages) * kPage;
-  static constexpr size_t kOffFull = kStageBytes;
+  static_assert(kStages % kDqGroups == 0, "a stage serves one dequant group");
+  // offsets from a 1024-byte aligned base (pages and query tiles are multiples of 1024 B)
+  static constexpr size_t kOffStage = 0;
+  static constexpr size_t kOffB = kOffStage + static_cast<size_t>(kStages) * kPage;
+  static constexpr size_t kOffFull = kOffB + static_cast<size_t>(kATiles) * kBTile;
   static constexpr size_t kOffEmpty = kOffFull + 8 * kStages;
-  static constexpr size_t kOffInfo = kOffEmpty + 8 * kStages;
-  static constexpr size_t kOffLut = kOffInfo + sizeof(SlotInfo) * kStages;
+  static constexpr size_t kOffAFull = kOffEmpty + 8 * kStages;
+  static constexpr size_t kOffAEmpty = kOffAFull + 8 * kATiles;
+  static constexpr size_t kOffDFull = kOffAEmpty + 8 * kATiles;
+  static constexpr size_t kOffDEmpty = kOffDFull + 8 * kDTiles;
+  static constexpr size_t kOffInfo = kOffDEmpty + 8 * kDTiles;
+  static constexpr size_t kOffAMeta = kOffInfo + sizeof(SlotInfo) * kStages;  // [kATiles] int2
+  static constexpr size_t kOffBTag = kOffAMeta + 8 * kATiles;                 // [kATiles][4] int
+  static constexpr size_t kOffPart = kOffBTag + 16 * kATiles;                 // [EP][2][4][32] fp32
+  static constexpr size_t kOffLut = kOffPart + 4 * kEpGroups * 2 * 4 * 32;
   static constexpr size_t kOffMisc = kOffLut + 256 * 8;
-  static constexpr size_t kOffPrefix = kOffMisc + 64;
-  static size_t bytes(int B) { return kOffPrefix + 4 * static_cast<size_t>(B + 1); }
+  static constexpr size_t kOffPtab = kOffMisc + 64;  // 32 x int4
+  static constexpr size_t kOffWarpSum = kOffPtab + 32 * 16;
+  static constexpr size_t kOffPrefix = kOffWarpSum + 4 * 32;
+  static size_t bytes(int B) { return 1024 + kOffPrefix + 4 * static_cast<size_t>(B + 1); }
 };
 
 // Pages of sequence b that the indexer scans (0 for padded or invalid rows).
@@ -98,163 +130,147 @@ __device__ __forceinline__ int seq_pages(const IdxParams& p, int b, bool* bad) {
   return ql > 0 ? ceil_div(L, kBS) : 0;
 }
 
-// Score one staged page for the N tiles of the current sequence and write its block scores.
-// NT = number of 8-column tiles (columns = q_len * 4). MASK: the page holds rows after a query
-// position (only the last page or two of a sequence), so rows are masked per column.
-template <int DT, int NT, bool MASK>
-__device__ __forceinline__ void score_page(const uint8_t* pg, const uint2* lut, const uint32_t (&bfrag)[4][4][2],
-                                           int lane, int k, int p0, int ncol, int q0, const IdxParams& p) {
-  const int gid = lane >> 2, t = lane & 3;
-  float mx[NT][2];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) mx[j][0] = mx[j][1] = -CUDART_INF_F;
-#pragma unroll 1
-  for (int tile = 0; tile < kBS / 16; ++tile) {
-    const int r0 = tile * 16 + gid, r1 = r0 + 8;
-    uint32_t a[4][4];
-    if constexpr (DT == MSA_INDEX_NVFP4) {
-      const uint4 c0 = lds128(pg + r0 * kRowCodes + t * 16);
-      const uint4 c1 = lds128(pg + r1 * kRowCodes + t * 16);
-      const uint32_t s0 = *reinterpret_cast<const uint16_t*>(pg + kScaleOff + r0 * kRowScales + 2 * t);
-      const uint32_t s1 = *reinterpret_cast<const uint16_t*>(pg + kScaleOff + r1 * kRowScales + 2 * t);
-      const uint2 e00 = lut[s0 & 0xFFu], e01 = lut[s0 >> 8], e10 = lut[s1 & 0xFFu], e11 = lut[s1 >> 8];
-      dq8(c0.x, e00, a[0][0], a[0][2]);
-      dq8(c1.x, e10, a[0][1], a[0][3]);
-      dq8(c0.y, e00, a[1][0], a[1][2]);
-      dq8(c1.y, e10, a[1][1], a[1][3]);
-      dq8(c0.z, e01, a[2][0], a[2][2]);
-      dq8(c1.z, e11, a[2][1], a[2][3]);
-      dq8(c0.w, e01, a[3][0], a[3][2]);
-      dq8(c1.w, e11, a[3][1], a[3][3]);
-    } else {
-      // 32 E4M3 bytes per row and thread; the half loaded first alternates with the row
-      // parity so the eight rows of a quarter-warp hit distinct banks.
-      const int sw = gid & 1;
-      const uint4 u0a = lds128(pg + r0 * kD + t * 32 + 16 * sw);
-      const uint4 u0b = lds128(pg + r0 * kD + t * 32 + 16 * (1 - sw));
-      const uint4 u1a = lds128(pg + r1 * kD + t * 32 + 16 * sw);
-      const uint4 u1b = lds128(pg + r1 * kD + t * 32 + 16 * (1 - sw));
-      const uint4 u0 = sw ? u0b : u0a, v0 = sw ? u0a : u0b;
-      const uint4 u1 = sw ? u1b : u1a, v1 = sw ? u1a : u1b;
-      a[0][0] = u0.x; a[0][2] = u0.y; a[1][0] = u0.z; a[1][2] = u0.w;
-      a[2][0] = v0.x; a[2][2] = v0.y; a[3][0] = v0.z; a[3][2] = v0.w;
-      a[0][1] = u1.x; a[0][3] = u1.y; a[1][1] = u1.z; a[1][3] = u1.w;
-      a[2][1] = v1.x; a[2][3] = v1.y; a[3][1] = v1.z; a[3][3] = v1.w;
-    }
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      float acc[4];
-      mma_e4m3_zc(acc, a[0][0], a[0][1], a[0][2], a[0][3], bfrag[j][0][0], bfrag[j][0][1]);
-#pragma unroll
-      for (int s = 1; s < 4; ++s) mma_e4m3(acc, a[s][0], a[s][1], a[s][2], a[s][3], bfrag[j][s][0], bfrag[j][s][1]);
-      if constexpr (MASK) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = (i < 2) ? r0 : r1;
-          const int col = j * 8 + 2 * t + (i & 1);
-          const int pos = k * kBS + row;
-          if (col >= ncol || pos > p0 + (col >> 2)) acc[i] = -CUDART_INF_F;
-        }
-      }
-      mx[j][0] = fmaxf(mx[j][0], fmaxf(acc[0], acc[2]));
-      mx[j][1] = fmaxf(mx[j][1], fmaxf(acc[1], acc[3]));
-    }
+// Sequence of global page gp: the largest b with prefix[b] <= gp.
+__device__ __forceinline__ int page_seq(const int* prefix, int B, int gp) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= gp) lo = mid; else hi = mid - 1;
   }
+  return lo;
+}
+
+// Dequantise key row r of a staged NVFP4 page (written by a 128-byte-swizzled copy) to 128
+// E4M3 bytes: w[c] holds elements 4c .. 4c+3, the TMEM A-operand layout of one row.
+__device__ __forceinline__ void dequant_row_nvfp4(const uint8_t* pg, int r, const uint2* lut, uint32_t (&w)[32]) {
+  const uint2 sc = lds64(pg + sw128_phys(static_cast<uint32_t>(kScaleOff + r * kRowScales)));
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = mx[j][e];
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      const int col = j * 8 + 2 * t + e;
-      if (gid == 0 && col < ncol) p.block_scores[static_cast<int64_t>(q0 * 4 + col) * p.maxb + k] = v;
-    }
+  for (int q = 0; q < 4; ++q) {  // 32 elements: 32q .. 32q+31, scales 2q and 2q+1
+    const uint4 c = lds128(pg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * q)));
+    const uint32_t s2 = ((q < 2) ? sc.x : sc.y) >> (16 * (q & 1));
+    const uint2 e0 = lut[s2 & 0xFFu], e1 = lut[(s2 >> 8) & 0xFFu];
+    dq8(c.x, e0, w[8 * q + 0], w[8 * q + 1]);
+    dq8(c.y, e0, w[8 * q + 2], w[8 * q + 3]);
+    dq8(c.z, e1, w[8 * q + 4], w[8 * q + 5]);
+    dq8(c.w, e1, w[8 * q + 6], w[8 * q + 7]);
   }
 }
 
-template <int DT, bool MASK>
-__device__ __forceinline__ void score_page_nt(int nt, const uint8_t* pg, const uint2* lut,
-                                              const uint32_t (&bfrag)[4][4][2], int lane, int k, int p0, int ncol,
-                                              int q0, const IdxParams& p) {
-  switch (nt) {
-    case 1: score_page<DT, 1, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    case 2: score_page<DT, 2, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    case 3: score_page<DT, 3, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
-    default: score_page<DT, 4, MASK>(pg, lut, bfrag, lane, k, p0, ncol, q0, p); break;
+// One step of a shuffle transpose-reduce: lanes l and l ^ k (k = lane bit) each keep half of
+// their values, the lower-bit lane the first half, and take the max with the partner's copy.
+template <int N>
+__device__ __forceinline__ void xreduce_step(float (&v)[8], int lane, int k) {
+  const bool up = (lane & k) != 0;
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    const float send = up ? v[c] : v[c + N];
+    const float keep = up ? v[c + N] : v[c];
+    v[c] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, k));
   }
+}
+
+// Wait on a warp's behalf: true when every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
 template <int DT>
-__device__ __forceinline__ void score_page_any(int nt, const uint8_t* pg, const uint2* lut,
-                                               const uint32_t (&bfrag)[4][4][2], int lane, int k, int p0, int ncol,
-                                               int q0, const IdxParams& p) {
-  if ((k + 1) * kBS - 1 > p0)  // some row lies after a query position: mask per column
-    score_page_nt<DT, true>(nt, pg, lut, bfrag, lane, k, p0, ncol, q0, p);
-  else
-    score_page_nt<DT, false>(nt, pg, lut, bfrag, lane, k, p0, ncol, q0, p);
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kMaxIdxThreads, 1) k_indexer(const IdxParams p) {
+__global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, const __grid_constant__ CUtensorMap tmap) {
   using S = IdxSmem<DT>;
-  constexpr int kConsumerWarps = IdxCfg<DT>::kWarps;
-  constexpr int kDepth = IdxCfg<DT>::kDepth;
-  constexpr int kIdxThreads = 32 * (kConsumerWarps + 1);
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stages = smem;
+  constexpr int kStages = S::kStages;
+  constexpr bool kNv = DT == MSA_INDEX_NVFP4;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = smem + S::kOffStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::kOffEmpty);
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + S::kOffAFull);
+  uint64_t* a_empty = reinterpret_cast<uint64_t*>(smem + S::kOffAEmpty);
+  uint64_t* d_full = reinterpret_cast<uint64_t*>(smem + S::kOffDFull);
+  uint64_t* d_empty = reinterpret_cast<uint64_t*>(smem + S::kOffDEmpty);
+  uint64_t* mma_fin = reinterpret_cast<uint64_t*>(smem + S::kOffMisc + 16);
   SlotInfo* info = reinterpret_cast<SlotInfo*>(smem + S::kOffInfo);
+  int2* ameta = reinterpret_cast<int2*>(smem + S::kOffAMeta);
+  int* btag = reinterpret_cast<int*>(smem + S::kOffBTag);
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
   int* bad_batch = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 8);
+  int* warp_sum = reinterpret_cast<int*>(smem + S::kOffWarpSum);
   int* prefix = reinterpret_cast<int*>(smem + S::kOffPrefix);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- prologue: barriers, LUT, per-sequence page prefix sums --------------------------
+  // ---- prologue: barriers, TMEM, LUT, per-sequence page prefix sums ---------------------
   if (tid == 0) {
-    for (int i = 0; i < S::kStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 4);  // NVFP4: the dequant group's 4 warps; FP8: the max-pool group's
     }
+    for (int i = 0; i < kATiles; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 4);  // the max-pool group's 4 warps, once the MMAs are done
+    }
+    for (int i = 0; i < kDTiles; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], 4);
+    }
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&mma_fin[i], 1);
     fence_mbar_init();
     *abort_flag = 0;
     *bad_batch = 0;
   }
-  if constexpr (DT == MSA_INDEX_NVFP4) build_dequant_lut(lut, tid, kIdxThreads);
+  if (tid < 4 * kATiles) btag[tid] = -1;
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if constexpr (kNv) build_dequant_lut(lut, tid, kIdxThreads);
+  __syncthreads();  // flags initialised before anyone raises them
   {
-    // chunked scan: thread i sums sequences [i*per, (i+1)*per), thread 0 scans the partials
+    // prefix[b] = pages of sequences 0 .. b-1: per-thread counts, warp scans, one scan of
+    // the warp totals
     const int per = ceil_div(p.B, kIdxThreads);
+    const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     int local = 0;
     bool bad = false;
-    for (int b = tid * per; b < min(p.B, (tid + 1) * per); ++b) local += seq_pages(p, b, &bad);
+    for (int b = b0; b < b1; ++b) {
+      const int c = seq_pages(p, b, &bad);
+      prefix[b] = c;
+      local += c;
+    }
     if (bad) *bad_batch = 1;
-    __shared__ int partial[kMaxIdxThreads + 1];
-    partial[tid] = local;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int i = 0; i < kIdxThreads; ++i) {
-        const int v = partial[i];
-        partial[i] = run;
-        run += v;
+    if (warp == 0) {
+      const int nw = kIdxThreads / 32;
+      int v = lane < nw ? warp_sum[lane] : 0, x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
       }
-      partial[kIdxThreads] = run;
+      if (lane < nw) warp_sum[lane] = x - v;  // exclusive
+      if (lane == nw - 1) prefix[p.B] = x;
+      if (lane == 0 && p.B > 0 && (p.qsl[0] != 0 || p.qsl[p.B] != p.T)) *bad_batch = 1;
     }
     __syncthreads();
-    int run = partial[tid];
-    for (int b = tid * per; b < min(p.B, (tid + 1) * per); ++b) {
+    int run = warp_sum[warp] + incl - local;
+    for (int b = b0; b < b1; ++b) {
+      const int c = prefix[b];
       prefix[b] = run;
-      bool dummy = false;
-      run += seq_pages(p, b, &dummy);
+      run += c;
     }
-    if (tid == 0) prefix[p.B] = partial[kIdxThreads];
-    if (p.qsl != nullptr && tid == 0 && p.B > 0 && (p.qsl[0] != 0 || p.qsl[p.B] != p.T)) *bad_batch = 1;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_a = tmem;                    // key tiles: columns 32a .. 32a+31
+  const uint32_t t_d = tmem + 32 * kATiles;     // accumulators
   if (blockIdx.x == 0 && tid == 0 && *bad_batch) set_status(p.status, MSA_ERR_INVALID_ARG);
 
   const int total = prefix[p.B];
@@ -263,103 +279,302 @@ __global__ void __launch_bounds__(kMaxIdxThreads, 1) k_indexer(const IdxParams p
   const int npages = end - start;
 
   if (warp == 0) {
-    // ---- producer ----------------------------------------------------------------------
-    if (lane == 0 && npages > 0) {
-      const uint64_t policy = policy_evict_first();
-      // locate the sequence of the first page
-      int lo = 0, hi = p.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= start) lo = mid; else hi = mid - 1;
+    // ---- producer ------------------------------------------------------------------------
+    int4* ptab = reinterpret_cast<int4*>(smem + S::kOffPtab);
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0) prefetch_tensormap(&tmap);
+    auto resolve = [&](int n) -> int4 {  // (sequence, block, page id) of this CTA's page n
+      if (n >= npages) return make_int4(0, 0, -1, 0);
+      const int gp = start + n;
+      const int b = page_seq(prefix, p.B, gp);
+      const int k = gp - prefix[b];
+      return make_int4(b, k, p.block_table[static_cast<int64_t>(b) * p.maxb + k], 0);
+    };
+    int4 cur = resolve(lane);
+    int issued = 0;
+    bool stop = false;
+    for (int base = 0; base < npages && !stop; base += 32) {
+      ptab[lane] = cur;
+      __syncwarp();
+      cur = resolve(base + 32 + lane);  // the next batch's loads fly while lane 0 issues
+      if (lane == 0) {
+        const int cnt = min(32, npages - base);
+        for (int u = 0; u < cnt; ++u) {
+          const int n = base + u;
+          const int slot = n % kStages;
+          const uint32_t ph = static_cast<uint32_t>(n / kStages) & 1u;
+          if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag)) {
+            if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          const int4 e = ptab[u];
+          const bool valid = e.z >= 0 && e.z < p.num_pages;
+          info[slot].b = e.x;
+          info[slot].k = e.y;
+          info[slot].valid = valid ? 1 : 0;
+          if (valid) {
+            mbar_arrive_expect_tx(&full[slot], S::kPage);
+            tma_load_2d(stages + static_cast<size_t>(slot) * S::kPage, &tmap, 0, e.z * (S::kPage / kD), &full[slot],
+                        policy);
+          } else {
+            set_status(p.status, MSA_ERR_DEVICE_FAULT);
+            mbar_arrive(&full[slot]);
+          }
+          issued = n + 1;
+        }
       }
-      int b = lo;
-      int issued = 0;
-      for (int n = 0; n < npages; ++n) {
-        const int gp = start + n;
-        while (prefix[b + 1] <= gp) ++b;
-        const int k = gp - prefix[b];
-        const int j = n / kConsumerWarps;  // the consumer's j-th page
-        const int slot = (n % kConsumerWarps) + kConsumerWarps * (j % kDepth);
-        const uint32_t ph = static_cast<uint32_t>(j / kDepth) & 1u;
-        if (!mbar_wait_bounded(&empty[slot], ph ^ 1u, kWaitLimitNs, abort_flag)) {
+      stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+      __syncwarp();
+    }
+    // Never leave while a copy into this CTA's shared memory may still be in flight: wait
+    // for the last page issued into every slot (in a normal run they have all landed).
+    if (lane == 0) {
+      for (int n = issued > kStages ? issued - kStages : 0; n < issued; ++n)
+        if (!mbar_wait_bounded(&full[n % kStages], static_cast<uint32_t>(n / kStages) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+  } else if (warp < kWarpDq) {
+    // ---- MMA issue: pages mw, mw + kMmaWarps, ...; the whole warp runs the loop (its
+    // indices stay warp-uniform), lane 0 issues -------------------------------------------------
+    constexpr uint32_t idesc = idesc_e4m3_f32(128, 32);  // rows >= 4 q_len of a query tile are zero
+    const int mw = warp - 1;
+    uint64_t* fin = mma_fin + mw;
+    int issued = 0;
+    for (int n = mw; n < npages; n += kMmaWarps) {
+      const int a = n % kATiles, d = n % kDTiles;
+      if (!warp_wait(&a_full[a], static_cast<uint32_t>(n / kATiles) & 1u, abort_flag) ||
+          !warp_wait(&d_empty[d], (static_cast<uint32_t>(n / kDTiles) & 1u) ^ 1u, abort_flag)) {
+        if (lane == 0) {
           if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
           *abort_flag = 1;
-          break;
         }
-        const int phys = p.block_table[static_cast<int64_t>(b) * p.maxb + k];
-        const bool valid = phys >= 0 && phys < p.num_pages;
-        info[slot].b = b;
-        info[slot].k = k;
-        info[slot].valid = valid ? 1 : 0;
-        if (valid) {
-          mbar_arrive_expect_tx(&full[slot], S::kPage);
-          bulk_g2s_stream(stages + static_cast<size_t>(slot) * S::kPage,
-                          p.index_pages + static_cast<int64_t>(phys) * S::kPage, S::kPage, &full[slot], policy);
-        } else {
-          set_status(p.status, MSA_ERR_DEVICE_FAULT);
-          mbar_arrive(&full[slot]);
-        }
-        issued = n + 1;
+        break;
       }
-      // Never leave while a copy into this CTA's shared memory may still be in flight: wait
-      // for the last page issued into every slot (in a normal run they have all landed).
-      const int first = issued > S::kStages ? issued - S::kStages : 0;
-      for (int n = first; n < issued; ++n) {
-        const int j = n / kConsumerWarps;
-        const int slot = (n % kConsumerWarps) + kConsumerWarps * (j % kDepth);
-        if (!mbar_wait_bounded(&full[slot], static_cast<uint32_t>(j / kDepth) & 1u, kWaitLimitNs, nullptr)) {
-          set_status(p.status, MSA_ERR_TIMEOUT);
-        }
-      }
-    }
-    return;
-  }
-
-  // ---- consumers ---------------------------------------------------------------------
-  const int cw = warp - 1;
-  uint32_t bfrag[4][4][2];
-  int cur_b = -1, q0 = 0, ncol = 0, nt = 0, p0 = 0;
-  for (int n = cw; n < npages; n += kConsumerWarps) {
-    const int j = n / kConsumerWarps;
-    const int slot = cw + kConsumerWarps * (j % kDepth);
-    const uint32_t ph = static_cast<uint32_t>(j / kDepth) & 1u;
-    if (!mbar_wait_bounded(&full[slot], ph, kWaitLimitNs, abort_flag)) {
+      tc_fence_after();
+      const bool valid = ameta[a].x != 0;
       if (lane == 0) {
-        if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      break;
-    }
-    const SlotInfo si = info[slot];
-    if (si.b != cur_b) {
-      cur_b = si.b;
-      q0 = p.qsl[cur_b];
-      const int ql = p.qsl[cur_b + 1] - q0;
-      p0 = p.seq_lens[cur_b] - ql;
-      ncol = ql * 4;
-      nt = ceil_div(ncol, 8);
-      const int gid = lane >> 2, t = lane & 3;
+        if (valid) {
+          const uint32_t b_addr = smem_u32(smem + S::kOffB) + static_cast<uint32_t>(a * kBTile);
+          const uint32_t st_addr = smem_u32(stages) + static_cast<uint32_t>((n % kStages) * S::kPage);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = j * 8 + gid;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          uint2 v = make_uint2(0u, 0u);
-          if (col < ncol) v = ldg_nc64(p.index_q + static_cast<int64_t>(q0 * 4 + col) * kD + 32 * t + 8 * s);
-          bfrag[j][s][0] = v.x;
-          bfrag[j][s][1] = v.y;
+          for (int s = 0; s < 4; ++s) {
+            if constexpr (kNv)
+              tc_mma_f8_ta(t_d + 32 * d, t_a + 32 * a + 8 * s, sw128_kmajor_desc(b_addr + 32 * s), idesc,
+                           s > 0 ? 1u : 0u);
+            else
+              tc_mma_f8(t_d + 32 * d, sw128_kmajor_desc(st_addr + 32 * s), sw128_kmajor_desc(b_addr + 32 * s), idesc,
+                        s > 0 ? 1u : 0u);
+          }
+          tc_commit(&d_full[d]);  // also tells the max-pool group the key tile (and FP8 stage) is free
+        } else {
+          mbar_arrive(&d_full[d]);
         }
       }
+      __syncwarp();
+      issued = n + 1;
     }
-    const uint8_t* pg = stages + static_cast<size_t>(slot) * S::kPage;
-    if (si.valid) {
-      score_page_any<DT>(nt, pg, lut, bfrag, lane, si.k, p0, ncol, q0, p);
-    } else if (lane < ncol) {
-      p.block_scores[static_cast<int64_t>(q0 * 4 + lane) * p.maxb + si.k] = -CUDART_INF_F;
+    // every MMA has completed before TMEM is released
+    if (lane == 0 && issued > 0) {
+      tc_commit(fin);
+      if (!mbar_wait_bounded(fin, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+  } else if (warp < kWarpEp) {
+    // ---- dequant groups: pages dq, dq + 2, ... ------------------------------------------------
+    const int dq = (warp - kWarpDq) >> 2;
+    const int wq = warp & 3;        // TMEM lane quarter this warp may access
+    const int i = 32 * wq + lane;   // key row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
+    int cur_b = -1, q0 = 0, ncol = 0;
+    for (int n = dq; n < npages; n += kDqGroups) {
+      const int s = n % kStages, a = n % kATiles;
+      if (!warp_wait(&full[s], static_cast<uint32_t>(n / kStages) & 1u, abort_flag)) break;
+      const SlotInfo si = info[s];
+      uint32_t w[32];
+      if constexpr (kNv) {
+        if (si.valid) dequant_row_nvfp4(stages + static_cast<size_t>(s) * S::kPage, i, lut, w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the warp's reads of the stage are done
+      }
+      if (!warp_wait(&a_empty[a], (static_cast<uint32_t>(n / kATiles) & 1u) ^ 1u, abort_flag)) break;
+      tc_fence_after();
+      if (si.b != cur_b) {
+        cur_b = si.b;
+        q0 = p.qsl[cur_b];
+        ncol = 4 * (p.qsl[cur_b + 1] - q0);
+      }
+      int* tag = btag + 4 * a + wq;
+      if (*tag != cur_b) {
+        // this warp's 8 rows of the slot's query tile: rows c < 4 * q_len, zero rows up to 32
+        uint8_t* btile = smem + S::kOffB + static_cast<size_t>(a) * kBTile;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int id = 64 * wq + 2 * lane + u;  // 256 chunks of 16 B
+          const int row = id >> 3, c = id & 7;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (row < ncol)
+            v = *reinterpret_cast<const uint4*>(p.index_q + static_cast<int64_t>(q0 * 4 + row) * kD + 16 * c);
+          *reinterpret_cast<uint4*>(btile + sw128_chunk_off(row, c)) = v;
+        }
+        fence_proxy_async_smem();  // visible to the tensor core
+        __syncwarp();
+        if (lane == 0) *tag = cur_b;
+      }
+      if constexpr (kNv) {
+        if (si.valid) tmem_st32(t_a + 32 * a + lane_base, w);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      if (wq == 0 && lane == 0) ameta[a] = make_int2(si.valid, ncol);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[a]);
+    }
+  } else {
+    // ---- max-pool groups: pages ep, ep + 2, ... ---------------------------------------------
+    const int ep = (warp - kWarpEp) >> 2;
+    const int wq = warp & 3;
+    const int i = 32 * wq + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
+    float* part = reinterpret_cast<float*>(smem + S::kOffPart) + ep * 256;  // [2][4 quarters][32]
+    const int bar_id = 1 + ep;
+    // lane l holds the facts of the group's page (base + l): block, first column row, columns,
+    // first query position, page id valid
+    int m_k = 0, m_q0 = 0, m_ncol = 0, m_p0 = 0, m_valid = 0;
+    bool fail = false;
+    int j = 0;
+    for (int n = ep; n < npages; n += kEpGroups, ++j) {
+      if ((j & 31) == 0) {
+        const int nn = n + kEpGroups * lane;
+        if (nn < npages) {
+          const int gp = start + nn;
+          const int b = page_seq(prefix, p.B, gp);
+          m_k = gp - prefix[b];
+          m_q0 = p.qsl[b];
+          const int ql = p.qsl[b + 1] - m_q0;
+          m_ncol = 4 * ql;
+          m_p0 = p.seq_lens[b] - ql;
+          const int phys = p.block_table[static_cast<int64_t>(b) * p.maxb + m_k];
+          m_valid = phys >= 0 && phys < p.num_pages;
+        }
+      }
+      const int src = j & 31;
+      const int k = __shfl_sync(0xffffffffu, m_k, src), q0 = __shfl_sync(0xffffffffu, m_q0, src);
+      const int ncol = __shfl_sync(0xffffffffu, m_ncol, src), p0 = __shfl_sync(0xffffffffu, m_p0, src);
+      const bool valid = __shfl_sync(0xffffffffu, m_valid, src) != 0;
+      const int d = n % kDTiles;
+      const bool ready = warp_wait(&d_full[d], static_cast<uint32_t>(n / kDTiles) & 1u, abort_flag);
+      if (!ready) fail = true;
+      float v[8];
+      if (ready) {
+        tc_fence_after();
+        if (lane == 0) {  // the MMAs are done: their key tile (and FP8 stage) may be refilled
+          mbar_arrive(&a_empty[n % kATiles]);
+          if constexpr (!kNv) mbar_arrive(&empty[n % kStages]);
+        }
+        uint32_t a[16], b[16];
+        if (valid) {
+          const uint32_t taddr = t_d + 32 * d + lane_base;
+          tmem_ld16x256_x4(taddr, a);
+          tmem_ld16x256_x4(taddr + (16u << 16), b);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&d_empty[d]);  // the accumulator may be overwritten
+        if (valid) {
+          if ((k + 1) * kBS - 1 > p0) {  // keys after a query position are masked per column
+            const int pos = k * kBS + 32 * wq + (lane >> 2);  // key of a[0]
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = 8 * (e >> 2) + 2 * (lane & 3) + (e & 1);
+              const int row = 8 * ((e >> 1) & 1);
+              const int lim = p0 + (col >> 2);
+              if (pos + row > lim) a[e] = __float_as_uint(-CUDART_INF_F);
+              if (pos + row + 16 > lim) b[e] = __float_as_uint(-CUDART_INF_F);
+            }
+          }
+          // v[2o + e]: column 8o + 2(lane % 4) + e, max over this thread's 4 keys
+#pragma unroll
+          for (int o = 0; o < 4; ++o)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              v[2 * o + e] = fmaxf(max3f(__uint_as_float(a[4 * o + e]), __uint_as_float(a[4 * o + 2 + e]),
+                                         __uint_as_float(b[4 * o + e])),
+                                   __uint_as_float(b[4 * o + 2 + e]));
+          // the 8 lanes with equal lane % 4 hold the same columns: reduce over lane bits 4, 3, 2
+          xreduce_step<4>(v, lane, 16);
+          xreduce_step<2>(v, lane, 8);
+          xreduce_step<1>(v, lane, 4);
+          const int col = 16 * ((lane >> 4) & 1) + 8 * ((lane >> 3) & 1) + 2 * (lane & 3) + ((lane >> 2) & 1);
+          part[(j & 1) * 128 + wq * 32 + col] = v[0];
+        }
+      }
+      if (fail) *abort_flag = 1;
+      if (named_barrier_or(bar_id, 128, fail || *abort_flag != 0)) break;
+      if (i < ncol) {
+        float m = -CUDART_INF_F;
+        if (valid) {
+          const float* s4 = part + (j & 1) * 128;
+          m = fmaxf(fmaxf(s4[i], s4[32 + i]), fmaxf(s4[64 + i], s4[96 + i]));
+        }
+        p.block_scores[static_cast<int64_t>(q0 * 4 + i) * p.maxb + k] = m;
+      }
+    }
   }
+  if (tid == 0 || (warp >= kWarpDq && lane == 0)) {
+    if (*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once per process.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// The page pool as a 2-D byte tensor of 128-byte rows (page p = rows p*R .. p*R + R-1), box =
+// one page, 128-byte swizzle.
+bool page_tensor_map(CUtensorMap* m, const uint8_t* base, int num_pages, int page_bytes) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const int rows = page_bytes / kD;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
+                              static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1) * static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DT>
+msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t stream) {
+  CUtensorMap tmap;
+  if (!page_tensor_map(&tmap, pages, p.num_pages, IdxCfg<DT>::kPage)) return MSA_ERR_CUDA;
+  const int sms = msa_host::num_sms();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  const size_t smem = IdxSmem<DT>::bytes(p.B);
+  if (cudaFuncSetAttribute(k_indexer<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return MSA_ERR_CUDA;
+  k_indexer<DT><<<sms, kIdxThreads, smem, stream>>>(p, tmap);
+  return msa_host::launch_status();
 }
 
 }  // namespace
@@ -378,8 +593,7 @@ extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batc
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (index_q == nullptr || block_scores == nullptr || !aligned(index_q, 16) || !aligned(block_scores, 4))
     return MSA_ERR_INVALID_ARG;
-  const int sms = num_sms();
-  if (sms <= 0) return MSA_ERR_CUDA;
+  if (cache->num_pages > (1 << 24)) return MSA_ERR_UNSUPPORTED;  // page rows index a 2^31-row tensor
   IdxParams p;
   p.B = batch->B;
   p.T = batch->T;
@@ -389,22 +603,9 @@ extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batc
   p.qsl = batch->query_start_loc;
   p.seq_lens = batch->seq_lens;
   p.block_table = batch->block_table;
-  p.index_pages = cache->index_pages;
   p.index_q = index_q;
   p.block_scores = block_scores;
   p.status = status;
-  if (cache->index_dtype == MSA_INDEX_NVFP4) {
-    const size_t smem = IdxSmem<MSA_INDEX_NVFP4>::bytes(p.B);
-    if (cudaFuncSetAttribute(k_indexer<MSA_INDEX_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MSA_ERR_CUDA;
-    k_indexer<MSA_INDEX_NVFP4><<<sms, 32 * (IdxCfg<MSA_INDEX_NVFP4>::kWarps + 1), smem, stream>>>(p);
-  } else {
-    const size_t smem = IdxSmem<MSA_INDEX_FP8>::bytes(p.B);
-    if (cudaFuncSetAttribute(k_indexer<MSA_INDEX_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MSA_ERR_CUDA;
-    k_indexer<MSA_INDEX_FP8><<<sms, 32 * (IdxCfg<MSA_INDEX_FP8>::kWarps + 1), smem, stream>>>(p);
-  }
-  return launch_status();
+  if (cache->index_dtype == MSA_INDEX_NVFP4) return launch_indexer<MSA_INDEX_NVFP4>(p, cache->index_pages, stream);
+  return launch_indexer<MSA_INDEX_FP8>(p, cache->index_pages, stream);
 }

@@ -65,6 +65,10 @@ inline int auto_splits(int T) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// A 2-D tensor map (CUtensorMap, 64-B aligned storage) over `rows` rows of 128 bytes at `base`
+// (16-B aligned), box = `box_rows` rows, 128-byte swizzle (defined in msa_indexer.cu).
+bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32_t box_rows);
+
 }  // namespace msa_host
 
 // Launchers implemented in the kernel translation units.

@@ -547,26 +547,34 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The page pool as a 2-D byte tensor of 128-byte rows (page p = rows p*R .. p*R + R-1), box =
-// one page, 128-byte swizzle.
-bool page_tensor_map(CUtensorMap* m, const uint8_t* base, int num_pages, int page_bytes) {
-  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  const int rows = page_bytes / kD;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
-                              static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1) * static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(rows)};
+}  // namespace
+}  // namespace msa
+
+namespace msa_host {
+bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = msa::tensor_map_encoder();
+  if (enc == nullptr || rows == 0 || rows > (1ull << 32) || box_rows == 0 || box_rows > 256) return false;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(static_cast<CUtensorMap*>(tmap64), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+}  // namespace msa_host
+
+namespace msa {
+namespace {
 
 template <int DT>
 msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t stream) {
+  // the index pool as rows of 128 B, one page per box
   CUtensorMap tmap;
-  if (!page_tensor_map(&tmap, pages, p.num_pages, IdxCfg<DT>::kPage)) return MSA_ERR_CUDA;
+  constexpr uint32_t kRows = IdxCfg<DT>::kPage / kD;
+  if (!msa_host::rows128_tensor_map(&tmap, pages, static_cast<uint64_t>(p.num_pages > 0 ? p.num_pages : 1) * kRows,
+                                    kRows))
+    return MSA_ERR_CUDA;
   const int sms = msa_host::num_sms();
   if (sms <= 0) return MSA_ERR_CUDA;
   const size_t smem = IdxSmem<DT>::bytes(p.B);

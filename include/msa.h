@@ -185,6 +185,15 @@ msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch,
                               const msa_cache* cache, const uint8_t* index_q,
                               float* block_scores, uint32_t* status, cudaStream_t stream);
 
+/* The indexer over one context shard ("Indexador NVFP4 DCP": the context is split across ranks
+ * by block range): as msa_indexer_decode, but only blocks block_begin <= k < block_end of each
+ * sequence are scanned and written (the others are left untouched). msa_indexer_decode is the
+ * range [0, 2^31 - 1). block_begin < 0 or block_end < block_begin: MSA_ERR_INVALID_ARG. */
+msa_status msa_indexer_decode_range(const msa_geometry* geo, const msa_batch* batch,
+                                    const msa_cache* cache, const uint8_t* index_q,
+                                    int32_t block_begin, int32_t block_end,
+                                    float* block_scores, uint32_t* status, cudaStream_t stream);
+
 /* Per-group block selection ("MSA primer"; "MSA 机制详解"). For token t at position p_t,
  * local = p_t / 128. sel[t][g][0] = local; sel[t][g][1..15] = the 15 highest-scoring blocks
  * among 0 .. local-1, in descending score order, equal scores ordered by lower block id
@@ -194,6 +203,37 @@ msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch,
 msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* batch,
                            const float* block_scores, int32_t* sel, uint32_t* status,
                            cudaStream_t stream);
+
+/* Context-sharded selection ("Indexador NVFP4 DCP": each rank keeps its own best blocks and
+ * one gather brings them to the rank that owns the query; scores are per block, so the merge
+ * is exact). A candidate is the 64-bit key (order-preserving bits of the fp32 score << 32 |
+ * ~block id; NaN ranks as -inf, -0 as +0), so one integer order is "score descending, lower
+ * block id first"; 0 = no candidate.
+ *
+ * msa_topk_candidates: for every (t, g) row, the 15 largest keys among blocks
+ * block_begin <= k < min(block_end, local) (local = p_t / 128 is never a candidate), descending,
+ * 0-padded.
+ *   block_scores [T][4][max_blocks_per_seq] fp32, device (only the shard's range is read)
+ *   cand         [T][4][15] uint64, device */
+msa_status msa_topk_candidates(const msa_geometry* geo, const msa_batch* batch,
+                               const float* block_scores, int32_t block_begin, int32_t block_end,
+                               uint64_t* cand, uint32_t* status, cudaStream_t stream);
+
+/* msa_topk_merge: sel[t][g] = [local, the 15 largest keys over the n_shards candidate lists as
+ * block ids, -1 padded] -- for shards that partition blocks 0 .. local-1 this equals
+ * msa_topk_blocks bit for bit.
+ *   cand  [n_shards][T][4][15] uint64, device; 1 <= n_shards <= 256
+ *   sel   [T][4][16] int32, device */
+msa_status msa_topk_merge(const msa_geometry* geo, const msa_batch* batch, const uint64_t* cand,
+                          int32_t n_shards, int32_t* sel, uint32_t* status, cudaStream_t stream);
+
+/* Host-memory versions of the two (synchronous, no GPU): rows = T x 4, local[rows] the rows'
+ * local blocks (a negative local marks a row to skip: no candidates, sel all -1). */
+msa_status msa_topk_candidates_host(const float* block_scores, int64_t rows,
+                                    int32_t max_blocks_per_seq, const int32_t* local,
+                                    int32_t block_begin, int32_t block_end, uint64_t* cand);
+msa_status msa_topk_merge_host(const uint64_t* cand, int32_t n_shards, int64_t rows,
+                               const int32_t* local, int32_t* sel);
 
 /* Workspace bytes msa_sparse_attn_decode needs for num_splits partial results per token
  * (num_splits 0 = the automatic choice, which never exceeds 16). */

@@ -11,6 +11,7 @@ import ctypes
 import os
 from typing import Optional
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +75,11 @@ _SIGS = {
     "msa_kv_insert": (_I32, [_P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _P, _P]),
     "msa_indexer_decode": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
     "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
+    "msa_indexer_decode_range": (_I32, [_GP, _BP, _CP, _P, _I32, _I32, _P, _P, _P]),
+    "msa_topk_candidates": (_I32, [_GP, _BP, _P, _I32, _I32, _P, _P, _P]),
+    "msa_topk_merge": (_I32, [_GP, _BP, _P, _I32, _P, _P, _P]),
+    "msa_topk_candidates_host": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P]),
+    "msa_topk_merge_host": (_I32, [_P, _I32, _I64, _P, _P]),
     "msa_attn_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_sparse_attn_decode": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _SZ, _P, _P, _P]),
     "msa_sparse_attn_decode_noalloc": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _P, _P]),
@@ -200,6 +206,50 @@ def msa_topk_blocks(batch: Batch, block_scores: torch.Tensor, sel: torch.Tensor,
                     status: Optional[torch.Tensor] = None) -> None:
     _check(_lib.msa_topk_blocks(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(block_scores), _ptr(sel),
                                 _ptr(status), _stream()), "msa_topk_blocks")
+
+
+def msa_indexer_decode_range(batch: Batch, cache: Cache, index_q: torch.Tensor, block_begin: int, block_end: int,
+                             block_scores: torch.Tensor, status: Optional[torch.Tensor] = None) -> None:
+    """The indexer over one context shard: blocks block_begin <= k < block_end of every sequence."""
+    _check(_lib.msa_indexer_decode_range(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                         _ptr(index_q), int(block_begin), int(block_end), _ptr(block_scores),
+                                         _ptr(status), _stream()), "msa_indexer_decode_range")
+
+
+def msa_topk_candidates(batch: Batch, block_scores: torch.Tensor, block_begin: int, block_end: int,
+                        cand: torch.Tensor, status: Optional[torch.Tensor] = None) -> None:
+    """A context shard's 15 best non-local blocks per (t, g) as 64-bit keys (int64 tensor [T, 4, 15])."""
+    _check(_lib.msa_topk_candidates(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(block_scores),
+                                    int(block_begin), int(block_end), _ptr(cand), _ptr(status), _stream()),
+           "msa_topk_candidates")
+
+
+def msa_topk_merge(batch: Batch, cand: torch.Tensor, n_shards: int, sel: torch.Tensor,
+                   status: Optional[torch.Tensor] = None) -> None:
+    """The owner's merge of n_shards candidate lists ([n_shards, T, 4, 15]) into sel [T, 4, 16]."""
+    _check(_lib.msa_topk_merge(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(cand), int(n_shards), _ptr(sel),
+                               _ptr(status), _stream()), "msa_topk_merge")
+
+
+def msa_topk_candidates_host(block_scores: np.ndarray, local: np.ndarray, block_begin: int,
+                             block_end: int) -> np.ndarray:
+    """Host version of msa_topk_candidates: block_scores float32 [rows, maxb], local int32 [rows]."""
+    sc = np.ascontiguousarray(block_scores, dtype=np.float32)
+    lc = np.ascontiguousarray(local, dtype=np.int32)
+    out = np.zeros((sc.shape[0], 15), dtype=np.uint64)
+    _check(_lib.msa_topk_candidates_host(sc.ctypes.data, sc.shape[0], sc.shape[1], lc.ctypes.data, int(block_begin),
+                                         int(block_end), out.ctypes.data), "msa_topk_candidates_host")
+    return out
+
+
+def msa_topk_merge_host(cand: np.ndarray, local: np.ndarray) -> np.ndarray:
+    """Host version of msa_topk_merge: cand uint64 [n_shards, rows, 15], local int32 [rows]."""
+    cd = np.ascontiguousarray(cand, dtype=np.uint64)
+    lc = np.ascontiguousarray(local, dtype=np.int32)
+    out = np.zeros((cd.shape[1], 16), dtype=np.int32)
+    _check(_lib.msa_topk_merge_host(cd.ctypes.data, cd.shape[0], cd.shape[1], lc.ctypes.data, out.ctypes.data),
+           "msa_topk_merge_host")
+    return out
 
 
 def msa_attn_workspace_size(B: int, T: int, num_splits: int = 0) -> int:

@@ -80,6 +80,7 @@ struct IdxCfg<MSA_INDEX_FP8> {
 
 struct IdxParams {
   int32_t B, T, maxb, max_q_len, num_pages;
+  int32_t kb, ke;  // the scanned block range [kb, ke) of every sequence (a context shard)
   const int32_t* qsl;
   const int32_t* seq_lens;
   const int32_t* block_table;
@@ -127,7 +128,8 @@ __device__ __forceinline__ int seq_pages(const IdxParams& p, int b, bool* bad) {
     *bad = true;
     return 0;
   }
-  return ql > 0 ? ceil_div(L, kBS) : 0;
+  const int nb = ql > 0 ? ceil_div(L, kBS) : 0;
+  return max(0, min(p.ke, nb) - min(p.kb, nb));
 }
 
 // Sequence of global page gp: the largest b with prefix[b] <= gp.
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       if (n >= npages) return make_int4(0, 0, -1, 0);
       const int gp = start + n;
       const int b = page_seq(prefix, p.B, gp);
-      const int k = gp - prefix[b];
+      const int k = p.kb + gp - prefix[b];
       return make_int4(b, k, p.block_table[static_cast<int64_t>(b) * p.maxb + k], 0);
     };
     int4 cur = resolve(lane);
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         if (nn < npages) {
           const int gp = start + nn;
           const int b = page_seq(prefix, p.B, gp);
-          m_k = gp - prefix[b];
+          m_k = p.kb + gp - prefix[b];
           m_q0 = p.qsl[b];
           const int ql = p.qsl[b + 1] - m_q0;
           m_ncol = 4 * ql;
@@ -591,14 +593,15 @@ msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t
 using namespace msa;
 using namespace msa_host;
 
-extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
-                                         const uint8_t* index_q, float* block_scores, uint32_t* status,
-                                         cudaStream_t stream) {
+extern "C" msa_status msa_indexer_decode_range(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                               const uint8_t* index_q, int32_t block_begin, int32_t block_end,
+                                               float* block_scores, uint32_t* status, cudaStream_t stream) {
   msa_status st = check_geometry(geo);
   if (st != MSA_OK) return st;
   if ((st = check_batch(batch)) != MSA_OK) return st;
   if ((st = check_cache(cache, true, false)) != MSA_OK) return st;
-  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  if (block_begin < 0 || block_end < block_begin) return MSA_ERR_INVALID_ARG;
+  if (batch->B == 0 || batch->T == 0 || block_end == block_begin) return MSA_OK;
   if (index_q == nullptr || block_scores == nullptr || !aligned(index_q, 16) || !aligned(block_scores, 4))
     return MSA_ERR_INVALID_ARG;
   if (cache->num_pages > (1 << 24)) return MSA_ERR_UNSUPPORTED;  // page rows index a 2^31-row tensor
@@ -608,6 +611,8 @@ extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batc
   p.maxb = batch->max_blocks_per_seq;
   p.max_q_len = batch->max_q_len;
   p.num_pages = cache->num_pages;
+  p.kb = block_begin;
+  p.ke = block_end;
   p.qsl = batch->query_start_loc;
   p.seq_lens = batch->seq_lens;
   p.block_table = batch->block_table;
@@ -616,4 +621,10 @@ extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batc
   p.status = status;
   if (cache->index_dtype == MSA_INDEX_NVFP4) return launch_indexer<MSA_INDEX_NVFP4>(p, cache->index_pages, stream);
   return launch_indexer<MSA_INDEX_FP8>(p, cache->index_pages, stream);
+}
+
+extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                         const uint8_t* index_q, float* block_scores, uint32_t* status,
+                                         cudaStream_t stream) {
+  return msa_indexer_decode_range(geo, batch, cache, index_q, 0, 0x7FFFFFFF, block_scores, status, stream);
 }

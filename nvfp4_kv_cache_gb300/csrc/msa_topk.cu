@@ -15,6 +15,10 @@
 // are the only input, so GPU selection == the oracle's sort on the same scores, bit for bit.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "msa.h"
 #include "msa_device.cuh"
@@ -25,15 +29,16 @@ namespace {
 
 constexpr int kKeysPerLane = 16;
 
-__device__ __forceinline__ uint64_t score_key(float s, int id) {
-  uint32_t u = __float_as_uint(s);
+__host__ __device__ inline uint64_t score_key(float s, int id) {
+  uint32_t u;
+  memcpy(&u, &s, 4);
   if (s != s) u = 0xFF800000u;   // NaN ranks as -inf
   if (s == 0.0f) u = 0u;         // -0 == +0
   const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(id));
 }
 
-__device__ __forceinline__ int key_id(uint64_t key) {
+__host__ __device__ inline int key_id(uint64_t key) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
 }
 
@@ -125,17 +130,69 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t k, int lane) {
 
 constexpr int kRowsPerCta = 8;
 constexpr int kSurvivors = 64;
+constexpr int kCand = kSel - 1;  // candidates per (token, group) and shard: the 15 best non-local blocks
 
-// One warp per (token, group) row. The 15 largest keys are all >= tau, the 15th largest of
-// the 32 lane maxima (15 distinct elements reach it); the survivors of that filter (usually
-// a few dozen) are sorted in registers. More than 64 survivors (adversarial ties across
-// lanes) fall back to repeated warp argmax over the whole row.
-__global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
-  __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kRowsPerCta + warp;  // t * 4 + g
-  if (row >= p.T * 4) return;
-  const int t = row >> 2;
+// The 15 largest of the n keys key_at(0 .. n-1) (unique; 0 = none), descending, into res[0..14]
+// (0 past the end). One warp. The 15th largest of the 32 lane maxima bounds the 15th largest key
+// (15 distinct elements reach it), so only keys at or above it survive (typically a few
+// dozen) and those are sorted in registers; more than 64 survivors (adversarial ties across
+// lanes) fall back to repeated warp argmax.
+template <class KeyAt>
+__device__ void top15_keys(KeyAt key_at, int n, uint64_t* buf, uint64_t* res, int lane) {
+  uint64_t k0 = 0, k1 = 0;
+  bool sorted = false;
+  if (n <= kSurvivors) {
+    k0 = 2 * lane < n ? key_at(2 * lane) : 0ull;
+    k1 = 2 * lane + 1 < n ? key_at(2 * lane + 1) : 0ull;
+    sorted = true;
+  } else {
+    uint64_t best = 0;
+    for (int i = lane; i < n; i += 32) {
+      const uint64_t k = key_at(i);
+      best = k > best ? k : best;
+    }
+    const uint64_t tau = __shfl_sync(0xffffffffu, warp_sort32_desc(best, lane), 14);
+    int count = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const uint64_t k = i < n ? key_at(i) : 0ull;
+      const bool keep = k >= tau && k != 0ull;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      const int pos = count + __popc(m & ((1u << lane) - 1u));
+      if (keep && pos < kSurvivors) buf[pos] = k;
+      count += __popc(m);
+    }
+    __syncwarp();
+    if (count <= kSurvivors) {
+      k0 = 2 * lane < count ? buf[2 * lane] : 0ull;
+      k1 = 2 * lane + 1 < count ? buf[2 * lane + 1] : 0ull;
+      sorted = true;
+    }
+    __syncwarp();
+  }
+  if (sorted) {
+    warp_sort64_desc(k0, k1, lane);  // elements 2 lane, 2 lane + 1 of the sorted run
+    if (2 * lane < kCand) res[2 * lane] = k0;
+    if (2 * lane + 1 < kCand) res[2 * lane + 1] = k1;
+  } else {
+    uint64_t top = 0;  // repeated warp argmax, 16 keys per lane per pass, running top 15 carried
+    for (int c0 = 0; c0 < n; c0 += 32 * kKeysPerLane) {
+      uint64_t keys[kKeysPerLane];
+#pragma unroll
+      for (int i = 0; i < kKeysPerLane; ++i) {
+        const int id = c0 + i * 32 + lane;
+        keys[i] = id < n ? key_at(id) : 0ull;
+      }
+      top = warp_pop15(keys, lane < kCand ? top : 0ull, lane);
+    }
+    if (lane < kCand) res[lane] = top;
+  }
+  __syncwarp();
+}
+
+// Row (t, g) of the batch: its sequence, and local = p_t / 128 for a consistent row (-1 else,
+// with MSA_ERR_INVALID_ARG raised).
+__device__ __forceinline__ int row_local(const TopkParams& p, int t) {
   int lo = 0, hi = p.B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -143,93 +200,206 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
   }
   const int q0 = p.qsl[lo], ql = p.qsl[lo + 1] - q0;
   const int L = p.seq_lens[lo];
+  if (!(t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) return -1;
+  return (L - ql + (t - q0)) / kBS;
+}
+
+// One warp per (token, group) row: sel = [local, the 15 best of blocks 0 .. local-1].
+__global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
+  __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
+  __shared__ uint64_t res[kRowsPerCta][kCand];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerCta + warp;  // t * 4 + g
+  if (row >= p.T * 4) return;
   int32_t* out = p.sel + static_cast<int64_t>(row) * kSel;
-  if (!(t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) {
+  const int local = row_local(p, row >> 2);
+  if (local < 0) {
     if (lane == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
     if (lane < kSel) out[lane] = -1;
     return;
   }
-  const int local = (L - ql + (t - q0)) / kBS;
-  const int ncand = local;
   const float* s = p.scores + static_cast<int64_t>(row) * p.maxb;
-  uint64_t k0 = 0, k1 = 0;
-  bool sorted = false;
-  if (ncand <= kSurvivors) {
-    const int i0 = 2 * lane, i1 = 2 * lane + 1;
-    k0 = i0 < ncand ? score_key(s[i0], i0) : 0ull;
-    k1 = i1 < ncand ? score_key(s[i1], i1) : 0ull;
-    sorted = true;
-  } else {
-    uint64_t best = 0;
-    for (int i = lane; i < ncand; i += 32) {
-      const uint64_t k = score_key(s[i], i);
-      best = k > best ? k : best;
-    }
-    const uint64_t tau = __shfl_sync(0xffffffffu, warp_sort32_desc(best, lane), 14);
-    int count = 0;
-    for (int base = 0; base < ncand; base += 32) {
-      const int i = base + lane;
-      const uint64_t k = i < ncand ? score_key(s[i], i) : 0ull;
-      const bool keep = k >= tau && k != 0ull;
-      const uint32_t m = __ballot_sync(0xffffffffu, keep);
-      const int pos = count + __popc(m & ((1u << lane) - 1u));
-      if (keep && pos < kSurvivors) buf[warp][pos] = k;
-      count += __popc(m);
-    }
-    __syncwarp();
-    if (count <= kSurvivors) {
-      k0 = 2 * lane < count ? buf[warp][2 * lane] : 0ull;
-      k1 = 2 * lane + 1 < count ? buf[warp][2 * lane + 1] : 0ull;
-      sorted = true;
-    }
-  }
-  if (sorted) {
-    warp_sort64_desc(k0, k1, lane);
-    // elements 0..14 of the sorted run: lane l holds 2l and 2l+1
-    if (lane == 0) out[0] = local;
-    if (2 * lane < 15) out[1 + 2 * lane] = k0 ? key_id(k0) : -1;
-    if (2 * lane + 1 < 15) out[2 + 2 * lane] = k1 ? key_id(k1) : -1;
-    return;
-  }
-  // fallback: repeated warp argmax, 16 keys per lane per pass, running top-15 carried
-  uint64_t top = 0;
-  for (int c0 = 0; c0 < ncand; c0 += 32 * kKeysPerLane) {
-    uint64_t keys[kKeysPerLane];
-#pragma unroll
-    for (int i = 0; i < kKeysPerLane; ++i) {
-      const int id = c0 + i * 32 + lane;
-      keys[i] = id < ncand ? score_key(s[id], id) : 0ull;
-    }
-    top = warp_pop15(keys, lane < 15 ? top : 0ull, lane);
-  }
+  top15_keys([&](int i) { return score_key(s[i], i); }, local, buf[warp], res[warp], lane);
   if (lane == 0) out[0] = local;
-  if (lane < 15) out[1 + lane] = top ? key_id(top) : -1;
+  if (lane < kCand) out[1 + lane] = res[warp][lane] ? key_id(res[warp][lane]) : -1;
 }
 
+struct CandParams {
+  TopkParams t;
+  int32_t kb, ke;        // this shard's block range
+  int32_t n_shards;      // merge: candidate lists per row
+  uint64_t* cand;        // [rows][15] (candidates) or [n_shards][rows][15] (merge)
+  const uint64_t* cand_in;
+};
+
+// A context shard's candidates: per row the 15 best of its non-local blocks in [kb, ke), as
+// keys, descending (0 = none).
+__global__ void __launch_bounds__(32 * kRowsPerCta) k_topk_cand(const CandParams c) {
+  __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
+  __shared__ uint64_t res[kRowsPerCta][kCand];
+  const TopkParams& p = c.t;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerCta + warp;
+  if (row >= p.T * 4) return;
+  uint64_t* out = c.cand + static_cast<int64_t>(row) * kCand;
+  const int local = row_local(p, row >> 2);
+  if (local < 0) {
+    if (lane == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+    if (lane < kCand) out[lane] = 0ull;
+    return;
+  }
+  const int lo = min(c.kb, local), n = max(0, min(c.ke, local) - lo);
+  const float* s = p.scores + static_cast<int64_t>(row) * p.maxb;
+  top15_keys([&](int i) { return score_key(s[lo + i], lo + i); }, n, buf[warp], res[warp], lane);
+  if (lane < kCand) out[lane] = res[warp][lane];
+}
+
+// The owner's merge: per row the 15 best of the shards' n_shards x 15 candidates, behind local.
+__global__ void __launch_bounds__(32 * kRowsPerCta) k_topk_merge(const CandParams c) {
+  __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
+  __shared__ uint64_t res[kRowsPerCta][kCand];
+  const TopkParams& p = c.t;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerCta + warp;
+  if (row >= p.T * 4) return;
+  int32_t* out = p.sel + static_cast<int64_t>(row) * kSel;
+  const int local = row_local(p, row >> 2);
+  if (local < 0) {
+    if (lane == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+    if (lane < kSel) out[lane] = -1;
+    return;
+  }
+  const int64_t rows = static_cast<int64_t>(p.T) * 4;
+  const uint64_t* cin = c.cand_in + static_cast<int64_t>(row) * kCand;
+  top15_keys([&](int i) { return cin[static_cast<int64_t>(i / kCand) * rows * kCand + i % kCand]; },
+             c.n_shards * kCand, buf[warp], res[warp], lane);
+  if (lane == 0) out[0] = local;
+  if (lane < kCand) out[1 + lane] = res[warp][lane] ? key_id(res[warp][lane]) : -1;
+}
+
+// Host: the 15 largest of keys (descending, 0-padded), the same order as the kernels.
+void host_top15(std::vector<uint64_t>& keys, uint64_t* out) {
+  const size_t m = std::min<size_t>(kCand, keys.size());
+  std::partial_sort(keys.begin(), keys.begin() + static_cast<std::ptrdiff_t>(m), keys.end(),
+                    [](uint64_t a, uint64_t b) { return a > b; });
+  for (int i = 0; i < kCand; ++i) out[i] = static_cast<size_t>(i) < m ? keys[i] : 0ull;
+}
 }  // namespace
 }  // namespace msa
 
 using namespace msa;
 using namespace msa_host;
 
+namespace {
+msa_status topk_setup(const msa_geometry* geo, const msa_batch* batch, const float* block_scores, int32_t* sel,
+                      uint32_t* status, TopkParams* p);
+}  // namespace
+
 extern "C" msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* batch, const float* block_scores,
                                       int32_t* sel, uint32_t* status, cudaStream_t stream) {
-  msa_status st = check_geometry(geo);
+  TopkParams p;
+  msa_status st = topk_setup(geo, batch, block_scores, sel, status, &p);
   if (st != MSA_OK) return st;
-  if ((st = check_batch(batch)) != MSA_OK) return st;
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
-  TopkParams p;
-  p.B = batch->B;
-  p.T = batch->T;
-  p.maxb = batch->max_blocks_per_seq;
-  p.max_q_len = batch->max_q_len;
-  p.qsl = batch->query_start_loc;
-  p.seq_lens = batch->seq_lens;
-  p.scores = block_scores;
-  p.sel = sel;
-  p.status = status;
   k_topk<<<ceil_div(batch->T * 4, kRowsPerCta), 32 * kRowsPerCta, 0, stream>>>(p);
   return launch_status();
+}
+
+namespace {
+msa_status topk_setup(const msa_geometry* geo, const msa_batch* batch, const float* block_scores, int32_t* sel,
+                      uint32_t* status, TopkParams* p) {
+  msa_status st = check_geometry(geo);
+  if (st != MSA_OK) return st;
+  if ((st = check_batch(batch)) != MSA_OK) return st;
+  p->B = batch->B;
+  p->T = batch->T;
+  p->maxb = batch->max_blocks_per_seq;
+  p->max_q_len = batch->max_q_len;
+  p->qsl = batch->query_start_loc;
+  p->seq_lens = batch->seq_lens;
+  p->scores = block_scores;
+  p->sel = sel;
+  p->status = status;
+  return MSA_OK;
+}
+}  // namespace
+
+extern "C" msa_status msa_topk_candidates(const msa_geometry* geo, const msa_batch* batch, const float* block_scores,
+                                          int32_t block_begin, int32_t block_end, uint64_t* cand, uint32_t* status,
+                                          cudaStream_t stream) {
+  CandParams c;
+  msa_status st = topk_setup(geo, batch, block_scores, nullptr, status, &c.t);
+  if (st != MSA_OK) return st;
+  if (block_begin < 0 || block_end < block_begin) return MSA_ERR_INVALID_ARG;
+  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  if (block_scores == nullptr || cand == nullptr || !aligned(block_scores, 4) || !aligned(cand, 8))
+    return MSA_ERR_INVALID_ARG;
+  c.kb = block_begin;
+  c.ke = block_end;
+  c.n_shards = 1;
+  c.cand = cand;
+  c.cand_in = nullptr;
+  k_topk_cand<<<ceil_div(batch->T * 4, kRowsPerCta), 32 * kRowsPerCta, 0, stream>>>(c);
+  return launch_status();
+}
+
+extern "C" msa_status msa_topk_merge(const msa_geometry* geo, const msa_batch* batch, const uint64_t* cand,
+                                     int32_t n_shards, int32_t* sel, uint32_t* status, cudaStream_t stream) {
+  CandParams c;
+  msa_status st = topk_setup(geo, batch, nullptr, sel, status, &c.t);
+  if (st != MSA_OK) return st;
+  if (n_shards < 1 || n_shards > 256) return MSA_ERR_INVALID_ARG;
+  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  if (cand == nullptr || sel == nullptr || !aligned(cand, 8) || !aligned(sel, 4)) return MSA_ERR_INVALID_ARG;
+  c.kb = 0;
+  c.ke = 0;
+  c.n_shards = n_shards;
+  c.cand = nullptr;
+  c.cand_in = cand;
+  k_topk_merge<<<ceil_div(batch->T * 4, kRowsPerCta), 32 * kRowsPerCta, 0, stream>>>(c);
+  return launch_status();
+}
+
+extern "C" msa_status msa_topk_candidates_host(const float* block_scores, int64_t rows, int32_t max_blocks_per_seq,
+                                               const int32_t* local, int32_t block_begin, int32_t block_end,
+                                               uint64_t* cand) {
+  if (rows < 0 || max_blocks_per_seq < 1 || block_begin < 0 || block_end < block_begin) return MSA_ERR_INVALID_ARG;
+  if (rows > 0 && (block_scores == nullptr || local == nullptr || cand == nullptr)) return MSA_ERR_INVALID_ARG;
+  std::vector<uint64_t> keys;
+  for (int64_t r = 0; r < rows; ++r) {
+    keys.clear();
+    const int lc = local[r];
+    if (lc > max_blocks_per_seq) return MSA_ERR_INVALID_ARG;
+    const float* s = block_scores + r * max_blocks_per_seq;
+    for (int k = block_begin; k < std::min(block_end, lc); ++k) keys.push_back(score_key(s[k], k));
+    host_top15(keys, cand + r * kCand);
+  }
+  return MSA_OK;
+}
+
+extern "C" msa_status msa_topk_merge_host(const uint64_t* cand, int32_t n_shards, int64_t rows, const int32_t* local,
+                                          int32_t* sel) {
+  if (rows < 0 || n_shards < 1) return MSA_ERR_INVALID_ARG;
+  if (rows > 0 && (cand == nullptr || local == nullptr || sel == nullptr)) return MSA_ERR_INVALID_ARG;
+  std::vector<uint64_t> keys;
+  uint64_t top[kCand];
+  for (int64_t r = 0; r < rows; ++r) {
+    int32_t* out = sel + r * kSel;
+    if (local[r] < 0) {
+      for (int i = 0; i < kSel; ++i) out[i] = -1;
+      continue;
+    }
+    keys.clear();
+    for (int sh = 0; sh < n_shards; ++sh)
+      for (int i = 0; i < kCand; ++i) {
+        const uint64_t k = cand[(static_cast<int64_t>(sh) * rows + r) * kCand + i];
+        if (k != 0ull) keys.push_back(k);
+      }
+    host_top15(keys, top);
+    out[0] = local[r];
+    for (int i = 0; i < kCand; ++i) out[1 + i] = top[i] ? key_id(top[i]) : -1;
+  }
+  return MSA_OK;
 }

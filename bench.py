@@ -191,6 +191,18 @@ def _cuda_ok():
 
 
 # ---------------------------------------------------------------------------- GPU leg
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The job's time: the slowest rank's (every rank runs its own replica of the batch)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -237,11 +249,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     wall = time.perf_counter() - t_wall
     clk = clocks.stop() if clocks else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(step_ms)
-    t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(statistics.mean(step_ms), world, dev)
 
     # ---- per-stage breakdown: the same three calls with events between them
     o2 = dl.outputs()
@@ -288,11 +296,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
         e2e_ev[i][1].record(stream)
         e2e_ev[i][1].synchronize()
     barrier()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    t2 = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t2.item())
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
 
     if rank != 0:
         return

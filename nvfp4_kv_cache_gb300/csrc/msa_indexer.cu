@@ -23,14 +23,14 @@
 //  * one MMA thread: four tcgen05.mma kind::f8f6f4 per page (M = 128 keys, N = 16 or 32
 //    (token, group) columns, K = 4 x 32) into a ring of TMEM accumulators, then commits that
 //    free the key tile and publish the scores;
-//  * two max-pool groups of four warps take alternate pages: the 16x256b TMEM load hands every
-//    thread four keys of eight columns, so a warp needs a 4-key register max and a 3-step
-//    shuffle transpose-reduce; the four warps' partial maxima meet in shared memory behind one
-//    group barrier, and 32 threads store the block scores. Keys after a query position are
+//  * eight max-pool warps, two per TMEM lane quarter, take alternate pages: the 16x256b TMEM
+//    load hands every thread four keys of eight columns, so a warp needs a 4-key register max
+//    and a 3-step shuffle transpose-reduce. Each quarter stores its partial maxima in shared
+//    memory and counts itself in; the page's last quarter combines the four and stores the block
+//    scores, so no quarter ever waits for another. Keys after a query position are
 //    masked on the (rare) pages that hold them.
-// Every wait is bounded (MSA_ERR_TIMEOUT); a max-pool group leaves its loop only on a barrier
-// that reports the same decision to all its threads; every page id is checked
-// (MSA_ERR_DEVICE_FAULT, the block is scored -inf); nothing traps.
+// Every wait is bounded (MSA_ERR_TIMEOUT); no role waits on a named barrier inside its loop;
+// every page id is checked (MSA_ERR_DEVICE_FAULT, the block is scored -inf); nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -56,6 +56,11 @@ constexpr int kATiles = 6;                       // TMEM key tiles (32 columns e
 constexpr int kDTiles = 6;                       // TMEM accumulators (32 columns each)
 constexpr int kTmemCols = 512;
 constexpr int kBTile = 32 * kD;                  // 32 query rows x 128 B
+// Partial-maximum slots of the max-pool quarters: page n uses slot n % kPartSlots. A slot is
+// written again only by page n + kPartSlots, whose MMA needed its accumulator released by all
+// four quarters at page n + kPartSlots - kDTiles, which each quarter reaches after combining
+// page n (a warp takes its pages in order): 2 * kDTiles slots are enough.
+constexpr int kPartSlots = 2 * kDTiles;
 static_assert(kATiles % kDqGroups == 0 && kDTiles % kEpGroups == 0, "a ring slot serves one group");
 static_assert(kIdxThreads <= 1024, "one CTA");
 static_assert(kATiles % kMmaWarps == 0 && kDTiles % kMmaWarps == 0, "a ring slot serves one MMA warp");
@@ -110,8 +115,9 @@ struct IdxSmem {
   static constexpr size_t kOffInfo = kOffDEmpty + 8 * kDTiles;
   static constexpr size_t kOffAMeta = kOffInfo + sizeof(SlotInfo) * kStages;  // [kATiles] int2
   static constexpr size_t kOffBTag = kOffAMeta + 8 * kATiles;                 // [kATiles][4] int
-  static constexpr size_t kOffPart = kOffBTag + 16 * kATiles;                 // [EP][2][4][32] fp32
-  static constexpr size_t kOffLut = kOffPart + 4 * kEpGroups * 2 * 4 * 32;
+  static constexpr size_t kOffPart = kOffBTag + 16 * kATiles;                 // [kPartSlots][4][32] fp32
+  static constexpr size_t kOffCnt = kOffPart + 4 * kPartSlots * 4 * 32;       // [kPartSlots] int
+  static constexpr size_t kOffLut = kOffCnt + 4 * kPartSlots;
   static constexpr size_t kOffMisc = kOffLut + 256 * 8;
   static constexpr size_t kOffPtab = kOffMisc + 64;  // 32 x int4
   static constexpr size_t kOffWarpSum = kOffPtab + 32 * 16;
@@ -223,6 +229,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
     *bad_batch = 0;
   }
   if (tid < 4 * kATiles) btag[tid] = -1;
+  if (tid < kPartSlots) reinterpret_cast<int*>(smem + S::kOffCnt)[tid] = 0;
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   if constexpr (kNv) build_dequant_lut(lut, tid, kIdxThreads);
   __syncthreads();  // flags initialised before anyone raises them
@@ -433,17 +440,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       if (lane == 0) mbar_arrive(&a_full[a]);
     }
   } else {
-    // ---- max-pool groups: pages ep, ep + 2, ... ---------------------------------------------
+    // ---- max-pool warps: warp (ep, wq) pools TMEM lane quarter wq of pages ep, ep + 2, ...;
+    // the quarter that finishes a page last (a shared counter) combines the four partial
+    // maxima, so the quarters never wait for one another ----------------------------------------
     const int ep = (warp - kWarpEp) >> 2;
     const int wq = warp & 3;
-    const int i = 32 * wq + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
-    float* part = reinterpret_cast<float*>(smem + S::kOffPart) + ep * 256;  // [2][4 quarters][32]
-    const int bar_id = 1 + ep;
-    // lane l holds the facts of the group's page (base + l): block, first column row, columns,
+    float* part = reinterpret_cast<float*>(smem + S::kOffPart);  // [kPartSlots][4 quarters][32]
+    int* cnt = reinterpret_cast<int*>(smem + S::kOffCnt);         // [kPartSlots] quarters done
+    // lane l holds the facts of the warp's page (base + l): block, first column row, columns,
     // first query position, page id valid
     int m_k = 0, m_q0 = 0, m_ncol = 0, m_p0 = 0, m_valid = 0;
-    bool fail = false;
     int j = 0;
     for (int n = ep; n < npages; n += kEpGroups, ++j) {
       if ((j & 31) == 0) {
@@ -461,19 +468,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         }
       }
       const int src = j & 31;
-      const int k = __shfl_sync(0xffffffffu, m_k, src), q0 = __shfl_sync(0xffffffffu, m_q0, src);
-      const int ncol = __shfl_sync(0xffffffffu, m_ncol, src), p0 = __shfl_sync(0xffffffffu, m_p0, src);
+      const int k = __shfl_sync(0xffffffffu, m_k, src);
+      const int p0 = __shfl_sync(0xffffffffu, m_p0, src);
       const bool valid = __shfl_sync(0xffffffffu, m_valid, src) != 0;
       const int d = n % kDTiles;
-      const bool ready = warp_wait(&d_full[d], static_cast<uint32_t>(n / kDTiles) & 1u, abort_flag);
-      if (!ready) fail = true;
-      float v[8];
-      if (ready) {
-        tc_fence_after();
-        if (lane == 0) {  // the MMAs are done: their key tile (and FP8 stage) may be refilled
-          mbar_arrive(&a_empty[n % kATiles]);
-          if constexpr (!kNv) mbar_arrive(&empty[n % kStages]);
+      if (!warp_wait(&d_full[d], static_cast<uint32_t>(n / kDTiles) & 1u, abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+          *abort_flag = 1;
         }
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {  // the MMAs are done: their key tile (and FP8 stage) may be refilled
+        mbar_arrive(&a_empty[n % kATiles]);
+        if constexpr (!kNv) mbar_arrive(&empty[n % kStages]);
+      }
+      float pm = -CUDART_INF_F;  // this lane's column maximum over the quarter's 32 keys
+      int col = 0;
+      {
         uint32_t a[16], b[16];
         if (valid) {
           const uint32_t taddr = t_d + 32 * d + lane_base;
@@ -489,14 +502,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
             const int pos = k * kBS + 32 * wq + (lane >> 2);  // key of a[0]
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int col = 8 * (e >> 2) + 2 * (lane & 3) + (e & 1);
+              const int c = 8 * (e >> 2) + 2 * (lane & 3) + (e & 1);
               const int row = 8 * ((e >> 1) & 1);
-              const int lim = p0 + (col >> 2);
+              const int lim = p0 + (c >> 2);
               if (pos + row > lim) a[e] = __float_as_uint(-CUDART_INF_F);
               if (pos + row + 16 > lim) b[e] = __float_as_uint(-CUDART_INF_F);
             }
           }
-          // v[2o + e]: column 8o + 2(lane % 4) + e, max over this thread's 4 keys
+          float v[8];  // v[2o + e]: column 8o + 2(lane % 4) + e, max over this thread's 4 keys
 #pragma unroll
           for (int o = 0; o < 4; ++o)
 #pragma unroll
@@ -508,19 +521,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
           xreduce_step<4>(v, lane, 16);
           xreduce_step<2>(v, lane, 8);
           xreduce_step<1>(v, lane, 4);
-          const int col = 16 * ((lane >> 4) & 1) + 8 * ((lane >> 3) & 1) + 2 * (lane & 3) + ((lane >> 2) & 1);
-          part[(j & 1) * 128 + wq * 32 + col] = v[0];
+          pm = v[0];
         }
+        col = 16 * ((lane >> 4) & 1) + 8 * ((lane >> 3) & 1) + 2 * (lane & 3) + ((lane >> 2) & 1);
       }
-      if (fail) *abort_flag = 1;
-      if (named_barrier_or(bar_id, 128, fail || *abort_flag != 0)) break;
-      if (i < ncol) {
-        float m = -CUDART_INF_F;
-        if (valid) {
-          const float* s4 = part + (j & 1) * 128;
-          m = fmaxf(fmaxf(s4[i], s4[32 + i]), fmaxf(s4[64 + i], s4[96 + i]));
+      // partial maxima of this quarter, then the page's quarter count
+      const int slot = n % kPartSlots;
+      part[(slot * 4 + wq) * 32 + col] = pm;
+      __threadfence_block();
+      __syncwarp();
+      int done = 0;
+      if (lane == 0) done = atomicAdd(&cnt[slot], 1);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done == 3) {  // the last quarter: combine and store the block scores
+        __threadfence_block();
+        const int ncol = __shfl_sync(0xffffffffu, m_ncol, src), q0 = __shfl_sync(0xffffffffu, m_q0, src);
+        if (lane < ncol) {
+          const float* s4 = part + slot * 128;
+          const float m = valid ? fmaxf(fmaxf(s4[lane], s4[32 + lane]), fmaxf(s4[64 + lane], s4[96 + lane]))
+                                : -CUDART_INF_F;
+          p.block_scores[static_cast<int64_t>(q0 * 4 + lane) * p.maxb + k] = m;
         }
-        p.block_scores[static_cast<int64_t>(q0 * 4 + i) * p.maxb + k] = m;
+        __syncwarp();
+        if (lane == 0) cnt[slot] = 0;  // free for page n + kPartSlots
       }
     }
   }

@@ -3,32 +3,42 @@
 // What it computes ("vLLM ofrece soporte en día 0 para MiniMax-M3.1-Flash", "MSA primer": exact
 // attention over the selected blocks only, every query head of a GQA group using its group's
 // selection; "MiniMax M3 in vLLM ...", "解码执行": split work merged from partial outputs, and
-// "MSA 机制详解": the partial last block and keys after the query position are masked). K and V
+// "MSA 机制详解": the partial last block and keys after the query position are masked;
+// "解码内核中的推测解码": the draft tokens of a sequence are causal among themselves). K and V
 // are dequantised from NVFP4 to E4M3 ("NVIDIA Blackwell optimizado kernes MSA") exactly as the
 // indexer does; QK^T is an FP8 MMA with fp32 accumulation; the softmax is fp32 (exp2 with the
 // log2(e) folded into the scale); PV takes P rounded to f16 and V widened exactly from E4M3 to
 // f16, because P rounded to E4M3 (3 mantissa bits) would cost several percent of relative
 // error.
 //
-// GB300 design: one CTA of 8 warps per (query token, group, split); a warp owns whole
-// selected blocks (16 query heads x 128 keys):
-//  * its block's K and V regions (2 x 9,216 B, contiguous in the page) arrive with one 1-D
-//    bulk copy (cp.async.bulk + mbarrier) into the warp's own shared-memory stage;
-//  * K is dequantised register-direct into the B fragments of mma.sync.m16n8k32.e4m3 (the
-//    16 heads of the group on M), 32 keys at a time, the same lane/dim mapping as the indexer;
-//  * V of those 32 keys is dequantised once into a private swizzled f16 tile and read back
-//    transposed with ldmatrix.trans for mma.sync.m16n8k16.f16 (P straight from the QK^T
-//    accumulators);
-//  * online softmax per warp; O is rescaled only when some row maximum moved; the 8 warps'
-//    states are merged in shared memory at the end.
-//  * Splits of a (token, group)'s 16 blocks raise the CTA count when T * 4 is small; the
-//    partial (lse, o) pairs are merged by log-sum-exp in a second kernel.
-// The next block's copy is issued as soon as the last V chunk of the current block has been
-// dequantised, so it overlaps the remaining MMAs.
+// GB300 design: two kernels, picked by the batch's max_q_len.
+//
+// k_attn (every sequence has one query token: plain decode): one CTA of 12 warps per
+// (sequence, group, split) that walks the union of the sequence's tokens' selected blocks
+// (for one token, its 16 blocks), each block once:
+//  * a 3-D tensor copy per block brings the group's K and V regions (144 rows of 128 B,
+//    128-byte swizzle) into a 3-deep stage ring;
+//  * four dequant warps (thread = key) turn the block into a 128 x 128 E4M3 K tile and a
+//    128 x 128 f16 V tile (E4M3 -> f16 is exact) in swizzled shared memory, a 3-deep ring;
+//  * eight token warps: the 16 heads of one query token are the M = 16 rows of
+//    mma.sync.m16n8k32.e4m3 (S = QK^T, K fragments by ldmatrix) and mma.sync.m16n8k16.f16
+//    (O += PV, V fragments by ldmatrix.trans, P straight from the S accumulators), with an
+//    online softmax; a token skips the blocks it did not select. A token gets
+//    8 / q_len' warps (q_len' = q_len rounded up to a power of two) that split the keys of
+//    each block (and, for q_len = 1, alternate blocks too); their states are merged at the end.
+//    So one token's 16 blocks are dequantised once by the whole CTA and its keys spread
+//    over 8 warps: short per-token latency, for batches of few tokens.
+//  * Splits of the union raise the CTA count when B x 4 is small; the partial (lse, o) pairs
+//    are merged by log-sum-exp in a second kernel.
+// tok::k_attn_tok (multi-token sequences): one CTA per (query token, group, split), described
+// where it is defined.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "msa.h"
@@ -38,11 +48,17 @@
 namespace msa {
 namespace {
 
-constexpr int kAttnWarps = 8;
-constexpr int kAttnThreads = 32 * kAttnWarps;
-constexpr int kStageBytes = 2 * kRegion;  // K region then V region of one (page, group)
-constexpr int kChunkKeys = 32;
-constexpr int kVTileBytes = kChunkKeys * kD * 2;  // 32 keys x 128 dims f16
+constexpr int kTokWarps = 8;                                // warps 0..7: query tokens
+constexpr int kDqWarps = 4;                                 // warps 8..11: dequant, thread = key
+constexpr int kAttnThreads = 32 * (kTokWarps + kDqWarps);   // 384
+constexpr int kStages = 3;                                  // NVFP4 K+V stage ring
+constexpr int kTiles = 3;                                   // dequantised K/V tile ring
+constexpr int kStageBytes = 2 * kRegion;                    // K region then V region of one (page, group)
+constexpr int kKTile = kBS * kD;                            // 128 keys x 128 E4M3
+constexpr int kVTile = kBS * kD * 2;                        // 128 keys x 128 f16
+constexpr int kTileBytes = kKTile + kVTile;
+constexpr int kUnionMax = kMaxQLen * kSel;                  // 128
+constexpr int kBarTok = 1, kBarDq = 2;                      // named barriers (0 = __syncthreads)
 
 struct AttnParams {
   int32_t B, T, maxb, max_q_len, num_pages, splits;
@@ -60,6 +76,455 @@ struct AttnParams {
 };
 
 struct AttnSmem {
+  static constexpr size_t kOffStage = 0;                                                  // 3 x 18 KB
+  static constexpr size_t kOffTile = kOffStage + static_cast<size_t>(kStages) * kStageBytes;  // 3 x 48 KB
+  static constexpr size_t kOffBar = kOffTile + static_cast<size_t>(kTiles) * kTileBytes;
+  // barriers: st_full [kStages]; t_full, t_empty [kTiles]
+  static constexpr int kBars = kStages + 2 * kTiles;
+  static constexpr size_t kOffLut = kOffBar + 8 * 16;
+  static constexpr size_t kOffCand = kOffLut + 256 * 8;          // 128 candidate block ids
+  static constexpr size_t kOffUBlk = kOffCand + 4 * kUnionMax;   // union: block, token mask, page
+  static constexpr size_t kOffUMask = kOffUBlk + 4 * kUnionMax;
+  static constexpr size_t kOffUPhys = kOffUMask + 4 * kUnionMax;
+  static constexpr size_t kOffWarpCnt = kOffUPhys + 4 * kUnionMax;  // 4 ints
+  static constexpr size_t kOffMisc = kOffWarpCnt + 16;
+  static constexpr size_t kBytes = 1024 + kOffMisc + 64;            // + alignment slack
+  // after the block loop the tile ring holds each token warp's final state
+  static constexpr size_t kWarpState = 16 * 4 * 2 + 16 * kD * 4;    // m, l, O[16][128]
+};
+static_assert(AttnSmem::kBars <= 16, "barrier area");
+static_assert(AttnSmem::kOffTile % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled stages sit on 1024-B boundaries");
+static_assert(kTiles * kTileBytes >= kTokWarps * AttnSmem::kWarpState, "merge area too small");
+static_assert(AttnSmem::kBytes <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+// The 64 code bytes and 8 scale bytes of key row r of a staged NVFP4 region (128-byte swizzled).
+struct RawRow {
+  uint4 c[4];  // c[q]: code words of dims 32 q .. 32 q + 31
+  uint2 sc;    // scale bytes of dims 16 i .. 16 i + 15, i = 0..7
+};
+
+__device__ __forceinline__ void load_row(const uint8_t* rg, int r, RawRow& raw) {
+  raw.sc = lds64(rg + sw128_phys(static_cast<uint32_t>(kScaleOff + r * kRowScales)));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) raw.c[q] = lds128(rg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * q)));
+}
+
+// Dims 32 q .. 32 q + 31 of a raw row as E4M3: w[i] = dims 32 q + 4 i .. +3.
+__device__ __forceinline__ void dequant_quarter(const RawRow& raw, int q, const uint2* lut, uint32_t (&w)[8]) {
+  const uint32_t s2 = ((q < 2) ? raw.sc.x : raw.sc.y) >> (16 * (q & 1));
+  const uint2 e0 = lut[s2 & 0xFFu], e1 = lut[(s2 >> 8) & 0xFFu];
+  dq8(raw.c[q].x, e0, w[0], w[1]);
+  dq8(raw.c[q].y, e0, w[2], w[3]);
+  dq8(raw.c[q].z, e1, w[4], w[5]);
+  dq8(raw.c[q].w, e1, w[6], w[7]);
+}
+
+// Running softmax state of one token warp for its 16 heads (rows gid and gid + 8 here).
+struct WarpState {
+  float m[2], l[2];
+  float o[16][4];  // 16 n-tiles of 8 dims: (head gid, dims 8j+2t..+1), (head gid+8, ...)
+};
+
+// Keys 32 c .. 32 c + 31 of chunks [c_lo, c_hi) of one dequantised block for the 16 heads of
+// this warp's token. kt: E4M3 [key][128] (16-byte chunk x of row k at x ^ (k & 7)); vt: f16
+// [key][128] (chunk x of row k at x ^ (k & 7)). Keys past p_tok are masked; chunks wholly past
+// it are skipped.
+__device__ __forceinline__ void attend_tile(WarpState& st, const uint32_t (&qa)[4][4], const uint8_t* kt,
+                                            const uint8_t* vt, int blk_pos0, int p_tok, float scale_log2, int c_lo,
+                                            int c_hi, int lane) {
+  const int t = lane & 3;
+  const int r8 = lane & 7, m8 = lane >> 3;
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; ++c) {
+    const int k0 = c * 32;
+    if (blk_pos0 + k0 > p_tok) break;  // every remaining key lies after the query position
+    // ---- S = Q K^T for keys k0 .. k0+31 (4 n-tiles of 8 keys)
+    float x[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint8_t* krow = kt + (k0 + 8 * j + r8) * kD;
+      uint32_t b0[4], b1[4];
+      ldmatrix_x4(b0, krow + ((m8 ^ r8) << 4));        // dims 0..63
+      ldmatrix_x4(b1, krow + (((m8 + 4) ^ r8) << 4));  // dims 64..127
+      mma_e4m3_zc(x[j], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b0[0], b0[1]);
+      mma_e4m3(x[j], qa[1][0], qa[1][1], qa[1][2], qa[1][3], b0[2], b0[3]);
+      mma_e4m3(x[j], qa[2][0], qa[2][1], qa[2][2], qa[2][3], b1[0], b1[1]);
+      mma_e4m3(x[j], qa[3][0], qa[3][1], qa[3][2], qa[3][3], b1[2], b1[3]);
+    }
+    // ---- scale, causal mask, online softmax
+    const bool need_mask = blk_pos0 + k0 + 31 > p_tok;
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v = x[j][i] * scale_log2;
+        if (need_mask && blk_pos0 + k0 + 8 * j + 2 * t + (i & 1) > p_tok) v = -CUDART_INF_F;
+        x[j][i] = v;
+      }
+      mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(x[j][2], x[j][3]));
+    }
+    mx0 = quad_max(mx0);
+    mx1 = quad_max(mx1);
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+    const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+    if (__any_sync(0xffffffffu, mn0 != st.m[0] || mn1 != st.m[1])) {
+      const float c0 = fast_exp2(st.m[0] - mu0), c1 = fast_exp2(st.m[1] - mu1);
+      st.l[0] *= c0;
+      st.l[1] *= c1;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        st.o[n][0] *= c0;
+        st.o[n][1] *= c0;
+        st.o[n][2] *= c1;
+        st.o[n][3] *= c1;
+      }
+      st.m[0] = mn0;
+      st.m[1] = mn1;
+    }
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[j][0] = fast_exp2(x[j][0] - mu0);
+      x[j][1] = fast_exp2(x[j][1] - mu0);
+      x[j][2] = fast_exp2(x[j][2] - mu1);
+      x[j][3] = fast_exp2(x[j][3] - mu1);
+      ls0 += x[j][0] + x[j][1];
+      ls1 += x[j][2] + x[j][3];
+    }
+    st.l[0] += ls0;
+    st.l[1] += ls1;
+    // ---- O += P V: 2 k-steps of 16 keys, 8 pairs of 8-dim n-tiles
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t a0 = pack_f16x2(x[2 * kk][0], x[2 * kk][1]);
+      const uint32_t a1 = pack_f16x2(x[2 * kk][2], x[2 * kk][3]);
+      const uint32_t a2 = pack_f16x2(x[2 * kk + 1][0], x[2 * kk + 1][1]);
+      const uint32_t a3 = pack_f16x2(x[2 * kk + 1][2], x[2 * kk + 1][3]);
+      const int rl = k0 + 16 * kk + (m8 & 1) * 8 + r8;
+      const uint8_t* vrow = vt + rl * (2 * kD);
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn) {
+        const int chunk = 2 * dn + (m8 >> 1);
+        uint32_t r[4];
+        ldmatrix_x4_trans(r, vrow + ((chunk ^ r8) << 4));
+        mma_f16(st.o[2 * dn], a0, a1, a2, a3, r[0], r[1]);
+        mma_f16(st.o[2 * dn + 1], a0, a1, a2, a3, r[2], r[3]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
+  using S = AttnSmem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
+  uint64_t* st_full = bars;
+  uint64_t* t_full = st_full + kStages;
+  uint64_t* t_empty = t_full + kTiles;
+  uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
+  int* cand = reinterpret_cast<int*>(smem + S::kOffCand);
+  int* ublk = reinterpret_cast<int*>(smem + S::kOffUBlk);
+  int* umask = reinterpret_cast<int*>(smem + S::kOffUMask);
+  int* uphys = reinterpret_cast<int*>(smem + S::kOffUPhys);
+  int* warp_cnt = reinterpret_cast<int*>(smem + S::kOffWarpCnt);
+  int* bad_tok = reinterpret_cast<int*>(smem + S::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
+  int* nunion = reinterpret_cast<int*>(smem + S::kOffMisc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % p.splits;
+  const int bg = blockIdx.x / p.splits;
+  const int b = bg >> 2, g = bg & 3;
+  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
+  const int L = p.seq_lens[b];
+  if (ql <= 0) return;  // a padded row: no tokens
+  if (!(ql <= p.max_q_len && q0 >= 0 && q0 + ql <= p.T && L >= ql && L <= p.maxb * kBS)) {
+    if (tid == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+    return;
+  }
+  const int nb = ceil_div(L, kBS);
+
+  // ---- prologue --------------------------------------------------------------------------
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(&st_full[i], 1);
+    for (int i = 0; i < kTiles; ++i) {
+      mbar_init(&t_full[i], kDqWarps);
+      mbar_init(&t_empty[i], kTokWarps);
+    }
+    fence_mbar_init();
+    *bad_tok = 0;
+    *abort_flag = 0;
+  }
+  build_dequant_lut(lut, tid, kAttnThreads);
+  // candidates: entry e = 16 * token + slot
+  if (tid < kUnionMax) {
+    const int tok = tid >> 4;
+    cand[tid] = tok < ql ? p.sel[(static_cast<int64_t>(q0 + tok) * 4 + g) * kSel + (tid & 15)] : -1;
+  }
+  __syncthreads();
+  // union of the tokens' selections, first occurrence order; a bad entry (block beyond the
+  // sequence, page id out of range) marks its tokens bad
+  {
+    bool keep = false;
+    int v = -1, mask = 0, ph = -1;
+    if (tid < kUnionMax) {
+      v = cand[tid];
+      if (v >= nb) {
+        set_status(p.status, MSA_ERR_DEVICE_FAULT);
+        atomicOr(bad_tok, 1 << (tid >> 4));
+      } else if (v >= 0) {
+        bool first = true;
+        for (int e = 0; e < kUnionMax; ++e) {
+          if (cand[e] == v) {
+            mask |= 1 << (e >> 4);
+            if (e < tid) first = false;
+          }
+        }
+        if (first) {
+          ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
+          if (ph >= 0 && ph < p.num_pages) {
+            keep = true;
+          } else {
+            set_status(p.status, MSA_ERR_DEVICE_FAULT);
+            atomicOr(bad_tok, mask);
+          }
+        }
+      }
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    if (tid < kUnionMax && lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    if (keep) {
+      int pos = __popc(m & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) pos += warp_cnt[w];
+      ublk[pos] = v;
+      umask[pos] = mask;
+      uphys[pos] = ph;
+    }
+    if (tid == 0) *nunion = warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
+  }
+  __syncthreads();
+  const int nu = *nunion;
+  const int i0 = (nu * split) / p.splits, i1 = (nu * (split + 1)) / p.splits;
+  const int n = i1 - i0;  // blocks of this CTA: union entries i0 .. i1-1
+  const int badm = *bad_tok;
+  auto issue = [&](int j) {  // the copy of union entry i0 + j into stage j % kStages
+    uint64_t* bar = &st_full[j % kStages];
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_3d(smem + S::kOffStage + static_cast<size_t>(j % kStages) * kStageBytes, &tmap, 0,
+                2 * g * (kRegion / kD), uphys[i0 + j], bar);
+  };
+
+  if (warp >= kTokWarps) {
+    // ---- dequant warps: thread = key kr of every block ------------------------------------
+    const int kr = 32 * (warp - kTokWarps) + lane;
+    const bool leader = warp == kTokWarps && lane == 0;
+    int issued = 0, consumed = 0;
+    if (leader) {
+      prefetch_tensormap(&tmap);
+      for (; issued < kStages && issued < n; ++issued) issue(issued);
+    }
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kStages, x = i % kTiles;
+      bool ok = warp_wait(&st_full[s], static_cast<uint32_t>(i / kStages) & 1u, abort_flag);
+      ok = ok && warp_wait(&t_empty[x], (static_cast<uint32_t>(i / kTiles) & 1u) ^ 1u, abort_flag);
+      RawRow rk, rv;  // key kr's codes and scales, read out of the stage before it is released
+      if (ok) {
+        const uint8_t* stg = smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes;
+        load_row(stg, kr, rk);
+        load_row(stg + kRegion, kr, rv);
+      }
+      // every dequant warp has read stage s (or one of them gave up: all leave together)
+      if (named_barrier_or(kBarDq, 32 * kDqWarps, !ok)) {
+        if (lane == 0 && !*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      consumed = i + 1;
+      if (leader && issued < n) issue(issued++);
+      uint8_t* kt = smem + S::kOffTile + static_cast<size_t>(x) * kTileBytes;
+      uint8_t* vt = kt + kKTile;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // code word group q = dims 32 q .. 32 q + 31
+        uint32_t w[8];
+        dequant_quarter(rk, q, lut, w);
+        *reinterpret_cast<uint4*>(kt + kr * kD + (((2 * q) ^ (kr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(kt + kr * kD + (((2 * q + 1) ^ (kr & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[8];
+        dequant_quarter(rv, q, lut, w);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // f16 chunk 4 q + h = dims 32 q + 8 h .. +7
+          const uint4 v = make_uint4(cvt_f16x2_e4m3x2(w[2 * h]), cvt_f16x2_e4m3x2(w[2 * h] >> 16),
+                                     cvt_f16x2_e4m3x2(w[2 * h + 1]), cvt_f16x2_e4m3x2(w[2 * h + 1] >> 16));
+          *reinterpret_cast<uint4*>(vt + kr * (2 * kD) + (((4 * q + h) ^ (kr & 7)) << 4)) = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&t_full[x]);
+    }
+    // copies still in flight after a give-up: wait for them before the CTA's memory goes
+    if (leader)
+      for (int j = consumed; j < issued; ++j)
+        if (!mbar_wait_bounded(&st_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
+    return;
+  }
+
+  // ---- token warps -------------------------------------------------------------------------
+  const int qlp = ql <= 1 ? 1 : ql <= 2 ? 2 : ql <= 4 ? 4 : 8;
+  const int wpt = kTokWarps / qlp;  // warps per token: 1, 2, 4, 8
+  const int tok = warp / wpt, sub = warp % wpt;
+  const int csplit = wpt < 4 ? wpt : 4;   // the token's warps split each block's 4 chunks ...
+  const int rsplit = wpt / csplit;        // ... and, with 8 warps, alternate blocks too
+  const int c_lo = (sub % csplit) * (4 / csplit), c_hi = c_lo + 4 / csplit;
+  const int rpart = sub / csplit;
+  const bool live = tok < ql && !((badm >> tok) & 1);
+  const int p_tok = L - ql + tok;
+  const int gid = lane >> 2, tq = lane & 3;
+  WarpState st;
+  st.m[0] = st.m[1] = -CUDART_INF_F;
+  st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) st.o[k][0] = st.o[k][1] = st.o[k][2] = st.o[k][3] = 0.f;
+  uint32_t qa[4][4];
+  {
+    const int qt = live ? q0 + tok : q0;
+    const uint8_t* qrow0 = p.q + (static_cast<int64_t>(qt) * kQHeads + g * kHPG + gid) * kD + 4 * tq;
+    const uint8_t* qrow1 = qrow0 + 8 * kD;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {  // k-step s: dims 32 s + 4 tq (a0, a1) and 32 s + 16 + 4 tq (a2, a3)
+      qa[s][0] = ldg_nc32(qrow0 + 32 * s);
+      qa[s][1] = ldg_nc32(qrow1 + 32 * s);
+      qa[s][2] = ldg_nc32(qrow0 + 32 * s + 16);
+      qa[s][3] = ldg_nc32(qrow1 + 32 * s + 16);
+    }
+  }
+  int cnt = 0;
+  for (int i = 0; i < n; ++i) {
+    const int x = i % kTiles;
+    if (!warp_wait(&t_full[x], static_cast<uint32_t>(i / kTiles) & 1u, abort_flag)) {
+      if (lane == 0) {
+        if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    const int e = i0 + i;
+    if (live && ((umask[e] >> tok) & 1)) {
+      if (cnt % rsplit == rpart) {
+        const uint8_t* kt = smem + S::kOffTile + static_cast<size_t>(x) * kTileBytes;
+        attend_tile(st, qa, kt, kt + kKTile, ublk[e] * kBS, p_tok, p.scale_log2, c_lo, c_hi, lane);
+      }
+      ++cnt;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&t_empty[x]);
+  }
+  named_barrier(kBarTok, 32 * kTokWarps);  // every token warp is done with the tiles
+
+  // ---- merge each token's warps, write the output or this split's partial ----------------
+  uint8_t* ws = smem + S::kOffTile;
+  {
+    float* mw = reinterpret_cast<float*>(ws + warp * S::kWarpState);
+    float* lw = mw + 16;
+    float* ow = lw + 16;
+    const float l0 = quad_sum(st.l[0]), l1 = quad_sum(st.l[1]);
+    if (tq == 0) {
+      mw[gid] = st.m[0];
+      mw[gid + 8] = st.m[1];
+      lw[gid] = l0;
+      lw[gid + 8] = l1;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      *reinterpret_cast<float2*>(ow + gid * kD + 8 * k + 2 * tq) = make_float2(st.o[k][0], st.o[k][1]);
+      *reinterpret_cast<float2*>(ow + (gid + 8) * kD + 8 * k + 2 * tq) = make_float2(st.o[k][2], st.o[k][3]);
+    }
+  }
+  named_barrier(kBarTok, 32 * kTokWarps);
+  const bool aborted = *abort_flag != 0;
+  for (int e = tid; e < ql * kHPG * (kD / 4); e += 32 * kTokWarps) {
+    const int tk = e / (kHPG * (kD / 4));
+    const int hh = (e / (kD / 4)) % kHPG;
+    const int d4 = e % (kD / 4);
+    const int w0 = tk * wpt;
+    float M = -CUDART_INF_F;
+    for (int w = w0; w < w0 + wpt; ++w) M = fmaxf(M, reinterpret_cast<const float*>(ws + w * S::kWarpState)[hh]);
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
+      for (int w = w0; w < w0 + wpt; ++w) {
+        const float* mw = reinterpret_cast<const float*>(ws + w * S::kWarpState);
+        const float f = fast_exp2(mw[hh] - M);
+        Lsum += mw[16 + hh] * f;
+        const float4 o = *reinterpret_cast<const float4*>(mw + 32 + hh * kD + 4 * d4);
+        acc.x += o.x * f;
+        acc.y += o.y * f;
+        acc.z += o.z * f;
+        acc.w += o.w * f;
+      }
+    }
+    const bool zero = (M == -CUDART_INF_F) || Lsum <= 0.f || ((badm >> tk) & 1) || aborted;
+    const float inv = zero ? 0.f : 1.0f / Lsum;
+    const int64_t orow = static_cast<int64_t>(q0 + tk) * kQHeads + g * kHPG + hh;
+    if (p.splits == 1) {
+      const uint2 v = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+      *reinterpret_cast<uint2*>(p.out + orow * kD + 4 * d4) = v;
+    } else {
+      const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
+      *reinterpret_cast<float4*>(p.part_o + prow * kD + 4 * d4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (d4 == 0) p.part_lse[prow] = zero ? -CUDART_INF_F : M + __log2f(Lsum);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Batches of multi-token sequences (max_q_len > 1): one CTA of 8 warps per (query token, group,
+// split); a warp owns whole selected blocks (16 query heads x 128 keys):
+//  * its block's K and V regions (2 x 9,216 B, contiguous in the page) arrive with one 1-D
+//    bulk copy (cp.async.bulk + mbarrier) into the warp's own shared-memory stage;
+//  * K is dequantised register-direct into the B fragments of mma.sync.m16n8k32.e4m3 (the
+//    16 heads of the group on M), 32 keys at a time, the same lane/dim mapping as the indexer;
+//  * V of those 32 keys is dequantised once into a private swizzled f16 tile and read back
+//    transposed with ldmatrix.trans for mma.sync.m16n8k16.f16 (P straight from the QK^T
+//    accumulators);
+//  * online softmax per warp; O is rescaled only when some row maximum moved; the 8 warps'
+//    states are merged in shared memory at the end.
+// The tokens of one sequence select mostly different blocks (the union of 8 tokens' 16
+// selections is 50-80 blocks at 16K context), so sharing a block's dequant across them saves
+// little, while coupling them through one tile ring costs more: here each token is its own CTA.
+// The next block's copy is issued as soon as the last V chunk of the current block has been
+// dequantised, so it overlaps the remaining MMAs.
+namespace tok {
+
+constexpr int kAttnWarps = 8;
+constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr int kStageBytes = 2 * kRegion;  // K region then V region of one (page, group)
+constexpr int kChunkKeys = 32;
+constexpr int kVTileBytes = kChunkKeys * kD * 2;  // 32 keys x 128 dims f16
+
+struct TokSmem {
   static constexpr size_t kOffStage = 0;                                        // 8 x 18,432
   static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kAttnWarps) * kStageBytes;  // 8 x 8,192
   static constexpr size_t kOffLut = kOffV + static_cast<size_t>(kAttnWarps) * kVTileBytes;    // 2 KB
@@ -71,22 +536,8 @@ struct AttnSmem {
   // after the block loop, the stage area holds each warp's final state
   static constexpr size_t kWarpState = 16 * 4 * 2 + 16 * kD * 4;  // m, l, O[16][128]
 };
-static_assert(AttnSmem::kOffV >= kAttnWarps * AttnSmem::kWarpState, "merge area too small");
+static_assert(TokSmem::kOffV >= kAttnWarps * TokSmem::kWarpState, "merge area too small");
 
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-}
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  return v + __shfl_xor_sync(0xffffffffu, v, 2);
-}
-
-// Per-warp running softmax state for 16 heads (rows gid and gid+8 in this lane).
-struct WarpState {
-  float m[2], l[2];
-  float o[16][4];  // 16 n-tiles of 8 dims: (head gid, dims 8j+2t..+1), (head gid+8, ...)
-};
 
 // Dequantise keys r0 + gid + 8i (i = 0..3), dims 32t .. 32t+31, of a staged NVFP4 region into
 // the f16 tile `vt` (32 rows x 256 B, 16-byte chunk c of row r stored at chunk c ^ (r & 7)).
@@ -232,8 +683,8 @@ __device__ __forceinline__ void attend_block(WarpState& st, const uint32_t (&qa)
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p) {
-  using S = AttnSmem;
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tok(const AttnParams p) {
+  using S = TokSmem;
   extern __shared__ __align__(128) uint8_t smem[];
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
@@ -413,6 +864,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p) {
   }
 }
 
+}  // namespace tok
+
 // out[t][h] = sum_s w_s o_s / sum_s w_s with w_s = 2^(lse_s - max lse); zeros if no split has keys.
 __global__ void __launch_bounds__(256) k_attn_merge(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                                     int32_t splits, int32_t T, uint16_t* __restrict__ out) {
@@ -442,10 +895,88 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float* __restrict__ pa
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
+// Splits of each (query token, group)'s blocks for the per-token kernel, from T alone: enough
+// CTAs for about two per SM of a 152-SM GB300, at most 16 (one block per split).
+int tok_splits(int T) {
+  const int items = 4 * T;
+  if (items <= 0 || items >= 304) return 1;
+  const int s = (304 + items - 1) / items;
+  return s > 16 ? 16 : s;
+}
+
 size_t attn_ws_bytes(int T, int splits) {
   if (splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(splits) * T * kQHeads;
   return msa_host::align256(rows * kD * 4) + msa_host::align256(rows * 4);
+}
+
+// Argument checks shared by both entry points; fills everything of p but the partial buffers.
+// Returns MSA_OK with p->T == 0 when there is nothing to do.
+msa_status attn_setup(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache, const uint8_t* q,
+                      const int32_t* sel, float softmax_scale, int32_t num_splits, uint16_t* out, uint32_t* status,
+                      AttnParams* p) {
+  p->T = 0;
+  msa_status st = msa_host::check_geometry(geo);
+  if (st != MSA_OK) return st;
+  if ((st = msa_host::check_batch(batch)) != MSA_OK) return st;
+  if ((st = msa_host::check_cache(cache, false, true)) != MSA_OK) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits) return MSA_ERR_INVALID_ARG;
+  if (batch->B == 0 || batch->T == 0) return MSA_OK;
+  if (q == nullptr || sel == nullptr || out == nullptr || !msa_host::aligned(q, 16) || !msa_host::aligned(sel, 4) ||
+      !msa_host::aligned(out, 16))
+    return MSA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
+  p->B = batch->B;
+  p->T = batch->T;
+  p->maxb = batch->max_blocks_per_seq;
+  p->max_q_len = batch->max_q_len;
+  p->num_pages = cache->num_pages;
+  p->splits = num_splits > 0 ? num_splits
+                             : (batch->max_q_len == 1 ? msa_host::auto_splits(batch->B) : tok_splits(batch->T));
+  p->qsl = batch->query_start_loc;
+  p->seq_lens = batch->seq_lens;
+  p->block_table = batch->block_table;
+  p->kv_pages = cache->kv_pages;
+  p->q = q;
+  p->sel = sel;
+  p->scale_log2 = softmax_scale * 1.4426950408889634f;
+  p->out = out;
+  p->part_o = nullptr;
+  p->part_lse = nullptr;
+  p->status = status;
+  return MSA_OK;
+}
+
+// Point p's partial buffers into `ws` (attn_ws_bytes(T, splits) bytes) when splits > 1.
+void attn_bind_ws(AttnParams* p, void* ws) {
+  if (p->splits <= 1) return;
+  p->part_o = static_cast<float*>(ws);
+  p->part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                         msa_host::align256(static_cast<size_t>(p->splits) * p->T * kQHeads * kD * 4));
+}
+
+msa_status attn_launch(const AttnParams& p, const uint8_t* kv_pages, cudaStream_t stream) {
+  if (p.max_q_len > 1) {
+    if (cudaFuncSetAttribute(tok::k_attn_tok, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tok::TokSmem::kBytes)) != cudaSuccess)
+      return MSA_ERR_CUDA;
+    tok::k_attn_tok<<<p.T * 4 * p.splits, tok::kAttnThreads, tok::TokSmem::kBytes, stream>>>(p);
+    msa_status st = msa_host::launch_status();
+    if (st != MSA_OK) return st;
+    if (p.splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, p.splits, p.T, p.out, stream);
+    return MSA_OK;
+  }
+  alignas(64) CUtensorMap tmap;
+  if (!msa_host::kv_tensor_map(&tmap, kv_pages, static_cast<uint64_t>(p.num_pages > 0 ? p.num_pages : 1)))
+    return MSA_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
+      cudaSuccess)
+    return MSA_ERR_CUDA;
+  k_attn<<<p.B * 4 * p.splits, kAttnThreads, AttnSmem::kBytes, stream>>>(p, tmap);
+  msa_status st = msa_host::launch_status();
+  if (st != MSA_OK) return st;
+  if (p.splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, p.splits, p.T, p.out, stream);
+  return MSA_OK;
 }
 
 }  // namespace
@@ -456,7 +987,8 @@ using namespace msa_host;
 
 extern "C" size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, int32_t num_splits) {
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || num_splits < 0 || num_splits > kMaxSplits) return 0;
-  const int s = num_splits > 0 ? num_splits : auto_splits(T);
+  // room for either kernel's automatic choice (the batch's max_q_len picks the kernel)
+  const int s = num_splits > 0 ? num_splits : std::max(auto_splits(B), tok_splits(T));
   return attn_ws_bytes(T, s);
 }
 
@@ -471,47 +1003,14 @@ extern "C" msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_
                                              const uint8_t* q, const int32_t* sel, float softmax_scale,
                                              int32_t num_splits, void* workspace, size_t workspace_bytes,
                                              uint16_t* out, uint32_t* status, cudaStream_t stream) {
-  msa_status st = check_geometry(geo);
-  if (st != MSA_OK) return st;
-  if ((st = check_batch(batch)) != MSA_OK) return st;
-  if ((st = check_cache(cache, false, true)) != MSA_OK) return st;
-  if (num_splits < 0 || num_splits > kMaxSplits) return MSA_ERR_INVALID_ARG;
-  if (batch->B == 0 || batch->T == 0) return MSA_OK;
-  if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
-    return MSA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->T);
-  const size_t need = attn_ws_bytes(batch->T, splits);
+  AttnParams p;
+  msa_status st = attn_setup(geo, batch, cache, q, sel, softmax_scale, num_splits, out, status, &p);
+  if (st != MSA_OK || p.T == 0) return st;
+  const size_t need = attn_ws_bytes(p.T, p.splits);
   if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned(workspace, 256))))
     return MSA_ERR_INVALID_ARG;
-  AttnParams p;
-  p.B = batch->B;
-  p.T = batch->T;
-  p.maxb = batch->max_blocks_per_seq;
-  p.max_q_len = batch->max_q_len;
-  p.num_pages = cache->num_pages;
-  p.splits = splits;
-  p.qsl = batch->query_start_loc;
-  p.seq_lens = batch->seq_lens;
-  p.block_table = batch->block_table;
-  p.kv_pages = cache->kv_pages;
-  p.q = q;
-  p.sel = sel;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.out = out;
-  p.part_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
-  p.part_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                     align256(static_cast<size_t>(splits) * batch->T * kQHeads * kD * 4))
-                          : nullptr;
-  p.status = status;
-  if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
-      cudaSuccess)
-    return MSA_ERR_CUDA;
-  const int grid = batch->T * 4 * splits;
-  k_attn<<<grid, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
-  if ((st = launch_status()) != MSA_OK) return st;
-  if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
-  return MSA_OK;
+  attn_bind_ws(&p, workspace);
+  return attn_launch(p, cache->kv_pages, stream);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -555,45 +1054,13 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, co
                                                      const msa_cache* cache, const uint8_t* q, const int32_t* sel,
                                                      float softmax_scale, int32_t num_splits, uint16_t* out,
                                                      uint32_t* status, cudaStream_t stream) {
-  msa_status st = check_geometry(geo);
-  if (st != MSA_OK) return st;
-  if ((st = check_batch(batch)) != MSA_OK) return st;
-  if ((st = check_cache(cache, false, true)) != MSA_OK) return st;
-  if (num_splits < 0 || num_splits > kMaxSplits) return MSA_ERR_INVALID_ARG;
-  if (batch->B == 0 || batch->T == 0) return MSA_OK;
-  if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
-    return MSA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const int splits = num_splits > 0 ? num_splits : auto_splits(batch->T);
-  const size_t need = attn_ws_bytes(batch->T, splits);
+  AttnParams p;
+  msa_status st = attn_setup(geo, batch, cache, q, sel, softmax_scale, num_splits, out, status, &p);
+  if (st != MSA_OK || p.T == 0) return st;
+  const size_t need = attn_ws_bytes(p.T, p.splits);
   if (need > kNoAllocScratchBytes) return MSA_ERR_INVALID_ARG;  // too many tokens x splits for the array
   void* scratch = nullptr;
   if (need > 0 && (st = scratch_address(&scratch)) != MSA_OK) return st;
-  AttnParams p;
-  p.B = batch->B;
-  p.T = batch->T;
-  p.maxb = batch->max_blocks_per_seq;
-  p.max_q_len = batch->max_q_len;
-  p.num_pages = cache->num_pages;
-  p.splits = splits;
-  p.qsl = batch->query_start_loc;
-  p.seq_lens = batch->seq_lens;
-  p.block_table = batch->block_table;
-  p.kv_pages = cache->kv_pages;
-  p.q = q;
-  p.sel = sel;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.out = out;
-  p.part_o = splits > 1 ? static_cast<float*>(scratch) : nullptr;
-  p.part_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
-                                                     align256(static_cast<size_t>(splits) * batch->T * kQHeads * kD * 4))
-                          : nullptr;
-  p.status = status;
-  if (cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(AttnSmem::kBytes)) !=
-      cudaSuccess)
-    return MSA_ERR_CUDA;
-  k_attn<<<batch->T * 4 * splits, kAttnThreads, AttnSmem::kBytes, stream>>>(p);
-  if ((st = launch_status()) != MSA_OK) return st;
-  if (splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, splits, batch->T, out, stream);
-  return MSA_OK;
+  attn_bind_ws(&p, scratch);
+  return attn_launch(p, cache->kv_pages, stream);
 }

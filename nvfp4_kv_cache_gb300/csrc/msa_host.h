@@ -53,14 +53,14 @@ inline int num_sms() {
   return n;
 }
 
-// Splits of each (query token, group)'s selected blocks, chosen from T alone (so workspace
-// sizes are a pure function of the arguments): enough CTAs for about two per SM of a 152-SM
-// GB300, at most 16 (one block per split).
-inline int auto_splits(int T) {
-  const int items = 4 * T;
-  if (items <= 0 || items >= 304) return 1;
-  int s = (304 + items - 1) / items;
-  return s > 16 ? 16 : s;
+// Splits of each (sequence, group)'s union of selected blocks, chosen from B alone (so
+// workspace sizes are a pure function of the arguments): as many as keep the B x 4 x splits
+// CTAs (one per SM) within one wave of a 152-SM GB300, at least 1, at most 16.
+inline int auto_splits(int B) {
+  const int items = 4 * B;
+  if (items <= 0) return 1;
+  const int s = 152 / items;
+  return s < 1 ? 1 : (s > 16 ? 16 : s);
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -68,6 +68,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // A 2-D tensor map (CUtensorMap, 64-B aligned storage) over `rows` rows of 128 bytes at `base`
 // (16-B aligned), box = `box_rows` rows, 128-byte swizzle (defined in msa_indexer.cu).
 bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32_t box_rows);
+
+// A 3-D tensor map over a KV page pool: (128 B, 576 rows, num_pages pages), box = the 144 rows
+// of one head's K and V regions of one page, 128-byte swizzle (defined in msa_indexer.cu).
+bool kv_tensor_map(void* tmap64, const uint8_t* base, uint64_t num_pages);
 
 }  // namespace msa_host
 

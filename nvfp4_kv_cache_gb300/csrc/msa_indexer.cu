@@ -587,6 +587,19 @@ bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+bool kv_tensor_map(void* tmap64, const uint8_t* base, uint64_t num_pages) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = msa::tensor_map_encoder();
+  if (enc == nullptr || num_pages == 0 || num_pages > (1ull << 31)) return false;
+  constexpr uint64_t kRowsPerPage = msa::kKvPage / 128;  // 576
+  const cuuint64_t dims[3] = {128, kRowsPerPage, num_pages};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(msa::kKvPage)};
+  const cuuint32_t box[3] = {128, 2 * msa::kRegion / 128, 1};  // the K and V regions of one head
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(static_cast<CUtensorMap*>(tmap64), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace msa_host
 
 namespace msa {

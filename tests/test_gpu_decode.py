@@ -18,6 +18,10 @@ CASES = {
     "dense": dict(seq_lens=[2048, 1500, 130], q_lens=[1, 5, 2], seed=24),
     "padded": dict(seq_lens=[4000, 0, 2500, 700, 1], q_lens=[2, 0, 0, 1, 1], seed=25),
     "many": dict(seq_lens=[129 * k + 17 for k in range(1, 20)], q_lens=[(k % 8) + 1 for k in range(19)], seed=26),
+    # one query token per sequence: the single-token-batch attention kernel
+    "decode1": dict(seq_lens=[1000, 4096 + 77, 300, 9000 + 5, 129, 1, 2048], q_lens=[1] * 7, seed=27, hot=6),
+    "decode1_fp8": dict(seq_lens=[3000, 5000, 129], q_lens=[1, 1, 1], seed=28, index_dtype=1),
+    "decode1_padded": dict(seq_lens=[4000, 0, 2500, 700], q_lens=[1, 0, 1, 1], seed=29),
 }
 
 
@@ -72,12 +76,13 @@ def test_decode_step_matches_oracle(msa, case):
     compare_case(w, dl, o)
 
 
+@pytest.mark.parametrize("case", ["ragged", "decode1"])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
-def test_standalone_stages_and_splits(msa, splits):
+def test_standalone_stages_and_splits(msa, splits, case):
     """indexer, top-k and attention called one by one (any split count) == the fused step."""
     from workloads.device import DeviceLayer, bf16_to_f32
 
-    w = W.small("ragged", **CASES["ragged"])
+    w = W.small(case, **CASES[case])
     dl = DeviceLayer(w, 0)
     o, st = run_step(msa, dl)
     assert st == msa.MSA_OK

@@ -36,10 +36,13 @@ def step(msa, dl, batch=None):
     return o, msa.msa_read_device_status(ws)
 
 
-def test_bad_page_id_is_reported_and_zero_filled(msa):
+# q_lens [2, 1] runs the per-token attention kernel, [1, 1] the single-token-batch kernel
+@pytest.mark.parametrize("q_lens", [[2, 1], [1, 1]])
+def test_bad_page_id_is_reported_and_zero_filled(msa, q_lens):
     from workloads.device import bf16_to_f32
 
-    w = W.small("fault", [3000, 2000], [2, 1], seed=41)
+    w = W.small("fault", [3000, 2000], q_lens, seed=41)
+    q0 = q_lens[0]
     dl = layer(w)
     good, st = step(msa, dl)
     assert st == msa.MSA_OK
@@ -51,23 +54,24 @@ def test_bad_page_id_is_reported_and_zero_filled(msa):
     o, st = step(msa, dl, batch)
     assert st == msa.MSA_ERR_DEVICE_FAULT
     s = o["scores"].cpu().numpy()
-    assert np.isneginf(s[0:2, :, 3]).all()
+    assert np.isneginf(s[0:q0, :, 3]).all()
     out = bf16_to_f32(o["out"])
-    assert (out[2] == 0).all(), "tokens whose selected page is bad are zero-filled"
+    assert (out[q0] == 0).all(), "tokens whose selected page is bad are zero-filled"
     # sequence 0 never selects the -inf block; its other scores are unchanged and its output
     # is the oracle's attention over its (new) selection
-    sel0 = o["sel"][0:2].cpu().numpy()
+    sel0 = o["sel"][0:q0].cpu().numpy()
     assert not (sel0 == 3).any()
     keep = [k for k in range(24) if k != 3]
-    assert torch.equal(o["scores"][0:2, :, keep], good["scores"][0:2, :, keep])
+    assert torch.equal(o["scores"][0:q0, :, keep], good["scores"][0:q0, :, keep])
     ref = OracleSeq(w, 0, 0, "cuda", kv_blocks=np.unique(sel0))
-    check_attention(out[0:2].cpu().numpy(), ref.attention(sel0, dl.softmax_scale), "seq 0")
+    check_attention(out[0:q0].cpu().numpy(), ref.attention(sel0, dl.softmax_scale), "seq 0")
 
 
-def test_selected_block_out_of_range(msa):
+@pytest.mark.parametrize("q_lens", [[1, 2], [1, 1]])
+def test_selected_block_out_of_range(msa, q_lens):
     from workloads.device import bf16_to_f32
 
-    w = W.small("selbad", [1500, 900], [1, 2], seed=42)
+    w = W.small("selbad", [1500, 900], q_lens, seed=42)
     dl = layer(w)
     o, st = step(msa, dl)
     sel = o["sel"].clone()

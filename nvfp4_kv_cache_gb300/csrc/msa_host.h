@@ -53,11 +53,11 @@ inline int num_sms() {
   return n;
 }
 
-// Splits of each (sequence, group)'s union of selected blocks, chosen from B alone (so
-// workspace sizes are a pure function of the arguments): as many as keep the B x 4 x splits
-// CTAs (one per SM) within one wave of a 152-SM GB300, at least 1, at most 16.
-inline int auto_splits(int B) {
-  const int items = 4 * B;
+// Splits of each (query token, group)'s selected blocks, chosen from T alone (so workspace
+// sizes are a pure function of the arguments): as many as keep the T x 4 x splits CTAs (one
+// per SM) within one wave of a 152-SM GB300, at least 1, at most 16.
+inline int auto_splits(int T) {
+  const int items = 4 * T;
   if (items <= 0) return 1;
   const int s = 152 / items;
   return s < 1 ? 1 : (s > 16 ? 16 : s);

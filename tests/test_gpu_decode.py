@@ -22,6 +22,8 @@ CASES = {
     "decode1": dict(seq_lens=[1000, 4096 + 77, 300, 9000 + 5, 129, 1, 2048], q_lens=[1] * 7, seed=27, hot=6),
     "decode1_fp8": dict(seq_lens=[3000, 5000, 129], q_lens=[1, 1, 1], seed=28, index_dtype=1),
     "decode1_padded": dict(seq_lens=[4000, 0, 2500, 700], q_lens=[1, 0, 1, 1], seed=29),
+    # more than 76 tokens: the attention kernel that packs a (token, group) into one CTA
+    "many_tokens": dict(seq_lens=[1500 + 301 * k for k in range(12)], q_lens=[8] * 10 + [3, 5], seed=30, hot=4),
 }
 
 
@@ -76,7 +78,7 @@ def test_decode_step_matches_oracle(msa, case):
     compare_case(w, dl, o)
 
 
-@pytest.mark.parametrize("case", ["ragged", "decode1"])
+@pytest.mark.parametrize("case", ["ragged", "decode1", "many_tokens"])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
 def test_standalone_stages_and_splits(msa, splits, case):
     """indexer, top-k and attention called one by one (any split count) == the fused step."""

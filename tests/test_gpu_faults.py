@@ -36,12 +36,16 @@ def step(msa, dl, batch=None):
     return o, msa.msa_read_device_status(ws)
 
 
-# q_lens [2, 1] runs the per-token attention kernel, [1, 1] the single-token-batch kernel
-@pytest.mark.parametrize("q_lens", [[2, 1], [1, 1]])
+# few tokens run the attention kernel that spreads a (token, group) over an SM; 88 tokens run
+# the one that packs a (token, group) into one CTA of eight block-owning warps
+MANY = [8, 8] + [8] * 9
+
+
+@pytest.mark.parametrize("q_lens", [[2, 1], [1, 1], MANY])
 def test_bad_page_id_is_reported_and_zero_filled(msa, q_lens):
     from workloads.device import bf16_to_f32
 
-    w = W.small("fault", [3000, 2000], q_lens, seed=41)
+    w = W.small("fault", [3000, 2000] + [1000] * (len(q_lens) - 2), q_lens, seed=41)
     q0 = q_lens[0]
     dl = layer(w)
     good, st = step(msa, dl)
@@ -67,11 +71,11 @@ def test_bad_page_id_is_reported_and_zero_filled(msa, q_lens):
     check_attention(out[0:q0].cpu().numpy(), ref.attention(sel0, dl.softmax_scale), "seq 0")
 
 
-@pytest.mark.parametrize("q_lens", [[1, 2], [1, 1]])
+@pytest.mark.parametrize("q_lens", [[1, 2], [1, 1], MANY])
 def test_selected_block_out_of_range(msa, q_lens):
     from workloads.device import bf16_to_f32
 
-    w = W.small("selbad", [1500, 900], q_lens, seed=42)
+    w = W.small("selbad", [1500, 900] + [1000] * (len(q_lens) - 2), q_lens, seed=42)
     dl = layer(w)
     o, st = step(msa, dl)
     sel = o["sel"].clone()

@@ -34,6 +34,8 @@
 // where it is defined.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -834,6 +836,484 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tok(const AttnParams p
 
 }  // namespace tok
 
+// ------------------------------------------------------------------------------------------
+// Batches of many tokens, on the 5th-generation tensor cores: one CTA of 16 warps per (query
+// token, group, split). The keys of a block are the M = 128 rows of both tcgen05 MMAs, so the
+// accumulators live in TMEM and the CUDA cores only dequantise and run the softmax:
+//  * S^T = K Q^T: kind::f8f6f4, A = the block's 128 x 128 E4M3 K tile in TMEM (the K dequant
+//    threads store their key row with tcgen05.st), B = the token's 16 x 128 E4M3 query tile
+//    (K-major, 128-byte swizzle, one tensor copy), N = 16 heads, into a ring of two TMEM
+//    score buffers; one warp issues these;
+//  * O^T += V^T P^T: kind::f16, A = the block's V tile as f16 (E4M3 -> f16 exact) in shared
+//    memory, MN-major with 128-byte swizzle, B = P^T (16 heads x 128 keys, K-major, 128-byte
+//    swizzle), N = 16, into one TMEM accumulator of 128 dims x 16 heads; another warp issues
+//    these (an MMA costs ~80 cycles of issue, so S and PV each get their own issuer);
+//  * three groups of four warps, thread = key = TMEM lane: K dequant, V dequant, softmax. A
+//    softmax thread reads its key's 16 head scores and writes P = exp2(s - m). The reference
+//    maximum m of a head only moves when some score of a block exceeds it by more than 2^8 (a
+//    vote of the four softmax warps), so P <= 256 in f16, the block maximum is reduced across
+//    the 128 threads only then, and O^T is rescaled in TMEM only then (after the PV MMA in
+//    flight has landed);
+//  * the output is O^T / l, the per-head sum l reduced across the 128 threads once.
+namespace tc {
+
+constexpr int kWarpProd = 0, kWarpMmaS = 1, kWarpMmaO = 2;  // warp 3 idles
+constexpr int kWarpK = 4, kWarpV = 8, kWarpSm = 12;         // groups of four warps
+constexpr int kThreads = 32 * 16;
+constexpr int kStages = 4;                                   // NVFP4 K+V stage ring
+constexpr int kStageBytes = 2 * kRegion;                     // K region then V region of one (page, group)
+constexpr int kQTile = kHPG * kD;                            // 16 heads x 128 E4M3
+constexpr int kVTile = kBS * kD * 2;                         // 128 keys x 128 f16
+constexpr int kPTile = kHPG * kBS * 2;                       // 16 heads x 128 keys f16
+constexpr uint32_t kVLbo = 16384;                            // V tile: the two 64-dim atom columns
+constexpr uint32_t kVSbo = 1024;                             //         8-key groups
+constexpr float kRescaleLog2 = 8.0f;                         // m moves when a score exceeds it by this
+constexpr int kBarWork = 4;                                  // named barrier of the softmax warps
+// TMEM columns: K tiles [2] 0..63, S^T [2] 64..95, O^T 96..111
+constexpr uint32_t kColK = 0, kColS = 64, kColO = 96;
+constexpr int kTmemCols = 128;
+
+struct Smem {
+  static constexpr size_t kOffQ = 0;                                                     // 2 KB
+  static constexpr size_t kOffStage = 1024 * 2;                                           // 4 x 18 KB
+  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kStages) * kStageBytes;  // 2 x 32 KB
+  static constexpr size_t kOffP = kOffV + 2 * static_cast<size_t>(kVTile);                // 2 x 4 KB
+  static constexpr size_t kOffBar = kOffP + 2 * static_cast<size_t>(kPTile);
+  // q_full; st_full, st_empty [kStages]; ka_full, ka_empty, v_full, v_empty, s_full, s_empty,
+  // p_full, p_empty [2]; o_final; fin_s; fin_o
+  static constexpr int kBars = 1 + 2 * kStages + 2 * 8 + 3;
+  static constexpr size_t kOffLut = kOffBar + 8 * 32;
+  static constexpr size_t kOffRed = kOffLut + 256 * 8;   // [2][4 warps][16] fp32
+  static constexpr size_t kOffBlk = kOffRed + 2 * 4 * 16 * 4;
+  static constexpr size_t kOffPhys = kOffBlk + 4 * kSel;
+  static constexpr size_t kOffMisc = kOffPhys + 4 * kSel;
+  static constexpr size_t kBytes = 1024 + kOffMisc + 64;  // + alignment slack
+};
+static_assert(Smem::kBars <= 32, "barrier area");
+static_assert(Smem::kOffStage % 1024 == 0 && Smem::kOffV % 1024 == 0 && Smem::kOffP % 1024 == 0,
+              "swizzled tiles sit on 1024-B boundaries");
+static_assert(Smem::kBytes <= 232448, "shared memory per CTA");
+
+// Op-reduce v[0..15] over the 32 lanes: afterwards lanes 2h and 2h + 1 hold head h's result.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float a8[8], a4[4], a2[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // keep heads 8..15 in lanes with bit 4 set
+    const float send = u16 ? v[i] : v[i + 8], keep = u16 ? v[i + 8] : v[i];
+    a8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u8 ? a8[i] : a8[i + 4], keep = u8 ? a8[i + 4] : a8[i];
+    a4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u4 ? a4[i] : a4[i + 2], keep = u4 ? a4[i + 2] : a4[i];
+    a2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  const float send = u2 ? a2[0] : a2[1], keep = u2 ? a2[1] : a2[0];
+  const float a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+}
+
+// Op-reduce v[0..15] over the 128 worker threads into out[0..15] (the same in every thread).
+// red: [4][16] fp32 shared scratch, not reused before every worker has passed the next call's
+// barrier (the caller alternates two of them).
+template <bool kMax>
+__device__ __forceinline__ void group_reduce16(const float (&v)[16], float (&out)[16], float* red, int wq, int lane) {
+  const float r = warp_reduce16<kMax>(v, lane);
+  if ((lane & 1) == 0) red[wq * 16 + (lane >> 1)] = r;
+  named_barrier(kBarWork, 128);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float4 x0 = *reinterpret_cast<const float4*>(red + 4 * c);
+    const float4 x1 = *reinterpret_cast<const float4*>(red + 16 + 4 * c);
+    const float4 x2 = *reinterpret_cast<const float4*>(red + 32 + 4 * c);
+    const float4 x3 = *reinterpret_cast<const float4*>(red + 48 + 4 * c);
+    if (kMax) {
+      out[4 * c + 0] = fmaxf(fmaxf(x0.x, x1.x), fmaxf(x2.x, x3.x));
+      out[4 * c + 1] = fmaxf(fmaxf(x0.y, x1.y), fmaxf(x2.y, x3.y));
+      out[4 * c + 2] = fmaxf(fmaxf(x0.z, x1.z), fmaxf(x2.z, x3.z));
+      out[4 * c + 3] = fmaxf(fmaxf(x0.w, x1.w), fmaxf(x2.w, x3.w));
+    } else {
+      out[4 * c + 0] = (x0.x + x1.x) + (x2.x + x3.x);
+      out[4 * c + 1] = (x0.y + x1.y) + (x2.y + x3.y);
+      out[4 * c + 2] = (x0.z + x1.z) + (x2.z + x3.z);
+      out[4 * c + 3] = (x0.w + x1.w) + (x2.w + x3.w);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_tc(const AttnParams p, const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map) {
+  using S = Smem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* st_full = bars + 1;
+  uint64_t* st_empty = st_full + kStages;
+  uint64_t* ka_full = st_empty + kStages;
+  uint64_t* ka_empty = ka_full + 2;
+  uint64_t* v_full = ka_empty + 2;
+  uint64_t* v_empty = v_full + 2;
+  uint64_t* s_full = v_empty + 2;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_empty = p_full + 2;
+  uint64_t* o_final = p_empty + 2;
+  uint64_t* fin_s = o_final + 1;
+  uint64_t* fin_o = fin_s + 1;
+  uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
+  float* red = reinterpret_cast<float*>(smem + S::kOffRed);
+  int* blk = reinterpret_cast<int*>(smem + S::kOffBlk);
+  int* phys = reinterpret_cast<int*>(smem + S::kOffPhys);
+  int* nblk = reinterpret_cast<int*>(smem + S::kOffMisc);
+  int* bad = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 12);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % p.splits;
+  const int tg = blockIdx.x / p.splits;
+  const int t = tg >> 2, g = tg & 3;
+  int lo = 0, hi = p.B - 1;  // the sequence of token t (largest b with qsl[b] <= t)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
+  const int L = p.seq_lens[b];
+  if (!(t - q0 >= 0 && t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) {
+    if (tid == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+    return;
+  }
+  const int nb = ceil_div(L, kBS);
+  const int p_tok = L - ql + (t - q0);
+
+  // ---- prologue --------------------------------------------------------------------------
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&st_empty[i], 8);  // the K and the V dequant warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ka_full[i], 4);
+      mbar_init(&ka_empty[i], 1);
+      mbar_init(&v_full[i], 4);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_empty[i], 1);
+    }
+    mbar_init(o_final, 1);
+    mbar_init(fin_s, 1);
+    mbar_init(fin_o, 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+    *bad = 0;
+  }
+  if (warp == kWarpMmaS) tmem_alloc(tmem_slot, kTmemCols);
+  build_dequant_lut(lut, tid, kThreads);
+  if (warp == kWarpProd) {  // the distinct selected blocks of (t, g), in slot order, and their pages
+    const int v = lane < kSel ? p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + lane] : -1;
+    bool keep = v >= 0 && v < nb;
+    if (lane < kSel && v >= nb) {
+      set_status(p.status, MSA_ERR_DEVICE_FAULT);
+      atomicOr(bad, 1);
+    }
+    for (int j = 0; j < kSel; ++j) {
+      const int vj = __shfl_sync(0xffffffffu, v, j);
+      if (j < lane && vj == v) keep = false;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, keep && lane < kSel);
+    const int pos = __popc(m & ((1u << lane) - 1u));
+    if (keep && lane < kSel) {
+      blk[pos] = v;
+      const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
+      const bool ok = ph >= 0 && ph < p.num_pages;
+      phys[pos] = ok ? ph : 0;
+      if (!ok) {
+        set_status(p.status, MSA_ERR_DEVICE_FAULT);
+        atomicOr(bad, 1);
+      }
+    }
+    if (lane == 0) *nblk = __popc(m);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool is_bad = *bad != 0;
+  const int nsel = is_bad ? 0 : *nblk;
+  const int i0 = (nsel * split) / p.splits, i1 = (nsel * (split + 1)) / p.splits;
+  const int n = i1 - i0;  // blocks of this CTA: entries i0 .. i1-1
+  bool ok = true;
+  auto give_up = [&]() {
+    if (lane == 0) {
+      if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  };
+  // a give-up stops this warp's work at once; every later wait is skipped
+  auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+    if (!ok) return false;
+    ok = warp_wait(bar, parity, abort_flag);
+    if (!ok) give_up();
+    return ok;
+  };
+
+  if (warp == kWarpProd) {
+    // ---- producer ------------------------------------------------------------------------
+    if (lane == 0 && n > 0) {
+      prefetch_tensormap(&kv_map);
+      prefetch_tensormap(&q_map);
+      mbar_arrive_expect_tx(q_full, kQTile);
+      tma_load_2d(smem + S::kOffQ, &q_map, 0, t * kQHeads + g * kHPG, q_full, policy_evict_first());
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(&st_empty[s], (static_cast<uint32_t>(j / kStages) & 1u) ^ 1u, abort_flag)) {
+          if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&st_full[s], kStageBytes);
+        tma_load_3d(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, &kv_map, 0, 2 * g * (kRegion / kD),
+                    phys[i0 + j], &st_full[s]);
+        issued = j + 1;
+      }
+      // copies that nobody waited for (after a give-up): wait before the CTA's memory goes
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        if (!mbar_wait_bounded(&st_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
+      if (!mbar_wait_bounded(q_full, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+  } else if (warp == kWarpMmaS) {
+    // ---- S(j) = K(j) Q^T; the whole warp runs the loop, lane 0 issues ------------------------
+    constexpr uint32_t idesc_s = idesc_e4m3_f32(128, kHPG);
+    const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + S::kOffQ));
+    if (n > 0) wait_ok(q_full, 0u);
+    for (int j = 0; ok && j < n; ++j) {
+      const int x = j & 1;
+      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+      if (!wait_ok(&ka_full[x], par) || !wait_ok(&s_empty[x], par ^ 1u)) break;
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 32 E4M3 per MMA: 8 TMEM columns of A, +32 B of B
+          tc_mma_f8_ta(tmem + kColS + 16 * x, tmem + kColK + 32 * x + 8 * k, dq + 2 * k, idesc_s, k > 0 ? 1u : 0u);
+        tc_commit(&s_full[x]);
+        tc_commit(&ka_empty[x]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {  // nothing of this warp's is in flight when TMEM is released
+      tc_commit(fin_s);
+      if (!mbar_wait_bounded(fin_s, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMmaO) {
+    // ---- O^T += V(j)^T P(j)^T ------------------------------------------------------------------
+    constexpr uint32_t idesc_o = idesc_f16_f32_amn(128, kHPG);
+    for (int j = 0; ok && j < n; ++j) {
+      const int x = j & 1;
+      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+      if (!wait_ok(&v_full[x], par) || !wait_ok(&p_full[x], par)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t dv = sw128_mnmajor_desc(smem_u32(smem + S::kOffV + static_cast<size_t>(x) * kVTile), kVLbo, kVSbo);
+        const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + S::kOffP + static_cast<size_t>(x) * kPTile));
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // K = 16 keys per MMA: two 8-key groups of V; 32 B (or the next atom) of P
+          tc_mma_f16(tmem + kColO, dv + ((2 * kVSbo) >> 4) * k, dp + (((k >> 2) * 2048 + (k & 3) * 32) >> 4), idesc_o,
+                     (j > 0 || k > 0) ? 1u : 0u);
+        tc_commit(&v_empty[x]);
+        tc_commit(&p_empty[x]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      tc_commit(o_final);  // every PV issued has landed (the softmax warps read O^T after it)
+      tc_commit(fin_o);
+      if (!mbar_wait_bounded(fin_o, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= kWarpK && warp < kWarpV) {
+    // ---- K dequant: thread = key kr = TMEM lane; the row goes to K tile x in TMEM ------------
+    const int kr = 32 * (warp & 3) + lane;
+    const uint32_t lanes = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    for (int j = 0; j < n; ++j) {
+      const int s = j % kStages, x = j & 1;
+      if (!wait_ok(&st_full[s], static_cast<uint32_t>(j / kStages) & 1u)) break;
+      RawRow rk;
+      load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, kr, rk);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_empty[s]);
+      if (!wait_ok(&ka_empty[x], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u)) break;  // S(j - 2) has landed
+      uint32_t w[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t u[8];
+        dequant_quarter(rk, q, lut, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[8 * q + e] = u[e];
+      }
+      tc_fence_after();
+      tmem_st32(tmem + lanes + kColK + 32 * x, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ka_full[x]);
+    }
+  } else if (warp >= kWarpV && warp < kWarpSm) {
+    // ---- V dequant: thread = key kr; the row goes to the f16 V tile x (MN-major: K row kr) ---
+    const int kr = 32 * (warp & 3) + lane;
+    for (int j = 0; j < n; ++j) {
+      const int s = j % kStages, x = j & 1;
+      if (!wait_ok(&st_full[s], static_cast<uint32_t>(j / kStages) & 1u)) break;
+      RawRow rv;
+      load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes + kRegion, kr, rv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_empty[s]);
+      if (!wait_ok(&v_empty[x], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u)) break;  // PV(j - 2) has landed
+      uint8_t* vt = smem + S::kOffV + static_cast<size_t>(x) * kVTile + (kr >> 3) * kVSbo + (kr & 7) * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t u[8];
+        dequant_quarter(rv, q, lut, u);
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {  // dims 32 q + 8 hh .. +7 = chunk cc = 4 q + hh
+          const int cc = 4 * q + hh;
+          const uint4 v = make_uint4(cvt_f16x2_e4m3x2(u[2 * hh]), cvt_f16x2_e4m3x2(u[2 * hh] >> 16),
+                                     cvt_f16x2_e4m3x2(u[2 * hh + 1]), cvt_f16x2_e4m3x2(u[2 * hh + 1] >> 16));
+          *reinterpret_cast<uint4*>(vt + (cc >> 3) * kVLbo + (((cc & 7) ^ (kr & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&v_full[x]);
+    }
+  } else if (warp >= kWarpSm) {
+    // ---- softmax: thread = key kr = TMEM lane --------------------------------------------------
+    const int wq = warp & 3;
+    const int kr = 32 * wq + lane;
+    const uint32_t lanes = static_cast<uint32_t>(32 * wq) << 16;
+    const float c = p.scale_log2;
+    float m_ref[16], l[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      m_ref[h] = -CUDART_INF_F;
+      l[h] = 0.f;
+    }
+    int nred = 0;  // reductions done: alternates the two scratch buffers
+    for (int j = 0; j < n; ++j) {
+      const int x = j & 1;
+      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+      float xs[16];
+      if (wait_ok(&s_full[x], par)) {
+        tc_fence_after();
+        uint32_t r[16];
+        tmem_ld16(tmem + lanes + kColS + 16 * x, r);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[x]);
+        const bool valid = blk[i0 + j] * kBS + kr <= p_tok;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) xs[h] = valid ? __uint_as_float(r[h]) * c : -CUDART_INF_F;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) xs[h] = -CUDART_INF_F;
+      }
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) need |= xs[h] > m_ref[h] + kRescaleLog2;
+      if (named_barrier_or(kBarWork, 128, need)) {  // the same answer in all four warps
+        float bm[16];
+        group_reduce16<true>(xs, bm, red + 64 * (nred & 1), wq, lane);
+        ++nred;
+        float cf[16];
+        bool moved = false;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float mn = fmaxf(m_ref[h], bm[h]);
+          cf[h] = (m_ref[h] == -CUDART_INF_F) ? 0.f : fast_exp2(m_ref[h] - mn);
+          moved |= mn != m_ref[h];
+          m_ref[h] = mn;
+          l[h] *= cf[h];
+        }
+        // O^T *= cf once PV(j - 1) has landed (PV(j) waits for this block's P)
+        if (moved && j > 0 && wait_ok(&p_empty[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
+          tc_fence_after();
+          uint32_t o[16];
+          tmem_ld16(tmem + lanes + kColO, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * cf[h]);
+          tmem_st16(tmem + lanes + kColO, o);
+          tmem_wait_st();
+          tc_fence_before();
+        }
+      }
+      // P = exp2(x - m) -> P^T tile x (free once PV(j - 2) has landed): row h, key kr
+      if (wait_ok(&p_empty[x], par ^ 1u)) {
+        uint8_t* pt = smem + S::kOffP + static_cast<size_t>(x) * kPTile + (kr >> 6) * 2048 + (kr & 7) * 2;
+        const int ch = (kr & 63) >> 3;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float mu = m_ref[h] == -CUDART_INF_F ? 0.f : m_ref[h];
+          const float pv = fast_exp2(xs[h] - mu);
+          l[h] += pv;
+          *reinterpret_cast<__half*>(pt + (h >> 3) * 1024 + (h & 7) * 128 + ((ch ^ (h & 7)) << 4)) = __float2half_rn(pv);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
+      }
+    }
+    // ---- output: lane kr = dim kr of O^T; l summed over the 128 keys' threads --------------
+    float lt[16];
+    group_reduce16<false>(l, lt, red + 64 * (nred & 1), wq, lane);
+    uint32_t o[16];
+    const bool have = n > 0 && ok && mbar_wait(o_final, 0u, abort_flag);
+    if (have) {
+      tc_fence_after();
+      tmem_ld16(tmem + lanes + kColO, o);
+      tmem_wait_ld();
+    }
+    const bool zero = !have || is_bad || *abort_flag != 0;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      const bool z = zero || !(lt[h] > 0.f);
+      const float val = z ? 0.f : __uint_as_float(o[h]) / lt[h];
+      const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
+      if (p.splits == 1) {
+        reinterpret_cast<__nv_bfloat16*>(p.out)[orow * kD + kr] = __float2bfloat16_rn(val);
+      } else {
+        const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
+        p.part_o[prow * kD + kr] = val;
+        if (kr == 0) p.part_lse[prow] = z ? -CUDART_INF_F : m_ref[h] + __log2f(lt[h]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMmaS) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+
 // out[t][h] = sum_s w_s o_s / sum_s w_s with w_s = 2^(lse_s - max lse); zeros if no split has keys.
 __global__ void __launch_bounds__(256) k_attn_merge(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                                     int32_t splits, int32_t T, uint16_t* __restrict__ out) {
@@ -932,6 +1412,20 @@ void attn_bind_ws(AttnParams* p, void* ws) {
 
 msa_status attn_launch(const AttnParams& p, const uint8_t* kv_pages, cudaStream_t stream) {
   if (use_tok_kernel(p.T)) {
+    alignas(64) CUtensorMap kv_map, q_map;
+    if (!msa_host::kv_tensor_map(&kv_map, kv_pages, static_cast<uint64_t>(p.num_pages > 0 ? p.num_pages : 1)) ||
+        !msa_host::rows128_tensor_map(&q_map, p.q, static_cast<uint64_t>(p.T) * kQHeads, kHPG))
+      return MSA_ERR_CUDA;
+    if (cudaFuncSetAttribute(tc::k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tc::Smem::kBytes)) != cudaSuccess)
+      return MSA_ERR_CUDA;
+    tc::k_attn_tc<<<p.T * 4 * p.splits, tc::kThreads, tc::Smem::kBytes, stream>>>(p, kv_map, q_map);
+    msa_status st = msa_host::launch_status();
+    if (st != MSA_OK) return st;
+    if (p.splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, p.splits, p.T, p.out, stream);
+    return MSA_OK;
+  }
+  if (false) {
     if (cudaFuncSetAttribute(tok::k_attn_tok, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tok::TokSmem::kBytes)) != cudaSuccess)
       return MSA_ERR_CUDA;

@@ -11,27 +11,22 @@
 // f16, because P rounded to E4M3 (3 mantissa bits) would cost several percent of relative
 // error.
 //
-// GB300 design: two kernels, picked by the batch's max_q_len.
+// GB300 design: two kernels, picked by the number of query tokens T (each (token, group) is
+// one unit of work: the token's 16 selected blocks of the group).
 //
-// k_attn (every sequence has one query token: plain decode): one CTA of 12 warps per
-// (sequence, group, split) that walks the union of the sequence's tokens' selected blocks
-// (for one token, its 16 blocks), each block once:
+// k_attn (T <= 76): one CTA of 12 warps per (token, group, split), a whole SM on one unit:
 //  * a 3-D tensor copy per block brings the group's K and V regions (144 rows of 128 B,
-//    128-byte swizzle) into a 3-deep stage ring;
-//  * four dequant warps (thread = key) turn the block into a 128 x 128 E4M3 K tile and a
-//    128 x 128 f16 V tile (E4M3 -> f16 is exact) in swizzled shared memory, a 3-deep ring;
-//  * eight token warps: the 16 heads of one query token are the M = 16 rows of
+//    128-byte swizzle) into a 4-deep stage ring;
+//  * two dequant groups of four warps (thread = key) take alternate blocks and turn each into
+//    a 128 x 128 E4M3 K tile and a 128 x 128 f16 V tile (E4M3 -> f16 is exact) in swizzled
+//    shared memory, a 3-deep ring;
+//  * four token warps each attend 32 keys of every block: the 16 heads are the M = 16 rows of
 //    mma.sync.m16n8k32.e4m3 (S = QK^T, K fragments by ldmatrix) and mma.sync.m16n8k16.f16
 //    (O += PV, V fragments by ldmatrix.trans, P straight from the S accumulators), with an
-//    online softmax; a token skips the blocks it did not select. A token gets
-//    8 / q_len' warps (q_len' = q_len rounded up to a power of two) that split the keys of
-//    each block (and, for q_len = 1, alternate blocks too); their states are merged at the end.
-//    So one token's 16 blocks are dequantised once by the whole CTA and its keys spread
-//    over 8 warps: short per-token latency, for batches of few tokens.
-//  * Splits of the union raise the CTA count when B x 4 is small; the partial (lse, o) pairs
-//    are merged by log-sum-exp in a second kernel.
-// tok::k_attn_tok (multi-token sequences): one CTA per (query token, group, split), described
-// where it is defined.
+//    online softmax; the four states are merged at the end.
+//  * Splits of the unit's blocks raise the CTA count when T x 4 is small; the partial
+//    (lse, o) pairs are merged by log-sum-exp in a second kernel.
+// tc::k_attn_tc (T > 76): a persistent tcgen05 kernel, described where it is defined.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -470,375 +465,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p, co
 }
 
 // ------------------------------------------------------------------------------------------
-// Batches of multi-token sequences (max_q_len > 1): one CTA of 8 warps per (query token, group,
-// split); a warp owns whole selected blocks (16 query heads x 128 keys):
-//  * its block's K and V regions (2 x 9,216 B, contiguous in the page) arrive with one 1-D
-//    bulk copy (cp.async.bulk + mbarrier) into the warp's own shared-memory stage;
-//  * K is dequantised register-direct into the B fragments of mma.sync.m16n8k32.e4m3 (the
-//    16 heads of the group on M), 32 keys at a time, the same lane/dim mapping as the indexer;
-//  * V of those 32 keys is dequantised once into a private swizzled f16 tile and read back
-//    transposed with ldmatrix.trans for mma.sync.m16n8k16.f16 (P straight from the QK^T
-//    accumulators);
-//  * online softmax per warp; O is rescaled only when some row maximum moved; the 8 warps'
-//    states are merged in shared memory at the end.
-// The tokens of one sequence select mostly different blocks (the union of 8 tokens' 16
-// selections is 50-80 blocks at 16K context), so sharing a block's dequant across them saves
-// little, while coupling them through one tile ring costs more: here each token is its own CTA.
-// The next block's copy is issued as soon as the last V chunk of the current block has been
-// dequantised, so it overlaps the remaining MMAs.
-namespace tok {
-
-constexpr int kAttnWarps = 8;
-constexpr int kAttnThreads = 32 * kAttnWarps;
-constexpr int kStageBytes = 2 * kRegion;  // K region then V region of one (page, group)
-constexpr int kChunkKeys = 32;
-constexpr int kVTileBytes = kChunkKeys * kD * 2;  // 32 keys x 128 dims f16
-
-struct TokSmem {
-  static constexpr size_t kOffStage = 0;                                        // 8 x 18,432
-  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kAttnWarps) * kStageBytes;  // 8 x 8,192
-  static constexpr size_t kOffLut = kOffV + static_cast<size_t>(kAttnWarps) * kVTileBytes;    // 2 KB
-  static constexpr size_t kOffBar = kOffLut + 256 * 8;                          // 8 mbarriers
-  static constexpr size_t kOffBlk = kOffBar + 8 * kAttnWarps;                   // 16 block ids
-  static constexpr size_t kOffPhys = kOffBlk + 4 * kSel;                        // 16 page ids
-  static constexpr size_t kOffMisc = kOffPhys + 4 * kSel;
-  static constexpr size_t kBytes = kOffMisc + 64;
-  // after the block loop, the stage area holds each warp's final state
-  static constexpr size_t kWarpState = 16 * 4 * 2 + 16 * kD * 4;  // m, l, O[16][128]
-};
-static_assert(TokSmem::kOffV >= kAttnWarps * TokSmem::kWarpState, "merge area too small");
-
-
-// Dequantise keys r0 + gid + 8i (i = 0..3), dims 32t .. 32t+31, of a staged NVFP4 region into
-// the f16 tile `vt` (32 rows x 256 B, 16-byte chunk c of row r stored at chunk c ^ (r & 7)).
-__device__ __forceinline__ void dequant_v_chunk(const uint8_t* vr, int r0, const uint2* lut, uint8_t* vt, int lane) {
-  const int gid = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int rl = gid + 8 * i;  // row inside the tile
-    const int r = r0 + rl;       // row inside the block
-    const uint4 c = lds128(vr + r * kRowCodes + 16 * t);
-    const uint32_t sc = *reinterpret_cast<const uint16_t*>(vr + kScaleOff + r * kRowScales + 2 * t);
-    const uint2 e0 = lut[sc & 0xFFu], e1 = lut[sc >> 8];
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // word q = dims 32t + 8q .. +7 = f16 chunk 4t + q
-      uint32_t lo, hi;
-      dq8(w[q], q < 2 ? e0 : e1, lo, hi);
-      const uint4 v = make_uint4(cvt_f16x2_e4m3x2(lo), cvt_f16x2_e4m3x2(lo >> 16), cvt_f16x2_e4m3x2(hi),
-                                 cvt_f16x2_e4m3x2(hi >> 16));
-      *reinterpret_cast<uint4*>(vt + rl * (2 * kD) + (((4 * t + q) ^ (rl & 7)) << 4)) = v;
-    }
-  }
-}
-
-// Copy of the next block into this warp's stage: src == nullptr means a bad page id (the
-// barrier phase still completes, with no bytes).
-__device__ __forceinline__ void issue_stage(uint8_t* stage, const uint8_t* src, uint64_t* bar) {
-  if (src != nullptr) {
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    bulk_g2s(stage, src, kStageBytes, bar);
-  } else {
-    mbar_arrive(bar);
-  }
-}
-
-// One block of 128 keys (K, V staged at kr, kr + kRegion) for the 16 heads of this warp.
-// Once every key and value of the stage has been read, lane 0 starts the copy of the warp's
-// next block (has_next; next_src as for issue_stage) into the same stage.
-__device__ __forceinline__ void attend_block(WarpState& st, const uint32_t (&qa)[4][4], uint8_t* kr,
-                                             const uint2* lut, uint8_t* vt, int blk_pos0, int p_tok, float scale_log2,
-                                             int lane, bool has_next, const uint8_t* next_src, uint64_t* bar) {
-  const int gid = lane >> 2, t = lane & 3;
-  const uint8_t* vr = kr + kRegion;
-  bool issued = !has_next;
-#pragma unroll 1
-  for (int c = 0; c < kBS / kChunkKeys; ++c) {
-    const int k0 = c * kChunkKeys;
-    if (blk_pos0 + k0 > p_tok) break;  // every remaining key lies after the query position
-    // ---- S = Q K^T for keys k0 .. k0+31 (4 n-tiles of 8 keys)
-    float x[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int key = k0 + 8 * j + gid;
-      const uint4 cw = lds128(kr + key * kRowCodes + 16 * t);
-      const uint32_t sc = *reinterpret_cast<const uint16_t*>(kr + kScaleOff + key * kRowScales + 2 * t);
-      const uint2 e0 = lut[sc & 0xFFu], e1 = lut[sc >> 8];
-      uint32_t b[4][2];
-      dq8(cw.x, e0, b[0][0], b[0][1]);
-      dq8(cw.y, e0, b[1][0], b[1][1]);
-      dq8(cw.z, e1, b[2][0], b[2][1]);
-      dq8(cw.w, e1, b[3][0], b[3][1]);
-      mma_e4m3_zc(x[j], qa[0][0], qa[0][1], qa[0][2], qa[0][3], b[0][0], b[0][1]);
-#pragma unroll
-      for (int s = 1; s < 4; ++s) mma_e4m3(x[j], qa[s][0], qa[s][1], qa[s][2], qa[s][3], b[s][0], b[s][1]);
-    }
-    // ---- V of these keys -> f16 tile; after the last chunk the stage is fully read
-    dequant_v_chunk(vr, k0, lut, vt, lane);
-    if (!issued && (c == kBS / kChunkKeys - 1 || blk_pos0 + k0 + kChunkKeys > p_tok)) {
-      __syncwarp();
-      if (lane == 0) issue_stage(kr, next_src, bar);
-      issued = true;
-    }
-    // ---- scale, causal mask, online softmax
-    const bool need_mask = blk_pos0 + k0 + kChunkKeys - 1 > p_tok;
-    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v = x[j][i] * scale_log2;
-        if (need_mask && blk_pos0 + k0 + 8 * j + 2 * t + (i & 1) > p_tok) v = -CUDART_INF_F;
-        x[j][i] = v;
-      }
-      mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][1]));
-      mx1 = fmaxf(mx1, fmaxf(x[j][2], x[j][3]));
-    }
-    mx0 = quad_max(mx0);
-    mx1 = quad_max(mx1);
-    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-    const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
-    const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
-    if (__any_sync(0xffffffffu, mn0 != st.m[0] || mn1 != st.m[1])) {
-      const float c0 = fast_exp2(st.m[0] - mu0), c1 = fast_exp2(st.m[1] - mu1);
-      st.l[0] *= c0;
-      st.l[1] *= c1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        st.o[n][0] *= c0;
-        st.o[n][1] *= c0;
-        st.o[n][2] *= c1;
-        st.o[n][3] *= c1;
-      }
-      st.m[0] = mn0;
-      st.m[1] = mn1;
-    }
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[j][0] = fast_exp2(x[j][0] - mu0);
-      x[j][1] = fast_exp2(x[j][1] - mu0);
-      x[j][2] = fast_exp2(x[j][2] - mu1);
-      x[j][3] = fast_exp2(x[j][3] - mu1);
-      ls0 += x[j][0] + x[j][1];
-      ls1 += x[j][2] + x[j][3];
-    }
-    st.l[0] += ls0;
-    st.l[1] += ls1;
-    __syncwarp();  // the V tile is complete
-    // ---- O += P V: 2 k-steps of 16 keys, 8 pairs of 8-dim n-tiles
-    const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t a0 = pack_f16x2(x[2 * kk][0], x[2 * kk][1]);
-      const uint32_t a1 = pack_f16x2(x[2 * kk][2], x[2 * kk][3]);
-      const uint32_t a2 = pack_f16x2(x[2 * kk + 1][0], x[2 * kk + 1][1]);
-      const uint32_t a3 = pack_f16x2(x[2 * kk + 1][2], x[2 * kk + 1][3]);
-      const int rl = 16 * kk + (mi & 1) * 8 + ri;
-      const uint8_t* vrow = vt + rl * (2 * kD);
-#pragma unroll
-      for (int dn = 0; dn < 8; ++dn) {
-        const int chunk = 2 * dn + (mi >> 1);
-        uint32_t r[4];
-        ldmatrix_x4_trans(r, vrow + ((chunk ^ (rl & 7)) << 4));
-        mma_f16(st.o[2 * dn], a0, a1, a2, a3, r[0], r[1]);
-        mma_f16(st.o[2 * dn + 1], a0, a1, a2, a3, r[2], r[3]);
-      }
-    }
-    __syncwarp();  // before the next chunk overwrites the V tile
-  }
-  if (!issued) {  // (not reached: the first chunk always holds a valid key)
-    __syncwarp();
-    if (lane == 0) issue_stage(kr, next_src, bar);
-  }
-}
-
-__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tok(const AttnParams p) {
-  using S = TokSmem;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  int* blk = reinterpret_cast<int*>(smem + S::kOffBlk);
-  int* phys = reinterpret_cast<int*>(smem + S::kOffPhys);
-  int* nblk = reinterpret_cast<int*>(smem + S::kOffMisc);
-  int* bad = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 8);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x % p.splits;
-  const int tg = blockIdx.x / p.splits;
-  const int t = tg >> 2, g = tg & 3;
-
-  // the sequence of token t (largest b with qsl[b] <= t)
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
-  const int L = p.seq_lens[b];
-  if (!(t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) {
-    if (tid == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
-    return;
-  }
-  const int nb = ceil_div(L, kBS);
-  const int p_tok = L - ql + (t - q0);
-
-  if (tid == 0) {
-    for (int w = 0; w < kAttnWarps; ++w) mbar_init(&bars[w], 1);
-    fence_mbar_init();
-    *abort_flag = 0;
-    *bad = 0;
-  }
-  build_dequant_lut(lut, tid, kAttnThreads);
-  // ---- the distinct selected blocks of (t, g), in slot order, and their pages
-  if (warp == 0) {
-    const int v = lane < kSel ? p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + lane] : -1;
-    bool keep = v >= 0 && v < nb;
-    if (lane < kSel && v >= nb) {
-      set_status(p.status, MSA_ERR_DEVICE_FAULT);
-      atomicOr(bad, 1);
-    }
-    // drop repeats of an earlier slot
-    for (int j = 0; j < kSel; ++j) {
-      const int vj = __shfl_sync(0xffffffffu, v, j);
-      if (j < lane && vj == v) keep = false;
-    }
-    const uint32_t m = __ballot_sync(0xffffffffu, keep && lane < kSel);
-    const int pos = __popc(m & ((1u << lane) - 1u));
-    if (keep && lane < kSel) {
-      blk[pos] = v;
-      const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
-      const bool ok = ph >= 0 && ph < p.num_pages;
-      phys[pos] = ok ? ph : -1;
-      if (!ok) {
-        set_status(p.status, MSA_ERR_DEVICE_FAULT);
-        atomicOr(bad, 1);
-      }
-    }
-    if (lane == 0) *nblk = __popc(m);
-  }
-  __syncthreads();
-  const int n = *nblk;
-  const bool is_bad = *bad != 0;
-  const int i0 = (n * split) / p.splits, i1 = (n * (split + 1)) / p.splits;
-
-  // ---- per-warp blocks i0 + warp, i0 + warp + 8, ...
-  const int gid = lane >> 2, tq = lane & 3;
-  WarpState st;
-  st.m[0] = st.m[1] = -CUDART_INF_F;
-  st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) st.o[k][0] = st.o[k][1] = st.o[k][2] = st.o[k][3] = 0.f;
-  uint32_t qa[4][4];
-  {
-    const uint8_t* qrow0 = p.q + (static_cast<int64_t>(t) * kQHeads + g * kHPG + gid) * kD + 32 * tq;
-    const uint8_t* qrow1 = qrow0 + 8 * kD;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint2 x0 = ldg_nc64(qrow0 + 8 * s);
-      const uint2 x1 = ldg_nc64(qrow1 + 8 * s);
-      qa[s][0] = x0.x;
-      qa[s][2] = x0.y;
-      qa[s][1] = x1.x;
-      qa[s][3] = x1.y;
-    }
-  }
-  uint8_t* stage = smem + S::kOffStage + static_cast<size_t>(warp) * kStageBytes;
-  uint8_t* vt = smem + S::kOffV + static_cast<size_t>(warp) * kVTileBytes;
-  uint64_t* bar = &bars[warp];
-  auto src_of = [&](int i) -> const uint8_t* {
-    const int ph = phys[i];
-    return ph >= 0 ? p.kv_pages + static_cast<int64_t>(ph) * kKvPage + (2 * g) * kRegion : nullptr;
-  };
-  int it = 0;
-  bool inflight = false;
-  if (!is_bad && i0 + warp < i1) {
-    if (lane == 0) issue_stage(stage, src_of(i0 + warp), bar);
-    inflight = true;
-  }
-  for (int i = i0 + warp; !is_bad && i < i1; i += kAttnWarps, ++it) {
-    if (!mbar_wait_bounded(bar, static_cast<uint32_t>(it) & 1u, kWaitLimitNs, abort_flag)) {
-      if (lane == 0) {
-        if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      break;  // inflight stays true: drained below
-    }
-    const bool has_next = i + kAttnWarps < i1;
-    // the copy of the next block starts inside, once this stage has been fully read
-    attend_block(st, qa, stage, lut, vt, blk[i] * kBS, p_tok, p.scale_log2, lane, has_next,
-                 has_next ? src_of(i + kAttnWarps) : nullptr, bar);
-    inflight = has_next;
-  }
-  if (inflight && lane == 0) {
-    // a copy into this warp's stage may still be in flight: wait for it (bounded)
-    mbar_wait_bounded(bar, static_cast<uint32_t>(it) & 1u, kWaitLimitNs, nullptr);
-  }
-  __syncthreads();
-
-  // ---- merge the 8 warps' states, write the output or this split's partial --------------
-  uint8_t* ws = smem;  // reuse the stages
-  {
-    float* mw = reinterpret_cast<float*>(ws + warp * S::kWarpState);
-    float* lw = mw + 16;
-    float* ow = lw + 16;
-    const float l0 = quad_sum(st.l[0]), l1 = quad_sum(st.l[1]);
-    if (tq == 0) {
-      mw[gid] = st.m[0];
-      mw[gid + 8] = st.m[1];
-      lw[gid] = l0;
-      lw[gid + 8] = l1;
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      *reinterpret_cast<float2*>(ow + gid * kD + 8 * k + 2 * tq) = make_float2(st.o[k][0], st.o[k][1]);
-      *reinterpret_cast<float2*>(ow + (gid + 8) * kD + 8 * k + 2 * tq) = make_float2(st.o[k][2], st.o[k][3]);
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < kHPG * (kD / 4); e += kAttnThreads) {
-    const int d4 = e % (kD / 4);
-    const int hh = e / (kD / 4);
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(ws + w * S::kWarpState)[hh]);
-    float Lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float* mw = reinterpret_cast<const float*>(ws + w * S::kWarpState);
-        const float f = fast_exp2(mw[hh] - M);
-        Lsum += mw[16 + hh] * f;
-        const float4 o = *reinterpret_cast<const float4*>(mw + 32 + hh * kD + 4 * d4);
-        acc.x += o.x * f;
-        acc.y += o.y * f;
-        acc.z += o.z * f;
-        acc.w += o.w * f;
-      }
-    }
-    const bool zero = (M == -CUDART_INF_F) || Lsum <= 0.f || is_bad;
-    const float inv = zero ? 0.f : 1.0f / Lsum;
-    const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + hh;
-    if (p.splits == 1) {
-      const uint2 v = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-      *reinterpret_cast<uint2*>(p.out + orow * kD + 4 * d4) = v;
-    } else {
-      const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
-      *reinterpret_cast<float4*>(p.part_o + prow * kD + 4 * d4) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      if (d4 == 0) p.part_lse[prow] = zero ? -CUDART_INF_F : M + __log2f(Lsum);
-    }
-  }
-}
-
-}  // namespace tok
-
-// ------------------------------------------------------------------------------------------
-// Batches of many tokens, on the 5th-generation tensor cores: one CTA of 16 warps per (query
-// token, group, split). The keys of a block are the M = 128 rows of both tcgen05 MMAs, so the
+// Batches of many tokens, on the 5th-generation tensor cores: a persistent CTA of 12 warps per
+// SM walks units of one (query token, group, split) each. The keys of a block are the M = 128 rows of both tcgen05 MMAs, so the
 // accumulators live in TMEM and the CUDA cores only dequantise and run the softmax:
 //  * S^T = K Q^T: kind::f8f6f4, A = the block's 128 x 128 E4M3 K tile in TMEM (the K dequant
 //    threads store their key row with tcgen05.st), B = the token's 16 x 128 E4M3 query tile
@@ -848,7 +476,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tok(const AttnParams p
 //    memory, MN-major with 128-byte swizzle, B = P^T (16 heads x 128 keys, K-major, 128-byte
 //    swizzle), N = 16, into one TMEM accumulator of 128 dims x 16 heads; another warp issues
 //    these (an MMA costs ~80 cycles of issue, so S and PV each get their own issuer);
-//  * three groups of four warps, thread = key = TMEM lane: K dequant, V dequant, softmax. A
+//  * two groups of four warps, thread = key = TMEM lane: K and V dequant, and softmax. A
 //    softmax thread reads its key's 16 head scores and writes P = exp2(s - m). The reference
 //    maximum m of a head only moves when some score of a block exceeds it by more than 2^8 (a
 //    vote of the four softmax warps), so P <= 256 in f16, the block maximum is reduced across
@@ -857,39 +485,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_tok(const AttnParams p
 //  * the output is O^T / l, the per-head sum l reduced across the 128 threads once.
 namespace tc {
 
-constexpr int kWarpProd = 0, kWarpMmaS = 1, kWarpMmaO = 2;  // warp 3 idles
-constexpr int kWarpK = 4, kWarpV = 8, kWarpSm = 12;         // groups of four warps
+constexpr int kWarpProd = 0, kWarpMmaS = 1, kWarpMmaO = 2;  // PV issuers: warps 2 (even blocks), 3 (odd)
+constexpr int kWarpDq = 4, kWarpSm = 12;                    // two dequant groups, one softmax group
 constexpr int kThreads = 32 * 16;
 constexpr int kStages = 4;                                   // NVFP4 K+V stage ring
 constexpr int kStageBytes = 2 * kRegion;                     // K region then V region of one (page, group)
 constexpr int kQTile = kHPG * kD;                            // 16 heads x 128 E4M3
 constexpr int kVTile = kBS * kD * 2;                         // 128 keys x 128 f16
 constexpr int kPTile = kHPG * kBS * 2;                       // 16 heads x 128 keys f16
+constexpr int kVTiles = 3;                                   // f16 V tile ring
 constexpr uint32_t kVLbo = 16384;                            // V tile: the two 64-dim atom columns
 constexpr uint32_t kVSbo = 1024;                             //         8-key groups
 constexpr float kRescaleLog2 = 8.0f;                         // m moves when a score exceeds it by this
 constexpr int kBarWork = 4;                                  // named barrier of the softmax warps
-// TMEM columns: K tiles [2] 0..63, S^T [2] 64..95, O^T 96..111
+// TMEM columns: K tiles [2] 0..63, S^T [2] 64..95, O^T [2 unit parities][2 block parities] 96..159
 constexpr uint32_t kColK = 0, kColS = 64, kColO = 96;
-constexpr int kTmemCols = 128;
+constexpr int kTmemCols = 256;
+
+// One unit of work = one (query token, group, split); a CTA walks units c, c + G, c + 2G, ...
+// The producer resolves each unit's selected blocks into a 2-deep ring of these records.
+struct UnitMeta {
+  int t, g, split, p_tok;  // token, group, split, the token's position
+  int n, valid, bad;       // blocks of this split; 0 = batch description inconsistent; a bad entry
+  int blk[kSel];           // the split's blocks (block ids), in slot order
+  int phys[kSel];          // and their pages
+  int pad;
+};
 
 struct Smem {
-  static constexpr size_t kOffQ = 0;                                                     // 2 KB
-  static constexpr size_t kOffStage = 1024 * 2;                                           // 4 x 18 KB
-  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kStages) * kStageBytes;  // 2 x 32 KB
-  static constexpr size_t kOffP = kOffV + 2 * static_cast<size_t>(kVTile);                // 2 x 4 KB
+  static constexpr size_t kOffQ = 0;                                                     // 2 x 2 KB
+  static constexpr size_t kOffStage = 1024 * 4;                                           // 4 x 18 KB
+  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kStages) * kStageBytes;  // 3 x 32 KB
+  static constexpr size_t kOffP = kOffV + kVTiles * static_cast<size_t>(kVTile);          // 2 x 4 KB
   static constexpr size_t kOffBar = kOffP + 2 * static_cast<size_t>(kPTile);
-  // q_full; st_full, st_empty [kStages]; ka_full, ka_empty, v_full, v_empty, s_full, s_empty,
-  // p_full, p_empty [2]; o_final; fin_s; fin_o
-  static constexpr int kBars = 1 + 2 * kStages + 2 * 8 + 3;
-  static constexpr size_t kOffLut = kOffBar + 8 * 32;
+  // st_full, st_empty [kStages]; v_full, v_empty [kVTiles]; ka_full, ka_empty, s_full, s_empty,
+  // p_full, p_empty, q_full, q_empty, o_final, o_free, meta_full, meta_empty [2]; fin_s; fin_o [2]
+  static constexpr int kBars = 2 * kStages + 2 * kVTiles + 2 * 12 + 3;
+  static constexpr size_t kOffLut = kOffBar + 8 * 48;
   static constexpr size_t kOffRed = kOffLut + 256 * 8;   // [2][4 warps][16] fp32
-  static constexpr size_t kOffBlk = kOffRed + 2 * 4 * 16 * 4;
-  static constexpr size_t kOffPhys = kOffBlk + 4 * kSel;
-  static constexpr size_t kOffMisc = kOffPhys + 4 * kSel;
+  static constexpr size_t kOffMeta = kOffRed + 2 * 4 * 16 * 4;
+  static constexpr size_t kOffMisc = kOffMeta + 2 * sizeof(UnitMeta);
   static constexpr size_t kBytes = 1024 + kOffMisc + 64;  // + alignment slack
 };
-static_assert(Smem::kBars <= 32, "barrier area");
+static_assert(Smem::kBars <= 48, "barrier area");
 static_assert(Smem::kOffStage % 1024 == 0 && Smem::kOffV % 1024 == 0 && Smem::kOffP % 1024 == 0,
               "swizzled tiles sit on 1024-B boundaries");
 static_assert(Smem::kBytes <= 232448, "shared memory per CTA");
@@ -954,107 +592,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* st_full = bars + 1;
+  uint64_t* st_full = bars;
   uint64_t* st_empty = st_full + kStages;
-  uint64_t* ka_full = st_empty + kStages;
+  uint64_t* v_full = st_empty + kStages;
+  uint64_t* v_empty = v_full + kVTiles;
+  uint64_t* ka_full = v_empty + kVTiles;
   uint64_t* ka_empty = ka_full + 2;
-  uint64_t* v_full = ka_empty + 2;
-  uint64_t* v_empty = v_full + 2;
-  uint64_t* s_full = v_empty + 2;
+  uint64_t* s_full = ka_empty + 2;
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;
   uint64_t* p_empty = p_full + 2;
-  uint64_t* o_final = p_empty + 2;
-  uint64_t* fin_s = o_final + 1;
+  uint64_t* q_full = p_empty + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* o_final = q_empty + 2;
+  uint64_t* o_free = o_final + 2;
+  uint64_t* meta_full = o_free + 2;
+  uint64_t* meta_empty = meta_full + 2;
+  uint64_t* fin_s = meta_empty + 2;
   uint64_t* fin_o = fin_s + 1;
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
   float* red = reinterpret_cast<float*>(smem + S::kOffRed);
-  int* blk = reinterpret_cast<int*>(smem + S::kOffBlk);
-  int* phys = reinterpret_cast<int*>(smem + S::kOffPhys);
-  int* nblk = reinterpret_cast<int*>(smem + S::kOffMisc);
-  int* bad = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 12);
+  UnitMeta* metas = reinterpret_cast<UnitMeta*>(smem + S::kOffMeta);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x % p.splits;
-  const int tg = blockIdx.x / p.splits;
-  const int t = tg >> 2, g = tg & 3;
-  int lo = 0, hi = p.B - 1;  // the sequence of token t (largest b with qsl[b] <= t)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
-  const int L = p.seq_lens[b];
-  if (!(t - q0 >= 0 && t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS)) {
-    if (tid == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
-    return;
-  }
-  const int nb = ceil_div(L, kBS);
-  const int p_tok = L - ql + (t - q0);
+  const int units = p.T * 4 * p.splits;
+  constexpr int kMetaUsers = 15;  // the S and two PV issuers, two dequant groups and the softmax group
 
   // ---- prologue --------------------------------------------------------------------------
   if (tid == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&st_full[i], 1);
-      mbar_init(&st_empty[i], 8);  // the K and the V dequant warps
+      mbar_init(&st_empty[i], 4);  // the dequant group of the stage's blocks
+    }
+    for (int i = 0; i < kVTiles; ++i) {
+      mbar_init(&v_full[i], 4);
+      mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ka_full[i], 4);
       mbar_init(&ka_empty[i], 1);
-      mbar_init(&v_full[i], 4);
-      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&p_empty[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&o_final[i], 2);  // both PV issuers
+      mbar_init(&o_free[i], 4);
+      mbar_init(&meta_full[i], 1);
+      mbar_init(&meta_empty[i], kMetaUsers);
     }
-    mbar_init(o_final, 1);
     mbar_init(fin_s, 1);
     mbar_init(fin_o, 1);
+    mbar_init(fin_o + 1, 1);
     fence_mbar_init();
     *abort_flag = 0;
-    *bad = 0;
   }
   if (warp == kWarpMmaS) tmem_alloc(tmem_slot, kTmemCols);
   build_dequant_lut(lut, tid, kThreads);
-  if (warp == kWarpProd) {  // the distinct selected blocks of (t, g), in slot order, and their pages
-    const int v = lane < kSel ? p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + lane] : -1;
-    bool keep = v >= 0 && v < nb;
-    if (lane < kSel && v >= nb) {
-      set_status(p.status, MSA_ERR_DEVICE_FAULT);
-      atomicOr(bad, 1);
-    }
-    for (int j = 0; j < kSel; ++j) {
-      const int vj = __shfl_sync(0xffffffffu, v, j);
-      if (j < lane && vj == v) keep = false;
-    }
-    const uint32_t m = __ballot_sync(0xffffffffu, keep && lane < kSel);
-    const int pos = __popc(m & ((1u << lane) - 1u));
-    if (keep && lane < kSel) {
-      blk[pos] = v;
-      const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
-      const bool ok = ph >= 0 && ph < p.num_pages;
-      phys[pos] = ok ? ph : 0;
-      if (!ok) {
-        set_status(p.status, MSA_ERR_DEVICE_FAULT);
-        atomicOr(bad, 1);
-      }
-    }
-    if (lane == 0) *nblk = __popc(m);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool is_bad = *bad != 0;
-  const int nsel = is_bad ? 0 : *nblk;
-  const int i0 = (nsel * split) / p.splits, i1 = (nsel * (split + 1)) / p.splits;
-  const int n = i1 - i0;  // blocks of this CTA: entries i0 .. i1-1
   bool ok = true;
   auto give_up = [&]() {
     if (lane == 0) {
@@ -1069,102 +670,202 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) give_up();
     return ok;
   };
+  // unit k of this CTA: its record (waited for) and, when done, its release
+  auto meta_get = [&](int k) -> const UnitMeta* {
+    if (!wait_ok(&meta_full[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) return nullptr;
+    return &metas[k & 1];
+  };
+  auto meta_put = [&](int k) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&meta_empty[k & 1]);
+  };
 
   if (warp == kWarpProd) {
-    // ---- producer ------------------------------------------------------------------------
-    if (lane == 0 && n > 0) {
+    // ---- producer: resolve each unit, then copy its query tile and its blocks -------------
+    int jg = 0, nq = 0;  // blocks and query tiles issued so far (ring positions)
+    if (lane == 0) {
       prefetch_tensormap(&kv_map);
       prefetch_tensormap(&q_map);
-      mbar_arrive_expect_tx(q_full, kQTile);
-      tma_load_2d(smem + S::kOffQ, &q_map, 0, t * kQHeads + g * kHPG, q_full, policy_evict_first());
-      int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(&st_empty[s], (static_cast<uint32_t>(j / kStages) & 1u) ^ 1u, abort_flag)) {
-          if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        mbar_arrive_expect_tx(&st_full[s], kStageBytes);
-        tma_load_3d(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, &kv_map, 0, 2 * g * (kRegion / kD),
-                    phys[i0 + j], &st_full[s]);
-        issued = j + 1;
+    }
+    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
+      if (!wait_ok(&meta_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
+      UnitMeta& m = metas[k & 1];
+      const int split = u % p.splits, tg = u / p.splits, t = tg >> 2, g = tg & 3;
+      int lo = 0, hi = p.B - 1;  // the sequence of token t (largest b with qsl[b] <= t)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
       }
-      // copies that nobody waited for (after a give-up): wait before the CTA's memory goes
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+      const int b = lo;
+      const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
+      const int L = p.seq_lens[b];
+      const bool valid = t - q0 >= 0 && t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS;
+      if (!valid && lane == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+      const int nb = valid ? ceil_div(L, kBS) : 0;
+      // the distinct selected blocks of (t, g), in slot order, and their pages
+      const int v = valid && lane < kSel ? p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + lane] : -1;
+      bool keep = v >= 0 && v < nb;
+      const bool out_of_range = lane < kSel && v >= nb && valid;
+      for (int j = 0; j < kSel; ++j) {
+        const int vj = __shfl_sync(0xffffffffu, v, j);
+        if (j < lane && vj == v) keep = false;
+      }
+      const uint32_t msk = __ballot_sync(0xffffffffu, keep && lane < kSel);
+      const int pos = __popc(msk & ((1u << lane) - 1u));
+      int ph = 0;
+      bool bad_page = false;
+      if (keep && lane < kSel) {
+        ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
+        bad_page = !(ph >= 0 && ph < p.num_pages);
+      }
+      const bool bad = __any_sync(0xffffffffu, out_of_range || bad_page);
+      if ((out_of_range || bad_page)) set_status(p.status, MSA_ERR_DEVICE_FAULT);
+      const int nsel = bad ? 0 : __popc(msk);
+      const int i0 = (nsel * split) / p.splits, i1 = (nsel * (split + 1)) / p.splits;
+      if (keep && lane < kSel && pos >= i0 && pos < i1) {
+        m.blk[pos - i0] = v;
+        m.phys[pos - i0] = bad_page ? 0 : ph;
+      }
+      if (lane == 0) {
+        m.t = t;
+        m.g = g;
+        m.split = split;
+        m.p_tok = L - ql + (t - q0);
+        m.n = i1 - i0;
+        m.valid = valid ? 1 : 0;
+        m.bad = bad ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&meta_full[k & 1]);  // release: the record is visible to the waiters
+      const int n = i1 - i0;
+      if (n == 0) continue;
+      // the query tile of the unit (free once the S MMAs of the unit two query tiles back landed)
+      if (!wait_ok(&q_empty[nq & 1], (static_cast<uint32_t>(nq >> 1) & 1u) ^ 1u)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&q_full[nq & 1], kQTile);
+        tma_load_2d(smem + S::kOffQ + static_cast<size_t>(nq & 1) * kQTile, &q_map, 0, t * kQHeads + g * kHPG,
+                    &q_full[nq & 1], policy_evict_first());
+      }
+      ++nq;
+      for (int j = 0; j < n; ++j, ++jg) {
+        const int s = jg % kStages;
+        if (!wait_ok(&st_empty[s], (static_cast<uint32_t>(jg / kStages) & 1u) ^ 1u)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&st_full[s], kStageBytes);
+          tma_load_3d(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, &kv_map, 0,
+                      2 * g * (kRegion / kD), m.phys[j], &st_full[s]);
+        }
+      }
+      if (!ok) break;
+    }
+    // copies that nobody waited for (after a give-up): wait before the CTA's memory goes
+    if (lane == 0) {
+      for (int j = jg > kStages ? jg - kStages : 0; j < jg; ++j)
         if (!mbar_wait_bounded(&st_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, kWaitLimitNs, nullptr))
           set_status(p.status, MSA_ERR_TIMEOUT);
-      if (!mbar_wait_bounded(q_full, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+      for (int j = nq > 2 ? nq - 2 : 0; j < nq; ++j)
+        if (!mbar_wait_bounded(&q_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
     }
   } else if (warp == kWarpMmaS) {
     // ---- S(j) = K(j) Q^T; the whole warp runs the loop, lane 0 issues ------------------------
     constexpr uint32_t idesc_s = idesc_e4m3_f32(128, kHPG);
-    const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + S::kOffQ));
-    if (n > 0) wait_ok(q_full, 0u);
-    for (int j = 0; ok && j < n; ++j) {
-      const int x = j & 1;
-      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
-      if (!wait_ok(&ka_full[x], par) || !wait_ok(&s_empty[x], par ^ 1u)) break;
-      tc_fence_after();
-      if (lane == 0) {
+    int jg = 0, nq = 0;
+    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
+      const UnitMeta* m = meta_get(k);
+      if (m == nullptr) break;
+      const int n = m->n;
+      meta_put(k);
+      if (n == 0) continue;
+      const int qs = nq & 1;
+      if (!wait_ok(&q_full[qs], static_cast<uint32_t>(nq >> 1) & 1u)) break;
+      const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + S::kOffQ + static_cast<size_t>(qs) * kQTile));
+      for (int j = 0; j < n; ++j, ++jg) {
+        const int x = jg & 1;
+        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
+        if (!wait_ok(&ka_full[x], par) || !wait_ok(&s_empty[x], par ^ 1u)) break;
+        tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // K = 32 E4M3 per MMA: 8 TMEM columns of A, +32 B of B
-          tc_mma_f8_ta(tmem + kColS + 16 * x, tmem + kColK + 32 * x + 8 * k, dq + 2 * k, idesc_s, k > 0 ? 1u : 0u);
-        tc_commit(&s_full[x]);
-        tc_commit(&ka_empty[x]);
+          for (int kk = 0; kk < 4; ++kk)  // K = 32 E4M3 per MMA: 8 TMEM columns of A, +32 B of B
+            tc_mma_f8_ta(tmem + kColS + 16 * x, tmem + kColK + 32 * x + 8 * kk, dq + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+          tc_commit(&s_full[x]);
+          tc_commit(&ka_empty[x]);
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&q_empty[qs]);  // the query tile is free once these MMAs landed
       __syncwarp();
+      ++nq;
     }
     if (lane == 0) {  // nothing of this warp's is in flight when TMEM is released
       tc_commit(fin_s);
       if (!mbar_wait_bounded(fin_s, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == kWarpMmaO) {
-    // ---- O^T += V(j)^T P(j)^T ------------------------------------------------------------------
+  } else if (warp == kWarpMmaO || warp == kWarpMmaO + 1) {
+    // ---- O^T(unit, x) += V(j)^T P(j)^T for the blocks j of parity x = warp - kWarpMmaO: two
+    // issuers, two accumulators (an MMA costs ~80 cycles of issue; the softmax adds the two) --
     constexpr uint32_t idesc_o = idesc_f16_f32_amn(128, kHPG);
-    for (int j = 0; ok && j < n; ++j) {
-      const int x = j & 1;
-      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
-      if (!wait_ok(&v_full[x], par) || !wait_ok(&p_full[x], par)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t dv = sw128_mnmajor_desc(smem_u32(smem + S::kOffV + static_cast<size_t>(x) * kVTile), kVLbo, kVSbo);
-        const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + S::kOffP + static_cast<size_t>(x) * kPTile));
+    const int x = warp - kWarpMmaO;
+    int jg = 0;
+    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
+      const UnitMeta* m = meta_get(k);
+      if (m == nullptr) break;
+      const int n = m->n;
+      meta_put(k);
+      const int os = k & 1;
+      // O^T[os] was read out by the softmax warps for unit k - 2
+      if (!wait_ok(&o_free[os], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
+      bool first = true;
+      for (int j = 0; j < n; ++j, ++jg) {
+        if ((jg & 1) != x) continue;
+        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
+        const int y = jg % kVTiles;
+        if (!wait_ok(&v_full[y], static_cast<uint32_t>(jg / kVTiles) & 1u) || !wait_ok(&p_full[x], par)) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dv = sw128_mnmajor_desc(smem_u32(smem + S::kOffV + static_cast<size_t>(y) * kVTile), kVLbo, kVSbo);
+          const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + S::kOffP + static_cast<size_t>(x) * kPTile));
 #pragma unroll
-        for (int k = 0; k < 8; ++k)  // K = 16 keys per MMA: two 8-key groups of V; 32 B (or the next atom) of P
-          tc_mma_f16(tmem + kColO, dv + ((2 * kVSbo) >> 4) * k, dp + (((k >> 2) * 2048 + (k & 3) * 32) >> 4), idesc_o,
-                     (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&v_empty[x]);
-        tc_commit(&p_empty[x]);
+          for (int kk = 0; kk < 8; ++kk)  // K = 16 keys per MMA: two 8-key groups of V; 32 B (or the next atom) of P
+            tc_mma_f16(tmem + kColO + 32 * os + 16 * x, dv + ((2 * kVSbo) >> 4) * kk,
+                       dp + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o, (!first || kk > 0) ? 1u : 0u);
+          tc_commit(&v_empty[y]);
+          tc_commit(&p_empty[x]);
+        }
+        __syncwarp();
+        first = false;
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&o_final[os]);  // every PV of this issuer for the unit has landed
       __syncwarp();
     }
     if (lane == 0) {
-      tc_commit(o_final);  // every PV issued has landed (the softmax warps read O^T after it)
-      tc_commit(fin_o);
-      if (!mbar_wait_bounded(fin_o, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+      tc_commit(fin_o + x);
+      if (!mbar_wait_bounded(fin_o + x, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp >= kWarpK && warp < kWarpV) {
-    // ---- K dequant: thread = key kr = TMEM lane; the row goes to K tile x in TMEM ------------
+  } else if (warp >= kWarpDq && warp < kWarpSm) {
+    // ---- dequant, two groups taking alternate blocks: thread = key kr = TMEM lane; K row -> K
+    // tile x in TMEM, V row -> f16 V tile y in shared memory (MN-major: key kr is K row kr) ---
     const int kr = 32 * (warp & 3) + lane;
     const uint32_t lanes = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    for (int j = 0; j < n; ++j) {
-      const int s = j % kStages, x = j & 1;
-      if (!wait_ok(&st_full[s], static_cast<uint32_t>(j / kStages) & 1u)) break;
+    int jg = 0;  // blocks started (K side)
+    auto do_k = [&](int jb) {  // K of block jb (stage jb % kStages stays held for its V)
+      const int s = jb % kStages, x = jb & 1;
+      if (!wait_ok(&st_full[s], static_cast<uint32_t>(jb / kStages) & 1u)) return;
       RawRow rk;
       load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, kr, rk);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&st_empty[s]);
-      if (!wait_ok(&ka_empty[x], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u)) break;  // S(j - 2) has landed
+      if (!wait_ok(&ka_empty[x], (static_cast<uint32_t>(jb >> 1) & 1u) ^ 1u)) return;  // S(jb - 2) has landed
       uint32_t w[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t u[8];
-        dequant_quarter(rk, q, lut, u);
+        uint32_t uu[8];
+        dequant_quarter(rk, q, lut, uu);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[8 * q + e] = u[e];
+        for (int e = 0; e < 8; ++e) w[8 * q + e] = uu[e];
       }
       tc_fence_after();
       tmem_st32(tmem + lanes + kColK + 32 * x, w);
@@ -1172,136 +873,192 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ka_full[x]);
-    }
-  } else if (warp >= kWarpV && warp < kWarpSm) {
-    // ---- V dequant: thread = key kr; the row goes to the f16 V tile x (MN-major: K row kr) ---
-    const int kr = 32 * (warp & 3) + lane;
-    for (int j = 0; j < n; ++j) {
-      const int s = j % kStages, x = j & 1;
-      if (!wait_ok(&st_full[s], static_cast<uint32_t>(j / kStages) & 1u)) break;
+    };
+    auto do_v = [&](int jb) {  // V of block jb, then its stage is free
+      const int s = jb % kStages, y = jb % kVTiles;
+      if (!ok) return;
       RawRow rv;
       load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes + kRegion, kr, rv);
       __syncwarp();
       if (lane == 0) mbar_arrive(&st_empty[s]);
-      if (!wait_ok(&v_empty[x], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u)) break;  // PV(j - 2) has landed
-      uint8_t* vt = smem + S::kOffV + static_cast<size_t>(x) * kVTile + (kr >> 3) * kVSbo + (kr & 7) * 128;
+      // PV(jb - kVTiles) has landed
+      if (!wait_ok(&v_empty[y], (static_cast<uint32_t>(jb / kVTiles) & 1u) ^ 1u)) return;
+      uint8_t* vt = smem + S::kOffV + static_cast<size_t>(y) * kVTile + (kr >> 3) * kVSbo + (kr & 7) * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t u[8];
-        dequant_quarter(rv, q, lut, u);
+        uint32_t uu[8];
+        dequant_quarter(rv, q, lut, uu);
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {  // dims 32 q + 8 hh .. +7 = chunk cc = 4 q + hh
           const int cc = 4 * q + hh;
-          const uint4 v = make_uint4(cvt_f16x2_e4m3x2(u[2 * hh]), cvt_f16x2_e4m3x2(u[2 * hh] >> 16),
-                                     cvt_f16x2_e4m3x2(u[2 * hh + 1]), cvt_f16x2_e4m3x2(u[2 * hh + 1] >> 16));
-          *reinterpret_cast<uint4*>(vt + (cc >> 3) * kVLbo + (((cc & 7) ^ (kr & 7)) << 4)) = v;
+          const uint4 vv = make_uint4(cvt_f16x2_e4m3x2(uu[2 * hh]), cvt_f16x2_e4m3x2(uu[2 * hh] >> 16),
+                                      cvt_f16x2_e4m3x2(uu[2 * hh + 1]), cvt_f16x2_e4m3x2(uu[2 * hh + 1] >> 16));
+          *reinterpret_cast<uint4*>(vt + (cc >> 3) * kVLbo + (((cc & 7) ^ (kr & 7)) << 4)) = vv;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&v_full[x]);
+      if (lane == 0) mbar_arrive(&v_full[y]);
+    };
+    const int gq = (warp - kWarpDq) >> 2;  // this group's blocks: jg % 2 == gq
+    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
+      const UnitMeta* m = meta_get(k);
+      if (m == nullptr) break;
+      const int n = m->n;
+      meta_put(k);
+      for (int j = 0; j < n && ok; ++j, ++jg) {
+        if ((jg & 1) != gq) continue;
+        do_k(jg);
+        do_v(jg);
+      }
+      if (!ok) break;
     }
   } else if (warp >= kWarpSm) {
-    // ---- softmax: thread = key kr = TMEM lane --------------------------------------------------
+    // ---- softmax: thread = key kr = TMEM lane ----------------------------------------------
     const int wq = warp & 3;
     const int kr = 32 * wq + lane;
     const uint32_t lanes = static_cast<uint32_t>(32 * wq) << 16;
     const float c = p.scale_log2;
-    float m_ref[16], l[16];
-#pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      m_ref[h] = -CUDART_INF_F;
-      l[h] = 0.f;
-    }
-    int nred = 0;  // reductions done: alternates the two scratch buffers
-    for (int j = 0; j < n; ++j) {
-      const int x = j & 1;
-      const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
-      float xs[16];
-      if (wait_ok(&s_full[x], par)) {
-        tc_fence_after();
-        uint32_t r[16];
-        tmem_ld16(tmem + lanes + kColS + 16 * x, r);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[x]);
-        const bool valid = blk[i0 + j] * kBS + kr <= p_tok;
-#pragma unroll
-        for (int h = 0; h < 16; ++h) xs[h] = valid ? __uint_as_float(r[h]) * c : -CUDART_INF_F;
-      } else {
-#pragma unroll
-        for (int h = 0; h < 16; ++h) xs[h] = -CUDART_INF_F;
+    int jg = 0, nred = 0;  // blocks seen; reductions done (alternates the two scratch buffers)
+    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
+      // every softmax warp takes the same path through a unit (the named barriers need all
+      // four): a warp whose wait gave up inside the unit keeps walking with its work skipped
+      const UnitMeta* m = meta_get(k);
+      if (named_barrier_or(kBarWork, 128, m == nullptr)) {  // one of the four gave up: all leave
+        ok = false;
+        give_up();
+        break;
       }
-      bool need = false;
+      const int n = m->n;
+      const int t = m->t, g = m->g, split = m->split, p_tok = m->p_tok;
+      const bool valid = m->valid != 0, bad = m->bad != 0;
+      const int os = k & 1;
+      // m_ref starts at a huge negative finite value rather than -inf, so that the exponent
+      // argument s * c - m_ref is +huge for any real score (the vote below takes the block's
+      // maximum then) and -inf for a masked key (P = 0), with no special case for the first block
+      constexpr float kNoRef = -1e30f;
+      float m_ref[16], l[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) need |= xs[h] > m_ref[h] + kRescaleLog2;
-      if (named_barrier_or(kBarWork, 128, need)) {  // the same answer in all four warps
-        float bm[16];
-        group_reduce16<true>(xs, bm, red + 64 * (nred & 1), wq, lane);
-        ++nred;
-        float cf[16];
-        bool moved = false;
+      for (int h = 0; h < 16; ++h) {
+        m_ref[h] = kNoRef;
+        l[h] = 0.f;
+      }
+      for (int j = 0; j < n; ++j, ++jg) {
+        const int x = jg & 1;
+        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
+        float sv[16];  // this key's raw scores, -inf when the key lies after the query position
+        if (wait_ok(&s_full[x], par)) {
+          tc_fence_after();
+          uint32_t r[16];
+          tmem_ld16(tmem + lanes + kColS + 16 * x, r);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[x]);
+          const bool kvalid = m->blk[j] * kBS + kr <= p_tok;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) sv[h] = kvalid ? __uint_as_float(r[h]) : -CUDART_INF_F;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 16; ++h) sv[h] = -CUDART_INF_F;
+        }
+        float d[16];  // exponent arguments against the current reference
+        bool need = false;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float mn = fmaxf(m_ref[h], bm[h]);
-          cf[h] = (m_ref[h] == -CUDART_INF_F) ? 0.f : fast_exp2(m_ref[h] - mn);
-          moved |= mn != m_ref[h];
-          m_ref[h] = mn;
-          l[h] *= cf[h];
+          d[h] = fmaf(sv[h], c, -m_ref[h]);
+          need |= d[h] > kRescaleLog2;
         }
-        // O^T *= cf once PV(j - 1) has landed (PV(j) waits for this block's P)
-        if (moved && j > 0 && wait_ok(&p_empty[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
-          tc_fence_after();
-          uint32_t o[16];
-          tmem_ld16(tmem + lanes + kColO, o);
+        if (named_barrier_or(kBarWork, 128, need)) {  // the same answer in all four warps
+          float cf[16];  // the block maxima, then the rescale factors
+#pragma unroll
+          for (int h = 0; h < 16; ++h) cf[h] = sv[h] * c;
+          group_reduce16<true>(cf, cf, red + 64 * (nred & 1), wq, lane);
+          ++nred;
+          bool moved = false;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float mn = fmaxf(m_ref[h], cf[h]);
+            moved |= mn != m_ref[h];
+            cf[h] = fast_exp2(m_ref[h] - mn);  // 0 when there was no reference yet
+            m_ref[h] = mn;
+            l[h] *= cf[h];
+            d[h] = fmaf(sv[h], c, -mn);
+          }
+          // both accumulators *= cf once PV(jg - 1) and PV(jg - 2) have landed (PV(jg) waits for
+          // this block's P); one not yet written in this unit is rescaled harmlessly: its first
+          // PV of the unit overwrites it
+          if (moved && j > 0 && wait_ok(&p_empty[(jg - 1) & 1], static_cast<uint32_t>((jg - 1) >> 1) & 1u) &&
+              (j < 2 || wait_ok(&p_empty[jg & 1], (static_cast<uint32_t>(jg >> 1) & 1u) ^ 1u))) {
+            tc_fence_after();
+#pragma unroll
+            for (int xx = 0; xx < 2; ++xx) {
+              uint32_t o[16];
+              tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * xx, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * cf[h]);
+              tmem_st16(tmem + lanes + kColO + 32 * os + 16 * xx, o);
+              tmem_wait_st();
+            }
+            tc_fence_before();
+          }
+        }
+        // P = exp2(s c - m) -> P^T tile x (free once PV(jg - 2) has landed): row h, key kr
+        if (wait_ok(&p_empty[x], par ^ 1u)) {
+          uint8_t* pt = smem + S::kOffP + static_cast<size_t>(x) * kPTile + (kr >> 6) * 2048 + (kr & 7) * 2;
+          const int ch = (kr & 63) >> 3;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float pv = fast_exp2(d[h]);
+            l[h] += pv;
+            *reinterpret_cast<__half*>(pt + (h >> 3) * 1024 + (h & 7) * 128 + ((ch ^ (h & 7)) << 4)) =
+                __float2half_rn(pv);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[x]);
+        }
+      }
+      // ---- the unit's output: lane kr = dim kr of O^T; l summed over the 128 keys' threads --
+      float lt[16];
+      group_reduce16<false>(l, lt, red + 64 * (nred & 1), wq, lane);
+      ++nred;
+      uint32_t o[16];
+      const bool have = n > 0 && wait_ok(&o_final[os], static_cast<uint32_t>(k >> 1) & 1u);
+      if (have) {  // the accumulator of the unit's first block, plus the other one if it was used
+        const int x0 = (jg - n) & 1;
+        tc_fence_after();
+        tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * x0, o);
+        tmem_wait_ld();
+        if (n > 1) {
+          uint32_t o2[16];
+          tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * (x0 ^ 1), o2);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * cf[h]);
-          tmem_st16(tmem + lanes + kColO, o);
-          tmem_wait_st();
-          tc_fence_before();
+          for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) + __uint_as_float(o2[h]));
         }
+        tc_fence_before();
       }
-      // P = exp2(x - m) -> P^T tile x (free once PV(j - 2) has landed): row h, key kr
-      if (wait_ok(&p_empty[x], par ^ 1u)) {
-        uint8_t* pt = smem + S::kOffP + static_cast<size_t>(x) * kPTile + (kr >> 6) * 2048 + (kr & 7) * 2;
-        const int ch = (kr & 63) >> 3;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[os]);  // O^T[os] may be overwritten
+      if (valid) {
+        const bool zero = !have || bad || *abort_flag != 0;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float mu = m_ref[h] == -CUDART_INF_F ? 0.f : m_ref[h];
-          const float pv = fast_exp2(xs[h] - mu);
-          l[h] += pv;
-          *reinterpret_cast<__half*>(pt + (h >> 3) * 1024 + (h & 7) * 128 + ((ch ^ (h & 7)) << 4)) = __float2half_rn(pv);
+          const bool z = zero || !(lt[h] > 0.f);
+          const float val = z ? 0.f : __uint_as_float(o[h]) / lt[h];
+          const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
+          if (p.splits == 1) {
+            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * kD + kr] = __float2bfloat16_rn(val);
+          } else {
+            const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
+            p.part_o[prow * kD + kr] = val;
+            if (kr == 0) p.part_lse[prow] = z ? -CUDART_INF_F : m_ref[h] + __log2f(lt[h]);
+          }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[x]);
       }
-    }
-    // ---- output: lane kr = dim kr of O^T; l summed over the 128 keys' threads --------------
-    float lt[16];
-    group_reduce16<false>(l, lt, red + 64 * (nred & 1), wq, lane);
-    uint32_t o[16];
-    const bool have = n > 0 && ok && mbar_wait(o_final, 0u, abort_flag);
-    if (have) {
-      tc_fence_after();
-      tmem_ld16(tmem + lanes + kColO, o);
-      tmem_wait_ld();
-    }
-    const bool zero = !have || is_bad || *abort_flag != 0;
-#pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      const bool z = zero || !(lt[h] > 0.f);
-      const float val = z ? 0.f : __uint_as_float(o[h]) / lt[h];
-      const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
-      if (p.splits == 1) {
-        reinterpret_cast<__nv_bfloat16*>(p.out)[orow * kD + kr] = __float2bfloat16_rn(val);
-      } else {
-        const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
-        p.part_o[prow * kD + kr] = val;
-        if (kr == 0) p.part_lse[prow] = z ? -CUDART_INF_F : m_ref[h] + __log2f(lt[h]);
-      }
+      meta_put(k);
     }
   }
   tc_fence_before();
@@ -1344,20 +1101,11 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float* __restrict__ pa
 }
 
 // The two kernels trade latency for throughput: k_attn spreads one (token, group) over a whole
-// SM (the keys of each block over four warps, the dequant over eight), so a batch of few tokens
-// finishes in one short wave; tok::k_attn_tok packs a (token, group) into 8 warps that each own
-// whole blocks, which uses the SM better once there are several waves of CTAs. Measured on
-// GB300: T = 8 and 32 tokens run 1.4-1.9x faster on k_attn, T = 512 1.2x faster on k_attn_tok.
-bool use_tok_kernel(int T) { return 4 * T > 2 * 152; }
-
-// Splits of each (query token, group)'s blocks for the per-token kernel, from T alone: enough
-// CTAs for about two per SM of a 152-SM GB300, at most 16 (one block per split).
-int tok_splits(int T) {
-  const int items = 4 * T;
-  if (items <= 0 || items >= 304) return 1;
-  const int s = (304 + items - 1) / items;
-  return s > 16 ? 16 : s;
-}
+// SM (the keys of each block over four mma.sync warps, the dequant over eight), so a batch of
+// few tokens finishes in one short wave; tc::k_attn_tc runs one persistent CTA per SM over all
+// the (token, group) units with the contractions on tcgen05, which keeps the SM busier once
+// there are several waves of units. The many-token kernel takes more than two units per SM.
+bool use_tc_kernel(int T) { return 4 * T > 2 * 152; }
 
 size_t attn_ws_bytes(int T, int splits) {
   if (splits <= 1) return 0;
@@ -1387,7 +1135,7 @@ msa_status attn_setup(const msa_geometry* geo, const msa_batch* batch, const msa
   p->max_q_len = batch->max_q_len;
   p->num_pages = cache->num_pages;
   p->splits = num_splits > 0 ? num_splits
-                             : (use_tok_kernel(batch->T) ? tok_splits(batch->T) : msa_host::auto_splits(batch->T));
+                             : (use_tc_kernel(batch->T) ? 1 : msa_host::auto_splits(batch->T));
   p->qsl = batch->query_start_loc;
   p->seq_lens = batch->seq_lens;
   p->block_table = batch->block_table;
@@ -1411,7 +1159,7 @@ void attn_bind_ws(AttnParams* p, void* ws) {
 }
 
 msa_status attn_launch(const AttnParams& p, const uint8_t* kv_pages, cudaStream_t stream) {
-  if (use_tok_kernel(p.T)) {
+  if (use_tc_kernel(p.T)) {
     alignas(64) CUtensorMap kv_map, q_map;
     if (!msa_host::kv_tensor_map(&kv_map, kv_pages, static_cast<uint64_t>(p.num_pages > 0 ? p.num_pages : 1)) ||
         !msa_host::rows128_tensor_map(&q_map, p.q, static_cast<uint64_t>(p.T) * kQHeads, kHPG))
@@ -1419,17 +1167,10 @@ msa_status attn_launch(const AttnParams& p, const uint8_t* kv_pages, cudaStream_
     if (cudaFuncSetAttribute(tc::k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tc::Smem::kBytes)) != cudaSuccess)
       return MSA_ERR_CUDA;
-    tc::k_attn_tc<<<p.T * 4 * p.splits, tc::kThreads, tc::Smem::kBytes, stream>>>(p, kv_map, q_map);
-    msa_status st = msa_host::launch_status();
-    if (st != MSA_OK) return st;
-    if (p.splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, p.splits, p.T, p.out, stream);
-    return MSA_OK;
-  }
-  if (false) {
-    if (cudaFuncSetAttribute(tok::k_attn_tok, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(tok::TokSmem::kBytes)) != cudaSuccess)
-      return MSA_ERR_CUDA;
-    tok::k_attn_tok<<<p.T * 4 * p.splits, tok::kAttnThreads, tok::TokSmem::kBytes, stream>>>(p);
+    const int sms = msa_host::num_sms();
+    if (sms <= 0) return MSA_ERR_CUDA;
+    const int units = p.T * 4 * p.splits;
+    tc::k_attn_tc<<<units < sms ? units : sms, tc::kThreads, tc::Smem::kBytes, stream>>>(p, kv_map, q_map);
     msa_status st = msa_host::launch_status();
     if (st != MSA_OK) return st;
     if (p.splits > 1) return msa_launch_attn_merge(p.part_o, p.part_lse, p.splits, p.T, p.out, stream);
@@ -1457,7 +1198,7 @@ using namespace msa_host;
 extern "C" size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, int32_t num_splits) {
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || num_splits < 0 || num_splits > kMaxSplits) return 0;
   // room for either kernel's automatic choice (the batch's max_q_len picks the kernel)
-  const int s = num_splits > 0 ? num_splits : (use_tok_kernel(T) ? tok_splits(T) : auto_splits(T));
+  const int s = num_splits > 0 ? num_splits : (use_tc_kernel(T) ? 1 : auto_splits(T));
   return attn_ws_bytes(T, s);
 }
 

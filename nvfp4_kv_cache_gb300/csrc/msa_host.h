@@ -66,11 +66,11 @@ inline int auto_splits(int T) {
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // A 2-D tensor map (CUtensorMap, 64-B aligned storage) over `rows` rows of 128 bytes at `base`
-// (16-B aligned), box = `box_rows` rows, 128-byte swizzle (defined in msa_indexer.cu).
+// (16-B aligned), box = `box_rows` rows, 128-byte swizzle (defined in msa_api.cu).
 bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32_t box_rows);
 
 // A 3-D tensor map over a KV page pool: (128 B, 576 rows, num_pages pages), box = the 144 rows
-// of one head's K and V regions of one page, 128-byte swizzle (defined in msa_indexer.cu).
+// of one head's K and V regions of one page, 128-byte swizzle (defined in msa_api.cu).
 bool kv_tensor_map(void* tmap64, const uint8_t* base, uint64_t num_pages);
 
 }  // namespace msa_host

@@ -37,8 +37,6 @@
 #include <math_constants.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "msa.h"
 #include "msa_device.cuh"
 #include "msa_host.h"
@@ -557,53 +555,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
     tmem_dealloc(tmem, kTmemCols);
   }
 }
-
-// cuTensorMapEncodeTiled, fetched from the driver once per process.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-}  // namespace
-}  // namespace msa
-
-namespace msa_host {
-bool rows128_tensor_map(void* tmap64, const uint8_t* base, uint64_t rows, uint32_t box_rows) {
-  const PFN_cuTensorMapEncodeTiled_v12000 enc = msa::tensor_map_encoder();
-  if (enc == nullptr || rows == 0 || rows > (1ull << 32) || box_rows == 0 || box_rows > 256) return false;
-  const cuuint64_t dims[2] = {128, rows};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(static_cast<CUtensorMap*>(tmap64), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool kv_tensor_map(void* tmap64, const uint8_t* base, uint64_t num_pages) {
-  const PFN_cuTensorMapEncodeTiled_v12000 enc = msa::tensor_map_encoder();
-  if (enc == nullptr || num_pages == 0 || num_pages > (1ull << 31)) return false;
-  constexpr uint64_t kRowsPerPage = msa::kKvPage / 128;  // 576
-  const cuuint64_t dims[3] = {128, kRowsPerPage, num_pages};
-  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(msa::kKvPage)};
-  const cuuint32_t box[3] = {128, 2 * msa::kRegion / 128, 1};  // the K and V regions of one head
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(static_cast<CUtensorMap*>(tmap64), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-}  // namespace msa_host
-
-namespace msa {
-namespace {
 
 template <int DT>
 msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t stream) {

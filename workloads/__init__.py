@@ -231,6 +231,11 @@ def spec() -> Workload:
     return make("spec-decode B=64 L=131072 q_len=8 hot=24", [131072] * 64, [8] * 64, seed=2, hot=24)
 
 
+def spec_16k() -> Workload:
+    """The spec-decode structure at 16K context (a profiling size: ~0.7 GB resident)."""
+    return make("spec-decode B=64 L=16384 q_len=8 hot=24", [16384] * 64, [8] * 64, seed=2, hot=24)
+
+
 def long_context() -> Workload:
     return make("long B=8 L=524288 q_len=1 outliers=1%", [524288] * 8, [1] * 8, seed=3, outlier_frac=0.01)
 
@@ -248,7 +253,8 @@ def ragged() -> Workload:
                 layer_seeds=[4000, 4001, 4002, 4003], prefix_len=prefix, prefix_seqs=nshare)
 
 
-CONFIGS = {"tiny": tiny, "decode": decode, "spec": spec, "long": long_context, "ragged": ragged}
+CONFIGS = {"tiny": tiny, "decode": decode, "spec": spec, "spec_16k": spec_16k, "long": long_context,
+           "ragged": ragged}
 
 
 def small(name: str, seq_lens, q_lens, seed: int, **kw) -> Workload:

@@ -38,6 +38,7 @@ K_SEL = 16
 
 INDEX_NVFP4 = 0
 INDEX_FP8 = 1
+INDEX_NVFP4_EXACT = 2  # the exact-score reading of an NVFP4 index cache (no E4M3 re-rounding)
 
 # Byte layout of one cache page (this library's choice; the pages fix none).
 ROW_CODE_BYTES = HEAD_DIM // 2          # 64 B of E2M1 codes per 128-element row
@@ -198,7 +199,7 @@ def indexer_seq(L: int, q_len: int, iq, index_dtype: int, ik_vals, ik_scales=Non
     nb = (L + BLOCK - 1) // BLOCK
     iq = _c(iq, np.uint8).reshape(q_len, GROUPS, HEAD_DIM)
     ik_vals = _c(ik_vals, np.uint8)
-    if index_dtype == INDEX_NVFP4:
+    if index_dtype in (INDEX_NVFP4, INDEX_NVFP4_EXACT):
         ik_scales = _c(ik_scales, np.uint8)
         assert ik_vals.shape == (L, ROW_CODE_BYTES) and ik_scales.shape == (L, ROW_SCALE_BYTES)
     else:

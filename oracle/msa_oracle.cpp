@@ -183,6 +183,16 @@ uint8_t dequant_fp8(uint8_t code, uint8_t scale) {
   return uint8_t(m | (sgn << 7));
 }
 
+// v = E2M1(c) * E4M3(s) exactly, no re-rounding: the exact-score reading of an NVFP4 index key
+// ("vLLM ofrece soporte en día 0 para MiniMax-M3.1-Flash", "NVIDIA Rubin MSA optimizado": the
+// index key goes from NVFP4 straight to FP16, so the scores carry no E4M3 re-rounding). The
+// product has at most 2 + 4 significant bits and is exact in double. A NaN scale gives NaN.
+double dequant_exact(uint8_t code, uint8_t scale) {
+  const double S = e4m3_decode(scale);
+  if (std::isnan(S)) return std::numeric_limits<double>::quiet_NaN();
+  return e2m1_decode(code) * S;
+}
+
 // Decode one NVFP4 row of kHeadDim elements to the FP8 values the MMA would see.
 void dequant_row_values(const uint8_t* vals, const uint8_t* scales, double* out) {
   uint8_t codes[kHeadDim];
@@ -258,18 +268,25 @@ void orc_dequant_nvfp4(const uint8_t* vals, const uint8_t* scales, int64_t rows,
 //   q_len    query tokens; token t sits at position p_t = L - q_len + t
 //   iq       [q_len][4][128] E4M3 index queries
 //   ik_vals  NVFP4: [L][64] code bytes, ik_scales [L][8];  FP8 (index_dtype 1): [L][128]
+//   index_dtype 0: NVFP4 keys re-rounded to E4M3 (the FP8 score MMA); 1: FP8 keys; 2: NVFP4
+//            keys taken exactly (dequant_exact, the exact-score variant)
 //   out      [q_len][4][out_stride] block scores, fp64; blocks without a valid key get -inf
 void orc_indexer_seq(int32_t L, int32_t q_len, int32_t index_dtype, const uint8_t* iq,
                      const uint8_t* ik_vals, const uint8_t* ik_scales, double* out,
                      int32_t out_stride, int32_t nthreads) {
   const int nb = (L + kBlock - 1) / kBlock;
   // Exact FP8 values of every index key (FP8 values are exact in float).
-  std::vector<float> key(size_t(L) * kHeadDim);
+  std::vector<float> key(size_t(L) * kHeadDim);  // (exact NVFP4 products are exact in float too)
   parallel_for(L, nthreads, [&](int64_t j) {
     if (index_dtype == 0) {
       double row[kHeadDim];
       dequant_row_values(ik_vals + j * (kHeadDim / 2), ik_scales + j * (kHeadDim / 16), row);
       for (int d = 0; d < kHeadDim; ++d) key[size_t(j) * kHeadDim + d] = float(row[d]);
+    } else if (index_dtype == 2) {
+      uint8_t codes[kHeadDim];
+      unpack_row(ik_vals + j * (kHeadDim / 2), kHeadDim, codes);
+      const uint8_t* sc = ik_scales + j * (kHeadDim / 16);
+      for (int d = 0; d < kHeadDim; ++d) key[size_t(j) * kHeadDim + d] = float(dequant_exact(codes[d], sc[d / 16]));
     } else {
       for (int d = 0; d < kHeadDim; ++d) key[size_t(j) * kHeadDim + d] = float(e4m3_decode(ik_vals[j * kHeadDim + d]));
     }

@@ -68,6 +68,11 @@ class OracleSeq:
     def scores(self):
         return oracle.indexer_seq(self.L, self.q_len, self.iq8, self.index_dtype, self.ik[0], self.ik[1])
 
+    def scores_exact(self):
+        """Block scores with the NVFP4 index keys taken exactly (no E4M3 re-rounding)."""
+        assert self.index_dtype == oracle.INDEX_NVFP4
+        return oracle.indexer_seq(self.L, self.q_len, self.iq8, oracle.INDEX_NVFP4_EXACT, self.ik[0], self.ik[1])
+
     def attention(self, sel, scale):
         return oracle.attention_seq(self.L, self.q_len, self.q8, *self.kv, sel, scale)
 

@@ -273,6 +273,20 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     assert msa.status_bits(status) == 0
     sel = o2["sel"].cpu().numpy()
 
+    # ---- the exact-score indexer variant (NVFP4 keys scored exactly), timed alone the same way
+    exact_ms = None
+    if w.layers[0].index_dtype == W.INDEX_NVFP4:
+        ex = torch.empty_like(o2["scores"])
+        ex_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ex_ev[i][0].record(stream)
+            msa.msa_indexer_decode_exact(dl.batch, dl.cache, dl.iq8, ex, status)
+            ex_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        exact_ms = statistics.mean(a.elapsed_time(b) for a, b in ex_ev)
+        assert msa.status_bits(status) == 0
+
     # ---- end to end through host buffers: pinned H2D of the step's inputs, D2H of the output
     q_h = dl.q8.cpu().pin_memory()
     iq_h = dl.iq8.cpu().pin_memory()
@@ -323,6 +337,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
         "achieved_tbps": total_bytes / (ms_max * 1e-3) / 1e12,
         "step_bytes": total_bytes, "step_frac_of_hbm_peak": total_bytes / (ms_max * 1e-3) / 1e9 / peak_gbs,
         "stages_us": {"indexer": stage_ms[0] * 1e3, "topk": stage_ms[1] * 1e3, "attention": stage_ms[2] * 1e3},
+        "indexer_exact_us": None if exact_ms is None else exact_ms * 1e3,
         "roofline": {"kernel": "k_indexer (msa_indexer_decode)", "bound": "hbm", "achieved": idx_gbs,
                      "peak": peak_gbs, "unit": "GB/s", "frac": idx_gbs / peak_gbs,
                      "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes": idx_bytes,

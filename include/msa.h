@@ -194,6 +194,17 @@ msa_status msa_indexer_decode_range(const msa_geometry* geo, const msa_batch* ba
                                     int32_t block_begin, int32_t block_end,
                                     float* block_scores, uint32_t* status, cudaStream_t stream);
 
+/* Exact-score variant of msa_indexer_decode ("vLLM ofrece soporte en día 0 para
+ * MiniMax-M3.1-Flash", "NVIDIA Rubin MSA optimizado": NVFP4 index keys converted straight to
+ * FP16 and scored with an FP16 MMA, so the scores carry no E4M3 re-rounding). Same arguments,
+ * layouts and results as msa_indexer_decode except that an NVFP4 index key element is taken
+ * as E2M1(code) x E4M3(scale) exactly (f16 holds it exactly), the index query widened exactly
+ * from E4M3 to f16, products accumulated in fp32. An FP8 index cache is scored exactly as
+ * msa_indexer_decode scores it (its keys are never re-rounded). Errors as msa_indexer_decode. */
+msa_status msa_indexer_decode_exact(const msa_geometry* geo, const msa_batch* batch,
+                                    const msa_cache* cache, const uint8_t* index_q,
+                                    float* block_scores, uint32_t* status, cudaStream_t stream);
+
 /* Per-group block selection ("MSA primer"; "MSA 机制详解"). For token t at position p_t,
  * local = p_t / 128. sel[t][g][0] = local; sel[t][g][1..15] = the 15 highest-scoring blocks
  * among 0 .. local-1, in descending score order, equal scores ordered by lower block id

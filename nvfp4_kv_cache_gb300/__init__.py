@@ -76,6 +76,7 @@ _SIGS = {
     "msa_indexer_decode": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
     "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
     "msa_indexer_decode_range": (_I32, [_GP, _BP, _CP, _P, _I32, _I32, _P, _P, _P]),
+    "msa_indexer_decode_exact": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
     "msa_topk_candidates": (_I32, [_GP, _BP, _P, _I32, _I32, _P, _P, _P]),
     "msa_topk_merge": (_I32, [_GP, _BP, _P, _I32, _P, _P, _P]),
     "msa_topk_candidates_host": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P]),
@@ -214,6 +215,14 @@ def msa_indexer_decode_range(batch: Batch, cache: Cache, index_q: torch.Tensor, 
     _check(_lib.msa_indexer_decode_range(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
                                          _ptr(index_q), int(block_begin), int(block_end), _ptr(block_scores),
                                          _ptr(status), _stream()), "msa_indexer_decode_range")
+
+
+def msa_indexer_decode_exact(batch: Batch, cache: Cache, index_q: torch.Tensor, block_scores: torch.Tensor,
+                             status: Optional[torch.Tensor] = None) -> None:
+    """The exact-score indexer: NVFP4 index keys as E2M1 x E4M3 exactly (f16 score MMA)."""
+    _check(_lib.msa_indexer_decode_exact(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                         _ptr(index_q), _ptr(block_scores), _ptr(status), _stream()),
+           "msa_indexer_decode_exact")
 
 
 def msa_topk_candidates(batch: Batch, block_scores: torch.Tensor, block_begin: int, block_end: int,

@@ -7,6 +7,7 @@
 // read with one byte-permute per four elements and a masked xor for the signs.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -314,6 +315,45 @@ __device__ __forceinline__ void build_dequant_lut(uint2* lut, int tid, int nthre
   }
 }
 
+// Fill the 256-entry exact f16 table: for scale byte s, the f16 values of E2M1(m) * E4M3(s)
+// for magnitudes m = 0..7 (exact: at most 6 significant bits, inside the f16 range), the sign
+// of s applied, a NaN scale giving NaN; stored as byte planes, low bytes of the eight values
+// in .x/.y and high bytes in .z/.w, for byte-permute lookups. 4 KB.
+__device__ __forceinline__ void build_exact_lut(uint4* lut, int tid, int nthreads) {
+  for (int s = tid; s < 256; s += nthreads) {
+    const uint32_t mag = static_cast<uint32_t>(s) & 0x7Fu;
+    uint16_t h[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (mag == 0x7Fu) {
+        h[m] = 0x7E00u;
+      } else {
+        const __half v = __float2half_rn(e2m1_mag(m) * e4m3_to_f32(mag));
+        h[m] = static_cast<uint16_t>(__half_as_ushort(v) | ((s & 0x80) ? 0x8000u : 0u));
+      }
+    }
+    uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      lo[m >> 2] |= static_cast<uint32_t>(h[m] & 0xFFu) << (8 * (m & 3));
+      hi[m >> 2] |= static_cast<uint32_t>(h[m] >> 8) << (8 * (m & 3));
+    }
+    lut[s] = make_uint4(lo[0], lo[1], hi[0], hi[1]);
+  }
+}
+
+// One code word (8 elements) to four f16x2 words with the exact table entry of its scale:
+// o[i] = elements 2i, 2i + 1. The element signs flip the high bytes' top bits.
+__device__ __forceinline__ void dq8_f16(uint32_t w, uint4 t, uint32_t (&o)[4]) {
+  const uint32_t x = w & 0x77777777u;
+  const uint32_t l03 = prmt(t.x, t.y, x), h03 = prmt(t.z, t.w, x) ^ (w & 0x80808080u);
+  const uint32_t l47 = prmt(t.x, t.y, x >> 16), h47 = prmt(t.z, t.w, x >> 16) ^ ((w << 4) & 0x80808080u);
+  o[0] = prmt(l03, h03, 0x5140u);
+  o[1] = prmt(l03, h03, 0x7362u);
+  o[2] = prmt(l47, h47, 0x5140u);
+  o[3] = prmt(l47, h47, 0x7362u);
+}
+
 // Dequantise one code word (8 elements, this library's layout) with the table entry of
 // its scale: lo = E4M3 bytes of elements 0..3, hi = elements 4..7, in element order.
 __device__ __forceinline__ void dq8(uint32_t w, uint2 e, uint32_t& lo, uint32_t& hi) {
@@ -417,6 +457,12 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: F16 x F16 -> F32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: F16 x F16 -> F32, A MN-major, B K-major.

@@ -50,19 +50,43 @@ constexpr int kMmaWarps = 3;                     // MMA-issuing warps (pages in 
 constexpr int kWarpDq = 1 + kMmaWarps;           // first dequant warp
 constexpr int kWarpEp = kWarpDq + 4 * kDqGroups; // first max-pool warp
 constexpr int kIdxThreads = 32 * (kWarpEp + 4 * kEpGroups);
-constexpr int kATiles = 6;                       // TMEM key tiles (32 columns each)
 constexpr int kDTiles = 6;                       // TMEM accumulators (32 columns each)
 constexpr int kTmemCols = 512;
-constexpr int kBTile = 32 * kD;                  // 32 query rows x 128 B
+// The exact-score variant (NVFP4 keys to f16 with no E4M3 re-rounding, f16 score MMA): an
+// internal index kind next to MSA_INDEX_NVFP4 and MSA_INDEX_FP8.
+constexpr int kIdxNvExact = 2;
 // Partial-maximum slots of the max-pool quarters: page n uses slot n % kPartSlots. A slot is
 // written again only by page n + kPartSlots, whose MMA needed its accumulator released by all
 // four quarters at page n + kPartSlots - kDTiles, which each quarter reaches after combining
 // page n (a warp takes its pages in order): 2 * kDTiles slots are enough.
 constexpr int kPartSlots = 2 * kDTiles;
-static_assert(kATiles % kDqGroups == 0 && kDTiles % kEpGroups == 0, "a ring slot serves one group");
+static_assert(kDTiles % kEpGroups == 0 && kDTiles % kMmaWarps == 0, "an accumulator serves one group");
 static_assert(kIdxThreads <= 1024, "one CTA");
-static_assert(kATiles % kMmaWarps == 0 && kDTiles % kMmaWarps == 0, "a ring slot serves one MMA warp");
-static_assert(32 * (kATiles + kDTiles) <= kTmemCols, "TMEM budget");
+
+// Key tiles and query tiles per index kind: E4M3 keys take 32 TMEM columns a tile and the
+// query tile is 32 rows x 128 E4M3; exact keys take 64 columns (f16) and the query tile is
+// 32 rows x 128 f16 (two 64-element K atoms of 4 KB).
+template <int DT>
+struct TileCfg {
+  static constexpr int kATiles = 6;        // TMEM key tiles
+  static constexpr int kACols = 32;        // TMEM columns of one key tile
+  static constexpr int kBTile = 32 * kD;   // bytes of one query tile
+  static constexpr int kLutBytes = 256 * 8;
+};
+template <>
+struct TileCfg<kIdxNvExact> {
+  static constexpr int kATiles = 3;
+  static constexpr int kACols = 64;
+  static constexpr int kBTile = 32 * kD * 2;
+  static constexpr int kLutBytes = 256 * 16;
+};
+template <int DT>
+constexpr bool tiles_ok() {
+  return TileCfg<DT>::kATiles % kDqGroups == 0 && TileCfg<DT>::kATiles % kMmaWarps == 0 &&
+         TileCfg<DT>::kACols * TileCfg<DT>::kATiles + 32 * kDTiles <= kTmemCols;
+}
+static_assert(tiles_ok<MSA_INDEX_NVFP4>() && tiles_ok<MSA_INDEX_FP8>() && tiles_ok<kIdxNvExact>(),
+              "a key tile serves one dequant group and one MMA warp; TMEM budget");
 
 // Page n of a CTA lives in stage n % kStages, key tile n % kATiles and accumulator
 // n % kDTiles; the ring sizes are multiples of the group counts, so every slot is used by one
@@ -79,6 +103,11 @@ template <>
 struct IdxCfg<MSA_INDEX_FP8> {
   static constexpr int kPage = kIdxPageFp8;
   static constexpr int kStages = 9;
+};
+template <>
+struct IdxCfg<kIdxNvExact> {
+  static constexpr int kPage = kIdxPageNv;
+  static constexpr int kStages = 18;
 };
 
 struct IdxParams {
@@ -100,6 +129,8 @@ template <int DT>
 struct IdxSmem {
   static constexpr int kStages = IdxCfg<DT>::kStages;
   static constexpr int kPage = IdxCfg<DT>::kPage;
+  static constexpr int kATiles = TileCfg<DT>::kATiles;
+  static constexpr int kBTile = TileCfg<DT>::kBTile;
   static_assert(kStages % kDqGroups == 0, "a stage serves one dequant group");
   // offsets from a 1024-byte aligned base (pages and query tiles are multiples of 1024 B)
   static constexpr size_t kOffStage = 0;
@@ -115,13 +146,15 @@ struct IdxSmem {
   static constexpr size_t kOffBTag = kOffAMeta + 8 * kATiles;                 // [kATiles][4] int
   static constexpr size_t kOffPart = kOffBTag + 16 * kATiles;                 // [kPartSlots][4][32] fp32
   static constexpr size_t kOffCnt = kOffPart + 4 * kPartSlots * 4 * 32;       // [kPartSlots] int
-  static constexpr size_t kOffLut = kOffCnt + 4 * kPartSlots;
-  static constexpr size_t kOffMisc = kOffLut + 256 * 8;
+  static constexpr size_t kOffLut = (kOffCnt + 4 * kPartSlots + 15) & ~static_cast<size_t>(15);  // 16-B entries
+  static constexpr size_t kOffMisc = kOffLut + TileCfg<DT>::kLutBytes;
   static constexpr size_t kOffPtab = kOffMisc + 64;  // 32 x int4
   static constexpr size_t kOffWarpSum = kOffPtab + 32 * 16;
   static constexpr size_t kOffPrefix = kOffWarpSum + 4 * 32;
   static size_t bytes(int B) { return 1024 + kOffPrefix + 4 * static_cast<size_t>(B + 1); }
 };
+static_assert(IdxSmem<kIdxNvExact>::kOffLut % 16 == 0 && IdxSmem<kIdxNvExact>::kOffB % 1024 == 0,
+              "the exact table's 16-B entries and the query atoms are aligned");
 
 // Pages of sequence b that the indexer scans (0 for padded or invalid rows).
 __device__ __forceinline__ int seq_pages(const IdxParams& p, int b, bool* bad) {
@@ -162,6 +195,33 @@ __device__ __forceinline__ void dequant_row_nvfp4(const uint8_t* pg, int r, cons
   }
 }
 
+// Dims 64 h .. 64 h + 63 of key row r of a staged NVFP4 page as exact f16 (table entries of
+// build_exact_lut): w[c] holds elements 64 h + 2c, +1, the TMEM A-operand layout of half a row.
+__device__ __forceinline__ void dequant_half_exact(const uint8_t* pg, int r, int h, const uint4* lut,
+                                                   uint32_t (&w)[32]) {
+  const uint2 sc2 = lds64(pg + sw128_phys(static_cast<uint32_t>(kScaleOff + r * kRowScales)));
+  const uint32_t sh = h ? sc2.y : sc2.x;  // the four scales of dims 64 h .. 64 h + 63
+#pragma unroll
+  for (int qq = 0; qq < 2; ++qq) {  // 32 elements: 64 h + 32 qq .. +31, scales 2 qq and 2 qq + 1 of sh
+    const uint4 c = lds128(pg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * (2 * h + qq))));
+    const uint32_t s2 = sh >> (16 * qq);
+    const uint4 t0 = lut[s2 & 0xFFu], t1 = lut[(s2 >> 8) & 0xFFu];
+    uint32_t o[4];
+    dq8_f16(c.x, t0, o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[16 * qq + e] = o[e];
+    dq8_f16(c.y, t0, o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[16 * qq + 4 + e] = o[e];
+    dq8_f16(c.z, t1, o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[16 * qq + 8 + e] = o[e];
+    dq8_f16(c.w, t1, o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[16 * qq + 12 + e] = o[e];
+  }
+}
+
 // One step of a shuffle transpose-reduce: lanes l and l ^ k (k = lane bit) each keep half of
 // their values, the lower-bit lane the first half, and take the max with the partner's copy.
 template <int N>
@@ -184,7 +244,9 @@ template <int DT>
 __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, const __grid_constant__ CUtensorMap tmap) {
   using S = IdxSmem<DT>;
   constexpr int kStages = S::kStages;
-  constexpr bool kNv = DT == MSA_INDEX_NVFP4;
+  constexpr int kATiles = TileCfg<DT>::kATiles, kACols = TileCfg<DT>::kACols, kBTile = TileCfg<DT>::kBTile;
+  constexpr bool kExact = DT == kIdxNvExact;
+  constexpr bool kNv = DT == MSA_INDEX_NVFP4 || kExact;  // NVFP4 pages, dequantised into TMEM
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem + S::kOffStage;
@@ -199,6 +261,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
   int2* ameta = reinterpret_cast<int2*>(smem + S::kOffAMeta);
   int* btag = reinterpret_cast<int*>(smem + S::kOffBTag);
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
+  uint4* lut16 = reinterpret_cast<uint4*>(smem + S::kOffLut);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
   int* bad_batch = reinterpret_cast<int*>(smem + S::kOffMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 8);
@@ -229,7 +292,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
   if (tid < 4 * kATiles) btag[tid] = -1;
   if (tid < kPartSlots) reinterpret_cast<int*>(smem + S::kOffCnt)[tid] = 0;
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-  if constexpr (kNv) build_dequant_lut(lut, tid, kIdxThreads);
+  if constexpr (kExact)
+    build_exact_lut(lut16, tid, kIdxThreads);
+  else if constexpr (kNv)
+    build_dequant_lut(lut, tid, kIdxThreads);
   __syncthreads();  // flags initialised before anyone raises them
   {
     // prefix[b] = pages of sequences 0 .. b-1: per-thread counts, warp scans, one scan of
@@ -276,8 +342,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_a = tmem;                    // key tiles: columns 32a .. 32a+31
-  const uint32_t t_d = tmem + 32 * kATiles;     // accumulators
+  const uint32_t t_a = tmem;                    // key tiles: columns kACols a .. kACols (a + 1) - 1
+  const uint32_t t_d = tmem + kACols * kATiles; // accumulators
   if (blockIdx.x == 0 && tid == 0 && *bad_batch) set_status(p.status, MSA_ERR_INVALID_ARG);
 
   const int total = prefix[p.B];
@@ -345,7 +411,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
   } else if (warp < kWarpDq) {
     // ---- MMA issue: pages mw, mw + kMmaWarps, ...; the whole warp runs the loop (its
     // indices stay warp-uniform), lane 0 issues -------------------------------------------------
-    constexpr uint32_t idesc = idesc_e4m3_f32(128, 32);  // rows >= 4 q_len of a query tile are zero
+    // rows >= 4 q_len of a query tile are zero
+    constexpr uint32_t idesc = kExact ? idesc_f16_f32(128, 32) : idesc_e4m3_f32(128, 32);
     const int mw = warp - 1;
     uint64_t* fin = mma_fin + mw;
     int issued = 0;
@@ -365,14 +432,21 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         if (valid) {
           const uint32_t b_addr = smem_u32(smem + S::kOffB) + static_cast<uint32_t>(a * kBTile);
           const uint32_t st_addr = smem_u32(stages) + static_cast<uint32_t>((n % kStages) * S::kPage);
+          if constexpr (kExact) {
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            if constexpr (kNv)
-              tc_mma_f8_ta(t_d + 32 * d, t_a + 32 * a + 8 * s, sw128_kmajor_desc(b_addr + 32 * s), idesc,
-                           s > 0 ? 1u : 0u);
-            else
-              tc_mma_f8(t_d + 32 * d, sw128_kmajor_desc(st_addr + 32 * s), sw128_kmajor_desc(b_addr + 32 * s), idesc,
-                        s > 0 ? 1u : 0u);
+            for (int s = 0; s < 8; ++s)  // K = 16 f16 per MMA: 8 TMEM columns; 32 B of the query atom
+              tc_mma_f16_ta(t_d + 32 * d, t_a + kACols * a + 8 * s,
+                            sw128_kmajor_desc(b_addr + (s >> 2) * 4096 + 32 * (s & 3)), idesc, s > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              if constexpr (kNv)
+                tc_mma_f8_ta(t_d + 32 * d, t_a + kACols * a + 8 * s, sw128_kmajor_desc(b_addr + 32 * s), idesc,
+                             s > 0 ? 1u : 0u);
+              else
+                tc_mma_f8(t_d + 32 * d, sw128_kmajor_desc(st_addr + 32 * s), sw128_kmajor_desc(b_addr + 32 * s),
+                          idesc, s > 0 ? 1u : 0u);
+            }
           }
           tc_commit(&d_full[d]);  // also tells the max-pool group the key tile (and FP8 stage) is free
         } else {
@@ -399,7 +473,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       if (!warp_wait(&full[s], static_cast<uint32_t>(n / kStages) & 1u, abort_flag)) break;
       const SlotInfo si = info[s];
       uint32_t w[32];
-      if constexpr (kNv) {
+      if constexpr (kNv && !kExact) {
         if (si.valid) dequant_row_nvfp4(stages + static_cast<size_t>(s) * S::kPage, i, lut, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the warp's reads of the stage are done
@@ -415,21 +489,46 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       if (*tag != cur_b) {
         // this warp's 8 rows of the slot's query tile: rows c < 4 * q_len, zero rows up to 32
         uint8_t* btile = smem + S::kOffB + static_cast<size_t>(a) * kBTile;
+        if constexpr (kExact) {
+          // f16 rows (E4M3 -> f16 is exact), two K atoms of 64 dims: 512 chunks of 8 dims
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int id = 64 * wq + 2 * lane + u;  // 256 chunks of 16 B
-          const int row = id >> 3, c = id & 7;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (row < ncol)
-            v = *reinterpret_cast<const uint4*>(p.index_q + static_cast<int64_t>(q0 * 4 + row) * kD + 16 * c);
-          *reinterpret_cast<uint4*>(btile + sw128_chunk_off(row, c)) = v;
+          for (int u = 0; u < 4; ++u) {
+            const int id = 128 * wq + 4 * lane + u;
+            const int row = id >> 4, cc = id & 15;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < ncol) {
+              const uint2 e = *reinterpret_cast<const uint2*>(p.index_q + static_cast<int64_t>(q0 * 4 + row) * kD + 8 * cc);
+              v = make_uint4(cvt_f16x2_e4m3x2(e.x), cvt_f16x2_e4m3x2(e.x >> 16), cvt_f16x2_e4m3x2(e.y),
+                             cvt_f16x2_e4m3x2(e.y >> 16));
+            }
+            *reinterpret_cast<uint4*>(btile + (cc >> 3) * 4096 + sw128_chunk_off(row, cc & 7)) = v;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int id = 64 * wq + 2 * lane + u;  // 256 chunks of 16 B
+            const int row = id >> 3, c = id & 7;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < ncol)
+              v = *reinterpret_cast<const uint4*>(p.index_q + static_cast<int64_t>(q0 * 4 + row) * kD + 16 * c);
+            *reinterpret_cast<uint4*>(btile + sw128_chunk_off(row, c)) = v;
+          }
         }
         fence_proxy_async_smem();  // visible to the tensor core
         __syncwarp();
         if (lane == 0) *tag = cur_b;
       }
-      if constexpr (kNv) {
-        if (si.valid) tmem_st32(t_a + 32 * a + lane_base, w);
+      if constexpr (kExact) {  // two halves of the f16 row, then the stage is free
+        const uint8_t* pg = stages + static_cast<size_t>(s) * S::kPage;
+        if (si.valid) dequant_half_exact(pg, i, 0, lut16, w);
+        if (si.valid) tmem_st32(t_a + kACols * a + lane_base, w);
+        if (si.valid) dequant_half_exact(pg, i, 1, lut16, w);
+        if (si.valid) tmem_st32(t_a + kACols * a + 32 + lane_base, w);
+        tmem_wait_st();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      } else if constexpr (kNv) {
+        if (si.valid) tmem_st32(t_a + kACols * a + lane_base, w);
         tmem_wait_st();
       }
       tc_fence_before();
@@ -580,9 +679,10 @@ msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t
 using namespace msa;
 using namespace msa_host;
 
-extern "C" msa_status msa_indexer_decode_range(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
-                                               const uint8_t* index_q, int32_t block_begin, int32_t block_end,
-                                               float* block_scores, uint32_t* status, cudaStream_t stream) {
+namespace {
+msa_status indexer_entry(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                         const uint8_t* index_q, int32_t block_begin, int32_t block_end, float* block_scores,
+                         uint32_t* status, bool exact, cudaStream_t stream) {
   msa_status st = check_geometry(geo);
   if (st != MSA_OK) return st;
   if ((st = check_batch(batch)) != MSA_OK) return st;
@@ -606,8 +706,23 @@ extern "C" msa_status msa_indexer_decode_range(const msa_geometry* geo, const ms
   p.index_q = index_q;
   p.block_scores = block_scores;
   p.status = status;
-  if (cache->index_dtype == MSA_INDEX_NVFP4) return launch_indexer<MSA_INDEX_NVFP4>(p, cache->index_pages, stream);
-  return launch_indexer<MSA_INDEX_FP8>(p, cache->index_pages, stream);
+  if (cache->index_dtype == MSA_INDEX_NVFP4)
+    return exact ? launch_indexer<kIdxNvExact>(p, cache->index_pages, stream)
+                 : launch_indexer<MSA_INDEX_NVFP4>(p, cache->index_pages, stream);
+  return launch_indexer<MSA_INDEX_FP8>(p, cache->index_pages, stream);  // FP8 keys are never re-rounded
+}
+}  // namespace
+
+extern "C" msa_status msa_indexer_decode_range(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                               const uint8_t* index_q, int32_t block_begin, int32_t block_end,
+                                               float* block_scores, uint32_t* status, cudaStream_t stream) {
+  return indexer_entry(geo, batch, cache, index_q, block_begin, block_end, block_scores, status, false, stream);
+}
+
+extern "C" msa_status msa_indexer_decode_exact(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                               const uint8_t* index_q, float* block_scores, uint32_t* status,
+                                               cudaStream_t stream) {
+  return indexer_entry(geo, batch, cache, index_q, 0, 0x7FFFFFFF, block_scores, status, true, stream);
 }
 
 extern "C" msa_status msa_indexer_decode(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,

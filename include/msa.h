@@ -296,6 +296,29 @@ msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_bat
 /* Size in bytes of the device array msa_sparse_attn_decode_noalloc uses. */
 size_t msa_noalloc_scratch_bytes(void);
 
+/* Workspace bytes msa_prefill_attn needs: the block -> query map (B x 4 x max_blocks_per_seq
+ * rows, T x 64 entries) and the per-(token, group, slot) partial results, about 2 MB a query
+ * token (T up to 2^22). 0 for invalid arguments. */
+size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
+                                  int32_t max_blocks_per_seq);
+
+/* Sparse GQA attention for any number of query tokens per sequence (the prefill / many-query
+ * path: "MiniMax M3 in vLLM ...", "预填充": block-major, a block's K and V read and dequantised
+ * once for all the queries that selected it, per-block results merged by log-sum-exp). Same
+ * result as msa_sparse_attn_decode for the same inputs (up to summation order); the batch may
+ * hold up to 2^20 query tokens per sequence (max_q_len) and 2^22 in all (T).
+ *   q, sel      as for msa_sparse_attn_decode ([T][64][128] E4M3, [T][4][16] int32)
+ *   workspace   device, 256-B aligned, >= msa_prefill_workspace_size(...) bytes
+ *   out         [T][64][128] bf16, device
+ *   status      nullable; an out-of-range selected block or a bad page id sets
+ *               MSA_ERR_DEVICE_FAULT and zero-fills that (token, group); an inconsistent batch
+ *               row sets MSA_ERR_INVALID_ARG
+ * Host-checkable errors return before any launch. */
+msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                            const uint8_t* q, const int32_t* sel, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, uint16_t* out,
+                            uint32_t* status, cudaStream_t stream);
+
 /* Workspace bytes msa_decode_step needs (depends only on its arguments). */
 size_t msa_decode_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
                                  int32_t max_blocks_per_seq);

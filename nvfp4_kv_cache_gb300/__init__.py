@@ -77,6 +77,8 @@ _SIGS = {
     "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
     "msa_indexer_decode_range": (_I32, [_GP, _BP, _CP, _P, _I32, _I32, _P, _P, _P]),
     "msa_indexer_decode_exact": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
+    "msa_prefill_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
+    "msa_prefill_attn": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _SZ, _P, _P, _P]),
     "msa_topk_candidates": (_I32, [_GP, _BP, _P, _I32, _I32, _P, _P, _P]),
     "msa_topk_merge": (_I32, [_GP, _BP, _P, _I32, _P, _P, _P]),
     "msa_topk_candidates_host": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P]),
@@ -223,6 +225,19 @@ def msa_indexer_decode_exact(batch: Batch, cache: Cache, index_q: torch.Tensor, 
     _check(_lib.msa_indexer_decode_exact(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
                                          _ptr(index_q), _ptr(block_scores), _ptr(status), _stream()),
            "msa_indexer_decode_exact")
+
+
+def msa_prefill_workspace_size(B: int, T: int, max_blocks_per_seq: int) -> int:
+    return int(_lib.msa_prefill_workspace_size(ctypes.byref(GEOMETRY), B, T, max_blocks_per_seq))
+
+
+def msa_prefill_attn(batch: Batch, cache: Cache, q: torch.Tensor, sel: torch.Tensor, softmax_scale: float,
+                     out: torch.Tensor, workspace: torch.Tensor, status: Optional[torch.Tensor] = None) -> None:
+    """Block-major sparse attention for any number of query tokens per sequence."""
+    _check(_lib.msa_prefill_attn(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(q),
+                                 _ptr(sel), ctypes.c_float(softmax_scale), _ptr(workspace),
+                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(out),
+                                 _ptr(status), _stream()), "msa_prefill_attn")
 
 
 def msa_topk_candidates(batch: Batch, block_scores: torch.Tensor, block_begin: int, block_end: int,

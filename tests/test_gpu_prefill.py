@@ -1,0 +1,137 @@
+"""GPU parity of the block-major prefill attention (msa_prefill_attn: a key-block -> query map,
+each selected block dequantised once for all the queries that picked it, log-sum-exp merge of
+the per-block partials) against the oracle's attention, for prompts of hundreds of query tokens
+per sequence, and against the decode attention where both apply."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from parity import OracleSeq, check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import nvfp4_kv_cache_gb300 as m
+
+    return m
+
+
+def random_selection(w: W.Workload, seed: int, dup: bool = False) -> np.ndarray:
+    """Valid selections [T, 4, 16]: the token's local block in slot 0, then up to 15 distinct
+    earlier blocks, -1 padding (and, with dup, a repeated block in some rows)."""
+    rng = np.random.default_rng(seed)
+    qsl = w.query_start_loc()
+    sel = np.full((w.T, 4, 16), -1, dtype=np.int32)
+    for b in range(w.B):
+        L, ql = w.seq_lens[b], w.q_lens[b]
+        for i in range(ql):
+            t = qsl[b] + i
+            local = (L - ql + i) // 128
+            for g in range(4):
+                k = min(15, local)
+                others = rng.choice(local, size=k, replace=False) if k else np.zeros(0, np.int64)
+                sel[t, g, 0] = local
+                sel[t, g, 1:1 + k] = others
+                if dup and k >= 2 and (t + g) % 5 == 0:
+                    sel[t, g, 2] = sel[t, g, 1]
+    return sel
+
+
+def run_prefill(msa, dl, w, sel_np, status=None):
+    sel = torch.from_numpy(sel_np).cuda()
+    out = torch.full((w.T, 64, 128), 0x7FC0, dtype=torch.uint16, device="cuda")  # NaN fill
+    n = msa.msa_prefill_workspace_size(w.B, w.T, dl.batch.max_blocks)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    msa.msa_prefill_attn(dl.batch, dl.cache, dl.q8, sel, dl.softmax_scale, out, ws, status)
+    torch.cuda.synchronize()
+    return out
+
+
+CASES = {
+    "prompts": dict(seq_lens=[3000, 1500 + 33, 700], q_lens=[200, 37, 1], seed=61),
+    "long_prompt": dict(seq_lens=[9000 + 5], q_lens=[1100], seed=62),
+    "ragged": dict(seq_lens=[129, 4000, 0, 2600], q_lens=[129, 64, 0, 300], seed=63),
+    "outliers": dict(seq_lens=[5000, 2000], q_lens=[150, 9], seed=64, outlier_frac=0.01),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_prefill_matches_the_oracle(msa, case):
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small(case, **CASES[case])
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 100 + len(case), dup=True)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = bf16_to_f32(run_prefill(msa, dl, w, sel, st)).cpu().numpy()
+    assert msa.status_bits(st) == 0
+    qsl = w.query_start_loc()
+    for b in range(w.B):
+        ql = w.q_lens[b]
+        if ql == 0:
+            continue
+        rows = slice(qsl[b], qsl[b] + ql)
+        s = sel[rows]
+        ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(s[s >= 0])).attention(s, dl.softmax_scale)
+        check_attention(out[rows], ref, f"{case} seq {b}")
+
+
+def test_prefill_equals_decode_attention_where_both_apply(msa):
+    """q_len <= 8 for every sequence: the prefill path and the decode path attend over the same
+    keys (different summation order)."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("both", [3000, 5000 + 7, 1300], [8, 3, 1], seed=65)
+    dl = DeviceLayer(w, 0)
+    sel_np = random_selection(w, 7)
+    a = bf16_to_f32(run_prefill(msa, dl, w, sel_np))
+    sel = torch.from_numpy(sel_np).cuda()
+    b = torch.empty((w.T, 64, 128), dtype=torch.uint16, device="cuda")
+    ws = torch.empty(max(msa.msa_attn_workspace_size(w.B, w.T, 0), 256), dtype=torch.uint8, device="cuda")
+    msa.msa_sparse_attn_decode(dl.batch, dl.cache, dl.q8, sel, dl.softmax_scale, b, 0, ws)
+    torch.cuda.synchronize()
+    b = bf16_to_f32(b)
+    assert float((a - b).abs().max()) <= 2e-2
+    assert float((a - b).norm() / b.norm()) <= 2e-3
+
+
+def test_prefill_faults_zero_fill_and_report(msa):
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("pfault", [3000, 2000], [100, 20], seed=66)
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 8)
+    good = bf16_to_f32(run_prefill(msa, dl, w, sel))
+    bad_sel = sel.copy()
+    bad_sel[5, 1, 3] = 10_000  # beyond sequence 0's blocks
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = bf16_to_f32(run_prefill(msa, dl, w, bad_sel, st))
+    assert msa.status_bits(st) == 1 << msa.MSA_ERR_DEVICE_FAULT
+    assert (out[5, 16:32] == 0).all()
+    keep = torch.ones(w.T, 64, dtype=torch.bool)
+    keep[5, 16:32] = False
+    assert torch.equal(out[keep], good[keep])
+    # a bad page id behind a block some tokens selected: those (token, group) rows are zeroed
+    bt = dl.batch.block_table.clone()
+    victim = int(sel[110, 0, 1])  # a non-local block of a token of sequence 1
+    bt[1, victim] = w.num_pages + 3
+    batch = msa.Batch(dl.batch.query_start_loc, dl.batch.seq_lens, bt, w.max_q_len, T=w.T)
+    st.zero_()
+    selt = torch.from_numpy(sel).cuda()
+    out2 = torch.empty((w.T, 64, 128), dtype=torch.uint16, device="cuda")
+    ws = torch.empty(msa.msa_prefill_workspace_size(w.B, w.T, dl.batch.max_blocks), dtype=torch.uint8, device="cuda")
+    msa.msa_prefill_attn(batch, dl.cache, dl.q8, selt, dl.softmax_scale, out2, ws, st)
+    torch.cuda.synchronize()
+    assert msa.status_bits(st) == 1 << msa.MSA_ERR_DEVICE_FAULT
+    out2 = bf16_to_f32(out2)
+    hit = (sel[100:120] == victim).any(-1)  # [20, 4] rows of sequence 1 that selected it
+    for i in range(20):
+        for g in range(4):
+            rows = out2[100 + i, 16 * g:16 * (g + 1)]
+            if hit[i, g]:
+                assert (rows == 0).all()
+            else:
+                assert torch.equal(rows, good[100 + i, 16 * g:16 * (g + 1)])

@@ -801,10 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = m->t, g = m->g, split = m->split, p_tok = m->p_tok;
       const bool valid = m->valid != 0, bad = m->bad != 0;
       const int os = k & 1;
-      // m_ref starts at a huge negative finite value rather than -inf, so that the exponent
-      // argument s * c - m_ref is +huge for any real score (the vote below takes the block's
-      // maximum then) and -inf for a masked key (P = 0), with no special case for the first block
-      constexpr float kNoRef = -1e30f;
+      // m_ref starts at a large negative finite value rather than -inf, so that the exponent
+      // argument s * c - m_ref is large for any real score (the vote below takes the block's
+      // maximum then) and -inf for a masked key (P = 0), with no special case for the first
+      // block; 2^14 keeps s * c = d + m_ref within 2^-9 of the score (fp32 at 2^14), which only
+      // shifts the reference, never a P beyond the vote's bound
+      constexpr float kNoRef = -16384.0f;
       float m_ref[16], l[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
@@ -814,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j, ++jg) {
         const int x = jg & 1;
         const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
-        float sv[16];  // this key's raw scores, -inf when the key lies after the query position
+        float d[16];  // exponent arguments s * c - m_ref against the current reference
         if (wait_ok(&s_full[x], par)) {
           tc_fence_after();
           uint32_t r[16];
@@ -823,24 +825,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[x]);
-          const bool kvalid = m->blk[j] * kBS + kr <= p_tok;
+          const bool kvalid = m->blk[j] * kBS + kr <= p_tok;  // keys after the query position: -inf
 #pragma unroll
-          for (int h = 0; h < 16; ++h) sv[h] = kvalid ? __uint_as_float(r[h]) : -CUDART_INF_F;
+          for (int h = 0; h < 16; ++h) d[h] = kvalid ? fmaf(__uint_as_float(r[h]), c, -m_ref[h]) : -CUDART_INF_F;
         } else {
 #pragma unroll
-          for (int h = 0; h < 16; ++h) sv[h] = -CUDART_INF_F;
+          for (int h = 0; h < 16; ++h) d[h] = -CUDART_INF_F;
         }
-        float d[16];  // exponent arguments against the current reference
         bool need = false;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          d[h] = fmaf(sv[h], c, -m_ref[h]);
-          need |= d[h] > kRescaleLog2;
-        }
+        for (int h = 0; h < 16; ++h) need |= d[h] > kRescaleLog2;
         if (named_barrier_or(kBarWork, 128, need)) {  // the same answer in all four warps
-          float cf[16];  // the block maxima, then the rescale factors
+          float cf[16];  // the block maxima of s * c, then the rescale factors
 #pragma unroll
-          for (int h = 0; h < 16; ++h) cf[h] = sv[h] * c;
+          for (int h = 0; h < 16; ++h) cf[h] = d[h] + m_ref[h];
           group_reduce16<true>(cf, cf, red + 64 * (nred & 1), wq, lane);
           ++nred;
           bool moved = false;
@@ -848,10 +846,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 16; ++h) {
             const float mn = fmaxf(m_ref[h], cf[h]);
             moved |= mn != m_ref[h];
+            d[h] += m_ref[h] - mn;              // the same arguments against the new reference
             cf[h] = fast_exp2(m_ref[h] - mn);  // 0 when there was no reference yet
             m_ref[h] = mn;
             l[h] *= cf[h];
-            d[h] = fmaf(sv[h], c, -mn);
           }
           // both accumulators *= cf once PV(jg - 1) and PV(jg - 2) have landed (PV(jg) waits for
           // this block's P); one not yet written in this unit is rescaled harmlessly: its first

@@ -297,7 +297,7 @@ msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_bat
 size_t msa_noalloc_scratch_bytes(void);
 
 /* Workspace bytes msa_prefill_attn needs: the block -> query map (B x 4 x max_blocks_per_seq
- * rows, T x 64 entries) and the per-(token, group, slot) partial results, about 2 MB a query
+ * rows, T x 64 entries) and the per-(token, group, slot) partial results, about 1 MB a query
  * token (T up to 2^22). 0 for invalid arguments. */
 size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
                                   int32_t max_blocks_per_seq);

@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- the unit's output: lane kr = dim kr of O^T; l summed over the 128 keys' threads --
-      float lt[16];
+      float (&lt)[16] = l;  // the per-head sums, reduced in place
       group_reduce16<false>(l, lt, red + 64 * (nred & 1), wq, lane);
       ++nred;
       uint32_t o[16];

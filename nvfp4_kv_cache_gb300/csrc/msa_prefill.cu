@@ -15,10 +15,12 @@
 //     tensor copy of the block's K and V regions, the K rows dequantised to an E4M3 tile and
 //     the V rows to an f16 tile (shared memory, swizzled) once, then each warp takes entries:
 //     the 16 heads of the entry's token attend over the block's 128 keys (mma.sync e4m3 QK^T,
-//     online softmax, mma.sync f16 PV) and the (lse, o) partial goes to the entry's slot;
+//     online softmax, mma.sync f16 PV) and the (lse, o) partial goes to the entry's slot (o
+//     normalised, in f16: half the partial traffic of fp32);
 //  3. k_prefill_merge: per (token, group), the log-sum-exp merge of its up to 16 partials.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -53,7 +55,7 @@ struct PfParams {
   int32_t* offset;   // [B * 4 * maxb + 1] exclusive prefix of count
   int32_t* entries;  // [T * 4 * 16] t << 4 | slot, grouped by (sequence, group, block)
   int32_t* tg_bad;   // [T * 4] the (token, group) saw a bad selection or page: zero output
-  float* part_o;     // [T * 4 * 16 slots][16 heads][128] normalised partial outputs
+  uint32_t* part_o;  // [T * 4 * 16 slots][16 heads][64] normalised partial outputs, f16 pairs
   float* part_lse;   // [T * 4 * 16 slots][16 heads] their log2-sum-exp (-inf: no partial)
   uint32_t* status;
 };
@@ -252,12 +254,12 @@ __global__ void __launch_bounds__(kPfThreads) k_prefill_attn(const PfParams p, c
     // the partial of (t, g, slot): o / l per head and log2(sum) + m
     const float l0 = quad_sum(st.l[0]), l1 = quad_sum(st.l[1]);
     const int64_t base = (static_cast<int64_t>(t) * 4 + g) * kSel + slot;
-    float* po = p.part_o + base * kHPG * kD;
+    uint32_t* po = p.part_o + base * kHPG * (kD / 2);  // f16 pairs: dims 2c, 2c + 1 in word c
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      *reinterpret_cast<float2*>(po + gid * kD + 8 * k + 2 * tq) = make_float2(st.o[k][0] * i0, st.o[k][1] * i0);
-      *reinterpret_cast<float2*>(po + (gid + 8) * kD + 8 * k + 2 * tq) = make_float2(st.o[k][2] * i1, st.o[k][3] * i1);
+      po[gid * (kD / 2) + 4 * k + tq] = pack_f16x2(st.o[k][0] * i0, st.o[k][1] * i0);
+      po[(gid + 8) * (kD / 2) + 4 * k + tq] = pack_f16x2(st.o[k][2] * i1, st.o[k][3] * i1);
     }
     if (tq == 0) {
       p.part_lse[base * kHPG + gid] = l0 > 0.f ? st.m[0] + __log2f(l0) : -CUDART_INF_F;
@@ -283,11 +285,13 @@ __global__ void __launch_bounds__(256) k_prefill_merge(const PfParams p) {
       const float lse = p.part_lse[(base + s) * kHPG + hh];
       if (lse == -CUDART_INF_F) continue;
       const float w = fast_exp2(lse - M);
-      const float4 o = *reinterpret_cast<const float4*>(p.part_o + ((base + s) * kHPG + hh) * kD + 4 * lane);
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
+      const uint2 ov = *reinterpret_cast<const uint2*>(p.part_o + ((base + s) * kHPG + hh) * (kD / 2) + 2 * lane);
+      const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&ov.x));
+      const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&ov.y));
+      acc.x += w * o01.x;
+      acc.y += w * o01.y;
+      acc.z += w * o23.x;
+      acc.w += w * o23.y;
       W += w;
     }
   }
@@ -310,7 +314,7 @@ PfLayout pf_layout(int B, int T, int maxb) {
   l.entries = l.offset + align256((rows + 1) * 4);
   l.tg_bad = l.entries + align256(ent * 4);
   l.part_o = l.tg_bad + align256(static_cast<size_t>(T) * 4 * 4);
-  l.part_lse = l.part_o + align256(ent * kHPG * kD * 4);
+  l.part_lse = l.part_o + align256(ent * kHPG * kD * 2);
   l.total = l.part_lse + align256(ent * kHPG * 4);
   return l;
 }
@@ -365,7 +369,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   p.offset = reinterpret_cast<int32_t*>(ws + lay.offset);
   p.entries = reinterpret_cast<int32_t*>(ws + lay.entries);
   p.tg_bad = reinterpret_cast<int32_t*>(ws + lay.tg_bad);
-  p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+  p.part_o = reinterpret_cast<uint32_t*>(ws + lay.part_o);
   p.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   p.status = status;
   const int64_t rows = static_cast<int64_t>(p.B) * 4 * p.maxb;

@@ -338,6 +338,40 @@ msa_status msa_decode_step(const msa_geometry* geo, const msa_batch* batch,
                            void* workspace, size_t workspace_bytes, uint16_t* out,
                            cudaStream_t stream);
 
+/* The step's inputs and output in page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister), for msa_decode_step_host. Shapes as in msa_batch / msa_decode_step. */
+typedef struct msa_host_step_io {
+  const int32_t* query_start_loc; /* [B + 1] */
+  const int32_t* seq_lens;        /* [B] */
+  const int32_t* block_table;     /* [B][max_blocks_per_seq] */
+  const uint8_t* q;               /* [T][64][128] E4M3 */
+  const uint8_t* index_q;         /* [T][4][128] E4M3 */
+  uint16_t* out;                  /* [T][64][128] bf16, written */
+} msa_host_step_io;
+
+/* msa_decode_step from host buffers: copies `host`'s inputs into the device buffers (batch's
+ * three arrays, q, index_q), runs the step, and copies the output back into host->out, with
+ * the copies on `copy_stream` overlapping the kernels on `stream`. The index queries and the
+ * batch arrays go first and the indexer starts on them while q is still copying; the
+ * attention runs as two launches (see msa_decode_step's batches of more than 76 tokens) and
+ * the first launch's output rows copy back while the second runs. Ordering: the copies wait
+ * for the work already on `stream` (the device buffers may be in use there), and `stream`
+ * waits for the last copy, so when `stream` reaches the end of the call host->out holds the
+ * output. Same result as msa_decode_step on the same inputs, bit for bit.
+ *   batch      B, T, max_blocks_per_seq, max_q_len and the DEVICE arrays to fill
+ *   host       page-locked host buffers (checked: MSA_ERR_INVALID_ARG otherwise)
+ *   q, index_q DEVICE buffers to fill, as for msa_decode_step
+ *   workspace  as for msa_decode_step
+ *   out        DEVICE [T][64][128] bf16, the output before its copy back
+ *   copy_stream may equal stream (no overlap then)
+ * Host-checkable errors return before anything is enqueued; the call creates and releases
+ * its own CUDA events (MSA_ERR_CUDA if it cannot). */
+msa_status msa_decode_step_host(const msa_geometry* geo, const msa_batch* batch,
+                                const msa_cache* cache, const msa_host_step_io* host,
+                                uint8_t* q, uint8_t* index_q, float softmax_scale,
+                                void* workspace, size_t workspace_bytes, uint16_t* out,
+                                cudaStream_t stream, cudaStream_t copy_stream);
+
 /* Test and debugging helper: waits for `stream`, then returns the most severe code whose
  * bit is set in the status word at the start of `workspace` (MSA_OK when none). */
 msa_status msa_read_device_status(const void* workspace, cudaStream_t stream);

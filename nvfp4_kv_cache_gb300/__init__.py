@@ -56,6 +56,10 @@ class msa_cache(ctypes.Structure):
                 ("num_pages", ctypes.c_int32)]
 
 
+class msa_host_step_io(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("query_start_loc", "seq_lens", "block_table", "q", "index_q", "out")]
+
+
 GEOMETRY = msa_geometry(64, 4, 128, 128, 128, 16, 1, 0)
 
 _P = ctypes.c_void_p
@@ -65,6 +69,7 @@ _SZ = ctypes.c_size_t
 _GP = ctypes.POINTER(msa_geometry)
 _BP = ctypes.POINTER(msa_batch)
 _CP = ctypes.POINTER(msa_cache)
+_HP = ctypes.POINTER(msa_host_step_io)
 
 _SIGS = {
     "msa_status_string": (ctypes.c_char_p, [_I32]),
@@ -89,6 +94,7 @@ _SIGS = {
     "msa_noalloc_scratch_bytes": (_SZ, []),
     "msa_decode_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_decode_step": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
+    "msa_decode_step_host": (_I32, [_GP, _BP, _CP, _HP, _P, _P, ctypes.c_float, _P, _SZ, _P, _P, _P]),
     "msa_read_device_status": (_I32, [_P, _P]),
     "msa_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
 }
@@ -314,6 +320,28 @@ def msa_decode_step(batch: Batch, cache: Cache, q: torch.Tensor, index_q: torch.
     _check(_lib.msa_decode_step(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(q),
                                 _ptr(index_q), float(softmax_scale), _ptr(dbg_block_scores), _ptr(dbg_sel),
                                 _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)), "msa_decode_step")
+
+
+def msa_decode_step_host(batch: Batch, cache: Cache, host_qsl: torch.Tensor, host_seq_lens: torch.Tensor,
+                         host_block_table: torch.Tensor, host_q: torch.Tensor, host_index_q: torch.Tensor,
+                         host_out: torch.Tensor, q: torch.Tensor, index_q: torch.Tensor, softmax_scale: float,
+                         workspace: torch.Tensor, out: torch.Tensor, copy_stream: torch.cuda.Stream,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """msa_decode_step from page-locked host tensors: `batch`'s device arrays, q and index_q are
+    filled from the host ones and host_out receives the output, the copies on copy_stream
+    overlapping the kernels on `stream` (include/msa.h). host_out is complete once `stream`
+    has passed the call."""
+    for n, t in (("host_qsl", host_qsl), ("host_seq_lens", host_seq_lens), ("host_block_table", host_block_table),
+                 ("host_q", host_q), ("host_index_q", host_index_q), ("host_out", host_out)):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous page-locked host tensor")
+    io = msa_host_step_io(host_qsl.data_ptr(), host_seq_lens.data_ptr(), host_block_table.data_ptr(),
+                          host_q.data_ptr(), host_index_q.data_ptr(), host_out.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.msa_decode_step_host(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                     ctypes.byref(io), _ptr(q), _ptr(index_q), float(softmax_scale), _ptr(workspace),
+                                     ws_bytes, _ptr(out), _stream(stream), _stream(copy_stream)),
+           "msa_decode_step_host")
 
 
 def msa_read_device_status(workspace: torch.Tensor) -> int:

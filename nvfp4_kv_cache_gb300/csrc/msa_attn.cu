@@ -60,6 +60,7 @@ constexpr int kBarTok = 1, kBarDq0 = 2;                     // named barriers (0
 
 struct AttnParams {
   int32_t B, T, maxb, max_q_len, num_pages, splits;
+  int32_t t0, nt;  // the tokens [t0, t0 + nt) this launch attends for (the many-token kernel)
   const int32_t* qsl;
   const int32_t* seq_lens;
   const int32_t* block_table;
@@ -485,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int units = p.T * 4 * p.splits;
+  const int units = p.nt * 4 * p.splits;
   constexpr int kMetaUsers = 15;  // the S and two PV issuers, two dequant groups and the softmax group
 
   // ---- prologue --------------------------------------------------------------------------
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
       if (!wait_ok(&meta_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
       UnitMeta& m = metas[k & 1];
-      const int split = u % p.splits, tg = u / p.splits, t = tg >> 2, g = tg & 3;
+      const int split = u % p.splits, tg = u / p.splits, t = p.t0 + (tg >> 2), g = tg & 3;
       int lo = 0, hi = p.B - 1;  // the sequence of token t (largest b with qsl[b] <= t)
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -997,6 +998,8 @@ msa_status attn_setup(const msa_geometry* geo, const msa_batch* batch, const msa
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
   p->B = batch->B;
   p->T = batch->T;
+  p->t0 = 0;
+  p->nt = batch->T;
   p->maxb = batch->max_blocks_per_seq;
   p->max_q_len = batch->max_q_len;
   p->num_pages = cache->num_pages;
@@ -1035,7 +1038,7 @@ msa_status attn_launch(const AttnParams& p, const uint8_t* kv_pages, cudaStream_
       return MSA_ERR_CUDA;
     const int sms = msa_host::num_sms();
     if (sms <= 0) return MSA_ERR_CUDA;
-    const int units = p.T * 4 * p.splits;
+    const int units = p.nt * 4 * p.splits;
     tc::k_attn_tc<<<units < sms ? units : sms, tc::kThreads, tc::Smem::kBytes, stream>>>(p, kv_map, q_map);
     msa_status st = msa_host::launch_status();
     if (st != MSA_OK) return st;
@@ -1087,6 +1090,34 @@ extern "C" msa_status msa_sparse_attn_decode(const msa_geometry* geo, const msa_
     return MSA_ERR_INVALID_ARG;
   attn_bind_ws(&p, workspace);
   return attn_launch(p, cache->kv_pages, stream);
+}
+
+// The attention of the tokens [t0, t1) alone, for batches the many-token kernel takes with one
+// split (the output rows of other tokens are left as they are). The host-buffer step runs the
+// attention as two such launches so that the copy of the first one's output to the host
+// overlaps the second.
+msa_status msa_attn_token_range(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                const uint8_t* q, const int32_t* sel, float softmax_scale, uint16_t* out,
+                                uint32_t* status, int32_t t0, int32_t t1, cudaStream_t stream) {
+  AttnParams p;
+  msa_status st = attn_setup(geo, batch, cache, q, sel, softmax_scale, 0, out, status, &p);
+  if (st != MSA_OK || p.T == 0) return st;
+  if (!use_tc_kernel(p.T) || p.splits != 1 || t0 < 0 || t1 > p.T || t0 >= t1) return MSA_ERR_INVALID_ARG;
+  p.t0 = t0;
+  p.nt = t1 - t0;
+  return attn_launch(p, cache->kv_pages, stream);
+}
+
+// Where the host-buffer step splits the attention: the second launch takes the tokens of the
+// persistent grid's last two rounds of units (one unit per SM a round, four units a token), so
+// the split adds no round; 0 = one launch (the small-batch kernel, or fewer than four rounds).
+int32_t msa_attn_split_token(int32_t T) {
+  if (!use_tc_kernel(T)) return 0;
+  const int sms = num_sms();
+  const int per_round = sms / 4;
+  if (per_round <= 0) return 0;
+  const int rounds = ceil_div(T, per_round);
+  return rounds < 4 ? 0 : per_round * (rounds - 2);
 }
 
 // ------------------------------------------------------------------------------------------

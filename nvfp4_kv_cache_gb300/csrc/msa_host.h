@@ -78,3 +78,12 @@ bool kv_tensor_map(void* tmap64, const uint8_t* base, uint64_t num_pages);
 // Launchers implemented in the kernel translation units.
 msa_status msa_launch_attn_merge(const float* part_o, const float* part_lse, int32_t splits, int32_t T,
                                  uint16_t* out, cudaStream_t stream);
+
+// The attention of the tokens [t0, t1) of the batch alone (msa_attn.cu): only for batches the
+// many-token kernel takes with one split; MSA_ERR_INVALID_ARG otherwise.
+msa_status msa_attn_token_range(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                                const uint8_t* q, const int32_t* sel, float softmax_scale, uint16_t* out,
+                                uint32_t* status, int32_t t0, int32_t t1, cudaStream_t stream);
+
+// The token at which the host-buffer step splits the attention into two launches (0 = one).
+int32_t msa_attn_split_token(int32_t T);

@@ -9,11 +9,12 @@ quoted on). One step = indexer -> top-k -> sparse attention -> merge over the wh
 Prints one JSON line. `value` is microseconds per layer-step (lower is better, max over
 ranks); the roofline object reports the dominant kernel (the stage with the longer time:
 the sparse attention or the indexer) against the measured HBM peak, `roofline_stages` both;
-`e2e` repeats the measurement through host buffers with msa_decode_step_host (pinned H2D of
-the step's queries and metadata, D2H of the output, on a copy stream overlapped with the
-kernels) inside the timed region, and `e2e.serial_copies_us` the same copies issued one after
-another around msa_decode_step; `cpu_baseline` times the oracle on a bounded sample on the
-host cores.
+`e2e` repeats the measurement through host buffers with msa_decode_step_host inside the
+timed region (pinned H2D of the step's queries and metadata on two streams, q behind the
+indexer, and the attention storing the output into the pinned host buffer);
+`e2e.copy_back_us` is the same call with the output copied back on the copy stream instead, and
+`e2e.serial_copies_us` the same copies issued one after another around msa_decode_step;
+`cpu_baseline` times the oracle on a bounded sample on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config spec] [--impl ours|reference]
 """
@@ -356,6 +357,10 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
 
     def host_step():
         msa.msa_decode_step_host(dl.batch, dl.cache, meta_h[0], meta_h[1], meta_h[2], q_h, iq_h, out_h, dl.q8, dl.iq8,
+                                 dl.softmax_scale, ws, None, copy_stream, direct_out=True)
+
+    def host_step_copy_back():
+        msa.msa_decode_step_host(dl.batch, dl.cache, meta_h[0], meta_h[1], meta_h[2], q_h, iq_h, out_h, dl.q8, dl.iq8,
                                  dl.softmax_scale, ws, o["out"], copy_stream)
 
     def serial_step():
@@ -385,6 +390,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     e2e_ms = time_e2e(host_step)
     if msa.msa_read_device_status(ws) != msa.MSA_OK:
         raise RuntimeError("device status not OK after the host-buffer steps")
+    e2e_copy_back_ms = time_e2e(host_step_copy_back)
     e2e_serial_ms = time_e2e(serial_step)
 
     if rank != 0:
@@ -433,8 +439,10 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
         "roofline": roof[dominant],
         "roofline_stages": roof,
         "e2e": {"value": e2e_ms * 1e3, "unit": "us/layer-step", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "api": "msa_decode_step_host (copies overlapped)",
-                "serial_copies_us": e2e_serial_ms * 1e3},
+                "d2h_bytes_per_step": int(d2h),
+                "api": "msa_decode_step_host, MSA_HOST_STEP_DIRECT_OUT: input copies on two streams, q behind "
+                       "the indexer, the attention storing the bf16 output into the pinned host buffer",
+                "copy_back_us": e2e_copy_back_ms * 1e3, "serial_copies_us": e2e_serial_ms * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

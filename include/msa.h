@@ -349,28 +349,40 @@ typedef struct msa_host_step_io {
   uint16_t* out;                  /* [T][64][128] bf16, written */
 } msa_host_step_io;
 
+/* Flags of msa_decode_step_host. */
+enum { MSA_HOST_STEP_DIRECT_OUT = 1 };
+
 /* msa_decode_step from host buffers: copies `host`'s inputs into the device buffers (batch's
- * three arrays, q, index_q), runs the step, and copies the output back into host->out, with
- * the copies on `copy_stream` overlapping the kernels on `stream`. The index queries and the
- * batch arrays go first and the indexer starts on them while q is still copying; the
- * attention runs as two launches (see msa_decode_step's batches of more than 76 tokens) and
- * the first launch's output rows copy back while the second runs. Ordering: the copies wait
- * for the work already on `stream` (the device buffers may be in use there), and `stream`
- * waits for the last copy, so when `stream` reaches the end of the call host->out holds the
- * output. Same result as msa_decode_step on the same inputs, bit for bit.
+ * three arrays, q, index_q), runs the step, and delivers the output into host->out, with the
+ * copies on `copy_stream` and `stream` overlapping the kernels. The block table goes first on
+ * the copy stream while the other batch arrays and the index queries go on `stream`; the
+ * indexer starts on them while q is still copying.
+ *   flags 0: the output is copied back from `out`; a batch that keeps the many-token attention
+ *            kernel busy for six or more rounds of units runs it as two launches (the last
+ *            three rounds in the second) so that the first launch's rows copy back while the
+ *            second runs.
+ *   flags MSA_HOST_STEP_DIRECT_OUT: the attention stores its output straight into host->out
+ *            (no copy back, `out` unused and may be null); host->out must be reachable by
+ *            kernels at its own address (page-locked memory under unified addressing, which
+ *            cudaPointerGetAttributes reports), else MSA_ERR_INVALID_ARG.
+ * Ordering: the copies wait for the work already on `stream` (the device buffers may be in
+ * use there), and `stream` waits for the copy stream's last copy, so when `stream` reaches the
+ * end of the call host->out holds the output. Same result as msa_decode_step on the same
+ * inputs, bit for bit.
  *   batch      B, T, max_blocks_per_seq, max_q_len and the DEVICE arrays to fill
  *   host       page-locked host buffers (checked: MSA_ERR_INVALID_ARG otherwise)
  *   q, index_q DEVICE buffers to fill, as for msa_decode_step
  *   workspace  as for msa_decode_step
- *   out        DEVICE [T][64][128] bf16, the output before its copy back
+ *   out        DEVICE [T][64][128] bf16, the output before its copy back (flags 0)
  *   copy_stream may equal stream (no overlap then)
- * Host-checkable errors return before anything is enqueued; the call creates and releases
- * its own CUDA events (MSA_ERR_CUDA if it cannot). */
+ * Host-checkable errors return before anything is enqueued. The call orders its streams with
+ * CUDA events it creates once per host thread and device and keeps until the thread exits
+ * (MSA_ERR_CUDA if it cannot create them). */
 msa_status msa_decode_step_host(const msa_geometry* geo, const msa_batch* batch,
                                 const msa_cache* cache, const msa_host_step_io* host,
                                 uint8_t* q, uint8_t* index_q, float softmax_scale,
                                 void* workspace, size_t workspace_bytes, uint16_t* out,
-                                cudaStream_t stream, cudaStream_t copy_stream);
+                                int32_t flags, cudaStream_t stream, cudaStream_t copy_stream);
 
 /* Test and debugging helper: waits for `stream`, then returns the most severe code whose
  * bit is set in the status word at the start of `workspace` (MSA_OK when none). */

@@ -30,6 +30,7 @@ MSA_ERR_TIMEOUT = 4
 MSA_ERR_DEVICE_FAULT = 5
 MSA_INDEX_NVFP4 = 0
 MSA_INDEX_FP8 = 1
+MSA_HOST_STEP_DIRECT_OUT = 1
 
 HEAD_DIM = 128
 GROUPS = 4
@@ -94,7 +95,7 @@ _SIGS = {
     "msa_noalloc_scratch_bytes": (_SZ, []),
     "msa_decode_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_decode_step": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
-    "msa_decode_step_host": (_I32, [_GP, _BP, _CP, _HP, _P, _P, ctypes.c_float, _P, _SZ, _P, _P, _P]),
+    "msa_decode_step_host": (_I32, [_GP, _BP, _CP, _HP, _P, _P, ctypes.c_float, _P, _SZ, _P, _I32, _P, _P]),
     "msa_read_device_status": (_I32, [_P, _P]),
     "msa_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
 }
@@ -325,12 +326,13 @@ def msa_decode_step(batch: Batch, cache: Cache, q: torch.Tensor, index_q: torch.
 def msa_decode_step_host(batch: Batch, cache: Cache, host_qsl: torch.Tensor, host_seq_lens: torch.Tensor,
                          host_block_table: torch.Tensor, host_q: torch.Tensor, host_index_q: torch.Tensor,
                          host_out: torch.Tensor, q: torch.Tensor, index_q: torch.Tensor, softmax_scale: float,
-                         workspace: torch.Tensor, out: torch.Tensor, copy_stream: torch.cuda.Stream,
-                         stream: Optional[torch.cuda.Stream] = None) -> None:
+                         workspace: torch.Tensor, out: Optional[torch.Tensor], copy_stream: torch.cuda.Stream,
+                         direct_out: bool = False, stream: Optional[torch.cuda.Stream] = None) -> None:
     """msa_decode_step from page-locked host tensors: `batch`'s device arrays, q and index_q are
-    filled from the host ones and host_out receives the output, the copies on copy_stream
-    overlapping the kernels on `stream` (include/msa.h). host_out is complete once `stream`
-    has passed the call."""
+    filled from the host ones and host_out receives the output (copied back from `out`, or with
+    direct_out stored there by the attention itself), the copies on copy_stream and `stream`
+    overlapping the kernels (include/msa.h). host_out is complete once `stream` has passed the
+    call."""
     for n, t in (("host_qsl", host_qsl), ("host_seq_lens", host_seq_lens), ("host_block_table", host_block_table),
                  ("host_q", host_q), ("host_index_q", host_index_q), ("host_out", host_out)):
         if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
@@ -340,7 +342,8 @@ def msa_decode_step_host(batch: Batch, cache: Cache, host_qsl: torch.Tensor, hos
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(_lib.msa_decode_step_host(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
                                      ctypes.byref(io), _ptr(q), _ptr(index_q), float(softmax_scale), _ptr(workspace),
-                                     ws_bytes, _ptr(out), _stream(stream), _stream(copy_stream)),
+                                     ws_bytes, _ptr(out), MSA_HOST_STEP_DIRECT_OUT if direct_out else 0,
+                                     _stream(stream), _stream(copy_stream)),
            "msa_decode_step_host")
 
 

@@ -149,46 +149,63 @@ extern "C" msa_status msa_decode_step(const msa_geometry* geo, const msa_batch* 
 
 namespace {
 
-bool page_locked(const void* ptr) {
+// Page-locked host memory, and the address kernels reach it at (nullptr when they cannot).
+bool page_locked(const void* ptr, void** device_ptr = nullptr) {
+  if (device_ptr != nullptr) *device_ptr = nullptr;
   if (ptr == nullptr) return false;
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
     cudaGetLastError();  // an unregistered pointer may leave an error behind on older runtimes
     return false;
   }
-  return a.type == cudaMemoryTypeHost;
+  if (a.type != cudaMemoryTypeHost) return false;
+  if (device_ptr != nullptr) *device_ptr = a.devicePointer;
+  return true;
 }
 
-// The CUDA events of one msa_decode_step_host call, released when it returns (a recorded
-// event may be destroyed before it completes; its waiters are unaffected).
-struct CallEvents {
-  static constexpr int kN = 6;
-  cudaEvent_t e[kN] = {};
-  bool ok = true;
-  CallEvents() {
-    for (auto& x : e)
-      if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) {
-        x = nullptr;
-        ok = false;
-      }
+// The CUDA events msa_decode_step_host orders its two streams with: one set per host thread
+// and device, created on first use and released when the thread exits. Reusing them across
+// calls is safe: a wait refers to the record enqueued before it, and a later record does not
+// change what an earlier wait waits for.
+struct StepEvents {
+  static constexpr int kN = 5;
+  static constexpr int kMaxDev = 64;
+  cudaEvent_t e[kMaxDev][kN] = {};
+  ~StepEvents() {
+    for (auto& d : e)
+      for (auto x : d)
+        if (x != nullptr) cudaEventDestroy(x);
   }
-  ~CallEvents() {
-    for (auto x : e)
-      if (x != nullptr) cudaEventDestroy(x);
+  // the current device's set, or nullptr when it cannot be created
+  cudaEvent_t* get() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    cudaEvent_t* d = e[dev];
+    for (int i = 0; i < kN; ++i)
+      if (d[i] == nullptr && cudaEventCreateWithFlags(&d[i], cudaEventDisableTiming) != cudaSuccess) {
+        d[i] = nullptr;
+        return nullptr;
+      }
+    return d;
   }
 };
+thread_local StepEvents t_step_events;
 
 }  // namespace
 
 extern "C" msa_status msa_decode_step_host(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
                                            const msa_host_step_io* host, uint8_t* q, uint8_t* index_q,
                                            float softmax_scale, void* workspace, size_t workspace_bytes,
-                                           uint16_t* out, cudaStream_t stream, cudaStream_t copy_stream) {
+                                           uint16_t* out, int32_t flags, cudaStream_t stream,
+                                           cudaStream_t copy_stream) {
   msa_status st = check_geometry(geo);
   if (st != MSA_OK) return st;
   if ((st = check_batch(batch)) != MSA_OK) return st;
   if ((st = check_cache(cache, true, true)) != MSA_OK) return st;
-  if (host == nullptr || workspace == nullptr || !aligned(workspace, 256)) return MSA_ERR_INVALID_ARG;
+  if (host == nullptr || workspace == nullptr || !aligned(workspace, 256) ||
+      (flags & ~MSA_HOST_STEP_DIRECT_OUT) != 0)
+    return MSA_ERR_INVALID_ARG;
+  const bool direct = (flags & MSA_HOST_STEP_DIRECT_OUT) != 0;
   const WsLayout w = decode_layout(batch->B, batch->T, batch->max_blocks_per_seq);
   if (workspace_bytes < w.total) return MSA_ERR_INVALID_ARG;
   const size_t B = static_cast<size_t>(batch->B), T = static_cast<size_t>(batch->T);
@@ -196,62 +213,76 @@ extern "C" msa_status msa_decode_step_host(const msa_geometry* geo, const msa_ba
   const size_t n_q = T * kQHeads * kD, n_iq = T * 4 * kD, n_out = T * kQHeads * kD * 2;
   if (B > 0 && !(page_locked(host->query_start_loc) && page_locked(host->seq_lens) && page_locked(host->block_table)))
     return MSA_ERR_INVALID_ARG;
-  if (T > 0 && !(page_locked(host->q) && page_locked(host->index_q) && page_locked(host->out) && q != nullptr &&
-                 index_q != nullptr && out != nullptr))
-    return MSA_ERR_INVALID_ARG;
-  CallEvents ev;
-  if (!ev.ok) return MSA_ERR_CUDA;
-  cudaEvent_t e_start = ev.e[0], e_meta = ev.e[1], e_q = ev.e[2], e_a0 = ev.e[3], e_a1 = ev.e[4], e_done = ev.e[5];
+  void* out_dev_view = nullptr;  // host->out as the kernels address it (direct mode)
+  if (T > 0) {
+    if (!(page_locked(host->q) && page_locked(host->index_q) && page_locked(host->out, &out_dev_view) &&
+          q != nullptr && index_q != nullptr))
+      return MSA_ERR_INVALID_ARG;
+    // direct: the kernels must reach host->out at its own address (unified addressing)
+    if (direct ? out_dev_view != static_cast<void*>(host->out) : out == nullptr) return MSA_ERR_INVALID_ARG;
+  }
+  uint16_t* attn_out = direct ? host->out : out;
+  cudaEvent_t* ev = t_step_events.get();
+  if (ev == nullptr) return MSA_ERR_CUDA;
+  cudaEvent_t e_start = ev[0], e_meta = ev[1], e_q = ev[2], e_a0 = ev[3], e_a1 = ev[4];
   auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
   // the device buffers may still be read by work already on `stream`
   if (!cuda(cudaEventRecord(e_start, stream)) || !cuda(cudaStreamWaitEvent(copy_stream, e_start, 0)))
     return MSA_ERR_CUDA;
+  // what the indexer reads, on both streams side by side (the block table on the copy stream,
+  // the rest on `stream`), then q on the copy stream behind it
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   if (B > 0 &&
-      (!cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->query_start_loc), host->query_start_loc, n_qsl, h2d,
-                             copy_stream)) ||
-       !cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->seq_lens), host->seq_lens, n_sl, h2d, copy_stream)) ||
-       !cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->block_table), host->block_table, n_bt, h2d, copy_stream))))
+      (!cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->block_table), host->block_table, n_bt, h2d, copy_stream)) ||
+       !cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->query_start_loc), host->query_start_loc, n_qsl, h2d,
+                             stream)) ||
+       !cuda(cudaMemcpyAsync(const_cast<int32_t*>(batch->seq_lens), host->seq_lens, n_sl, h2d, stream))))
     return MSA_ERR_CUDA;
-  if (T > 0 && !cuda(cudaMemcpyAsync(index_q, host->index_q, n_iq, h2d, copy_stream))) return MSA_ERR_CUDA;
   if (!cuda(cudaEventRecord(e_meta, copy_stream))) return MSA_ERR_CUDA;
   if (T > 0 && !cuda(cudaMemcpyAsync(q, host->q, n_q, h2d, copy_stream))) return MSA_ERR_CUDA;
   if (!cuda(cudaEventRecord(e_q, copy_stream))) return MSA_ERR_CUDA;
+  if (T > 0 && !cuda(cudaMemcpyAsync(index_q, host->index_q, n_iq, h2d, stream))) return MSA_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   if (!cuda(cudaStreamWaitEvent(stream, e_meta, 0)) || !cuda(cudaMemsetAsync(status, 0, sizeof(uint32_t), stream)))
     return MSA_ERR_CUDA;
-  int32_t ta = 0;  // the attention's split token (0: one launch)
   if (T > 0) {
     float* scores = reinterpret_cast<float*>(ws + w.scores);
     int32_t* sel = reinterpret_cast<int32_t*>(ws + w.sel);
     if ((st = msa_indexer_decode(geo, batch, cache, index_q, scores, status, stream)) != MSA_OK) return st;
     if ((st = msa_topk_blocks(geo, batch, scores, sel, status, stream)) != MSA_OK) return st;
     if (!cuda(cudaStreamWaitEvent(stream, e_q, 0))) return MSA_ERR_CUDA;
-    ta = msa_attn_split_token(batch->T);
+    // direct: one launch that stores the output into host memory as it goes; else the attention
+    // in two launches when the batch is large enough, the first one's rows copying back while
+    // the second runs
+    const int32_t ta = direct ? 0 : msa_attn_split_token(batch->T);
     if (ta > 0) {
-      if ((st = msa_attn_token_range(geo, batch, cache, q, sel, softmax_scale, out, status, 0, ta, stream)) != MSA_OK)
-        return st;
-      if (!cuda(cudaEventRecord(e_a0, stream))) return MSA_ERR_CUDA;
-      if ((st = msa_attn_token_range(geo, batch, cache, q, sel, softmax_scale, out, status, ta, batch->T, stream)) !=
+      if ((st = msa_attn_token_range(geo, batch, cache, q, sel, softmax_scale, attn_out, status, 0, ta, stream)) !=
           MSA_OK)
         return st;
+      if (!cuda(cudaEventRecord(e_a0, stream))) return MSA_ERR_CUDA;
+      if ((st = msa_attn_token_range(geo, batch, cache, q, sel, softmax_scale, attn_out, status, ta, batch->T,
+                                     stream)) != MSA_OK)
+        return st;
     } else if ((st = msa_sparse_attn_decode(geo, batch, cache, q, sel, softmax_scale, 0, ws + w.attn,
-                                            w.total - w.attn, out, status, stream)) != MSA_OK) {
+                                            w.total - w.attn, attn_out, status, stream)) != MSA_OK) {
       return st;
     }
-    if (!cuda(cudaEventRecord(e_a1, stream))) return MSA_ERR_CUDA;
-    const size_t row = static_cast<size_t>(kQHeads) * kD;  // bf16 elements of one token's output
-    if (ta > 0 && (!cuda(cudaStreamWaitEvent(copy_stream, e_a0, 0)) ||
-                   !cuda(cudaMemcpyAsync(host->out, out, static_cast<size_t>(ta) * row * 2, d2h, copy_stream))))
-      return MSA_ERR_CUDA;
-    if (!cuda(cudaStreamWaitEvent(copy_stream, e_a1, 0)) ||
-        !cuda(cudaMemcpyAsync(host->out + static_cast<size_t>(ta) * row, out + static_cast<size_t>(ta) * row,
-                              n_out - static_cast<size_t>(ta) * row * 2, d2h, copy_stream)))
-      return MSA_ERR_CUDA;
+    if (!direct) {
+      if (!cuda(cudaEventRecord(e_a1, stream))) return MSA_ERR_CUDA;
+      const size_t row = static_cast<size_t>(kQHeads) * kD;  // bf16 elements of one token's output
+      if (ta > 0 && (!cuda(cudaStreamWaitEvent(copy_stream, e_a0, 0)) ||
+                     !cuda(cudaMemcpyAsync(host->out, out, static_cast<size_t>(ta) * row * 2, d2h, copy_stream))))
+        return MSA_ERR_CUDA;
+      if (!cuda(cudaStreamWaitEvent(copy_stream, e_a1, 0)) ||
+          !cuda(cudaMemcpyAsync(host->out + static_cast<size_t>(ta) * row, out + static_cast<size_t>(ta) * row,
+                                n_out - static_cast<size_t>(ta) * row * 2, d2h, copy_stream)))
+        return MSA_ERR_CUDA;
+    }
   }
-  if (!cuda(cudaEventRecord(e_done, copy_stream)) || !cuda(cudaStreamWaitEvent(stream, e_done, 0)))
+  // e_start is free again (its wait is enqueued): it marks the end of the copy stream's work
+  if (!cuda(cudaEventRecord(e_start, copy_stream)) || !cuda(cudaStreamWaitEvent(stream, e_start, 0)))
     return MSA_ERR_CUDA;
   return MSA_OK;
 }

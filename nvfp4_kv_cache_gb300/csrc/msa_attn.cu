@@ -1109,15 +1109,17 @@ msa_status msa_attn_token_range(const msa_geometry* geo, const msa_batch* batch,
 }
 
 // Where the host-buffer step splits the attention: the second launch takes the tokens of the
-// persistent grid's last two rounds of units (one unit per SM a round, four units a token), so
-// the split adds no round; 0 = one launch (the small-batch kernel, or fewer than four rounds).
+// persistent grid's last kTailRounds rounds of units (one unit per SM a round, four units a
+// token), so the split adds no round, and the first launch's output (the larger part) copies
+// to the host while the second runs; 0 = one launch (the small-batch kernel, or too few rounds).
+constexpr int kTailRounds = 3;
 int32_t msa_attn_split_token(int32_t T) {
   if (!use_tc_kernel(T)) return 0;
   const int sms = num_sms();
   const int per_round = sms / 4;
   if (per_round <= 0) return 0;
   const int rounds = ceil_div(T, per_round);
-  return rounds < 4 ? 0 : per_round * (rounds - 2);
+  return rounds < 2 * kTailRounds ? 0 : per_round * (rounds - kTailRounds);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 """The decode step from page-locked host buffers (msa_decode_step_host): its output equals
-msa_decode_step's bit for bit, with the attention in one launch or split in two, and the host
-checks reject buffers that are not page-locked."""
+msa_decode_step's bit for bit, copied back (the attention in one launch or split in two) or
+stored into host memory by the attention itself, and the host checks reject buffers that are
+not page-locked."""
 import ctypes
 
 import numpy as np
@@ -16,8 +17,9 @@ CASES = {
     "decode1": dict(seq_lens=[1000, 4096 + 77, 300, 9000 + 5, 129], q_lens=[1] * 5, seed=41),
     # 96 tokens: the many-token kernel, too few rounds to split
     "tc_one_launch": dict(seq_lens=[1500 + 211 * k for k in range(12)], q_lens=[8] * 12, seed=42, hot=3),
-    # 163 tokens (ragged query counts): the many-token kernel in two launches
-    "tc_split": dict(seq_lens=[1200 + 173 * k for k in range(22)], q_lens=[8] * 19 + [1, 3, 7], seed=43, hot=3),
+    # 211 tokens (ragged query counts): the many-token kernel in two launches, split inside a
+    # sequence's tokens
+    "tc_split": dict(seq_lens=[1200 + 173 * k for k in range(28)], q_lens=[8] * 25 + [1, 3, 7], seed=43, hot=3),
 }
 
 
@@ -32,8 +34,9 @@ def pinned(t: torch.Tensor) -> torch.Tensor:
     return t.cpu().contiguous().pin_memory()
 
 
+@pytest.mark.parametrize("direct", [False, True])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_host_step_equals_device_step(msa, case):
+def test_host_step_equals_device_step(msa, case, direct):
     from workloads.device import DeviceLayer
 
     w = W.small(case, **CASES[case])
@@ -50,15 +53,16 @@ def test_host_step_equals_device_step(msa, case):
     # fresh device buffers: everything the step reads comes through the copies
     d = [torch.zeros_like(x) for x in (b.query_start_loc, b.seq_lens, b.block_table, dl.q8, dl.iq8)]
     batch2 = msa.Batch(d[0], d[1], d[2], b.max_q_len, T=b.T)
-    out2 = torch.zeros_like(o["out"])
+    out2 = None if direct else torch.zeros_like(o["out"])
     ws2 = dl.workspace()
     copy = torch.cuda.Stream()
     for _ in range(2):  # the second call reuses every buffer
         msa.msa_decode_step_host(batch2, dl.cache, h[0], h[1], h[2], h[3], h[4], h_out, d[3], d[4], dl.softmax_scale,
-                                 ws2, out2, copy)
+                                 ws2, out2, copy, direct_out=direct)
         torch.cuda.current_stream().synchronize()
         assert msa.msa_read_device_status(ws2) == msa.MSA_OK
         assert torch.equal(h_out.view(torch.int16), ref), case
+        h_out.fill_(7)
 
 
 def test_host_step_rejects_pageable_buffers(msa):
@@ -77,7 +81,16 @@ def test_host_step_rejects_pageable_buffers(msa):
     # the library's own check, past the binding's
     io = msa.msa_host_step_io(*(x.data_ptr() for x in pageable), out_h.data_ptr())
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for flags in (0, msa.MSA_HOST_STEP_DIRECT_OUT):
+        code = msa._lib.msa_decode_step_host(ctypes.byref(msa.GEOMETRY), ctypes.byref(b.c), ctypes.byref(dl.cache.c),
+                                             ctypes.byref(io), msa._ptr(dl.q8), msa._ptr(dl.iq8),
+                                             float(dl.softmax_scale), msa._ptr(ws), ws.numel(), msa._ptr(o["out"]),
+                                             flags, s, s)
+        assert code == msa.MSA_ERR_INVALID_ARG
+    # pinned inputs but a pageable output: the direct mode has nowhere to store
+    pinned_in = [x.pin_memory() for x in pageable]
+    io2 = msa.msa_host_step_io(*(x.data_ptr() for x in pinned_in), out_h.data_ptr())
     code = msa._lib.msa_decode_step_host(ctypes.byref(msa.GEOMETRY), ctypes.byref(b.c), ctypes.byref(dl.cache.c),
-                                         ctypes.byref(io), msa._ptr(dl.q8), msa._ptr(dl.iq8),
-                                         float(dl.softmax_scale), msa._ptr(ws), ws.numel(), msa._ptr(o["out"]), s, s)
+                                         ctypes.byref(io2), msa._ptr(dl.q8), msa._ptr(dl.iq8), float(dl.softmax_scale),
+                                         msa._ptr(ws), ws.numel(), None, msa.MSA_HOST_STEP_DIRECT_OUT, s, s)
     assert code == msa.MSA_ERR_INVALID_ARG

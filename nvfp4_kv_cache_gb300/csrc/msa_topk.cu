@@ -130,6 +130,7 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t k, int lane) {
 
 constexpr int kRowsPerCta = 8;
 constexpr int kSurvivors = 64;
+constexpr int kRegKeys = 32;  // rows of up to 32 x 32 keys are held in registers (one load each)
 constexpr int kCand = kSel - 1;  // candidates per (token, group) and shard: the 15 best non-local blocks
 
 // The 15 largest of the n keys key_at(0 .. n-1) (unique; 0 = none), descending, into res[0..14]
@@ -145,6 +146,31 @@ __device__ void top15_keys(KeyAt key_at, int n, uint64_t* buf, uint64_t* res, in
     k0 = 2 * lane < n ? key_at(2 * lane) : 0ull;
     k1 = 2 * lane + 1 < n ? key_at(2 * lane + 1) : 0ull;
     sorted = true;
+  } else if (n <= 32 * kRegKeys) {
+    // the same filter with the row's keys loaded once, all loads in flight together
+    uint64_t kk[kRegKeys];
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) kk[j] = 32 * j + lane < n ? key_at(32 * j + lane) : 0ull;
+    uint64_t best = 0;
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) best = kk[j] > best ? kk[j] : best;
+    const uint64_t tau = __shfl_sync(0xffffffffu, warp_sort32_desc(best, lane), 14);
+    int count = 0;
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      const bool keep = kk[j] >= tau && kk[j] != 0ull;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      const int pos = count + __popc(m & ((1u << lane) - 1u));
+      if (keep && pos < kSurvivors) buf[pos] = kk[j];
+      count += __popc(m);
+    }
+    __syncwarp();
+    if (count <= kSurvivors) {
+      k0 = 2 * lane < count ? buf[2 * lane] : 0ull;
+      k1 = 2 * lane + 1 < count ? buf[2 * lane + 1] : 0ull;
+      sorted = true;
+    }
+    __syncwarp();
   } else {
     uint64_t best = 0;
     for (int i = lane; i < n; i += 32) {

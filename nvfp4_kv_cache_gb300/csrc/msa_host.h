@@ -16,6 +16,26 @@ inline msa_status launch_status() {
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
+// Launch `kernel` so that it may start while the kernel before it on `stream` finishes
+// (programmatic dependent launch): the kernel must call grid_dependency_wait() before it reads
+// anything the previous kernel writes, and must not write what the previous kernel reads.
+// After anything but a kernel on the stream the launch is ordered as usual.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 inline msa_status check_geometry(const msa_geometry* g) {
   if (g == nullptr) return MSA_ERR_INVALID_ARG;
   if (g->num_q_heads != 64 || g->num_kv_heads != 4 || g->head_dim != 128 || g->index_dim != 128 ||

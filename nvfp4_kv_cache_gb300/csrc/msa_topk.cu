@@ -234,6 +234,7 @@ __device__ __forceinline__ int row_local(const TopkParams& p, int t) {
 __global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
   __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
   __shared__ uint64_t res[kRowsPerCta][kCand];
+  grid_dependency_wait();  // the indexer's scores (this kernel may launch while it finishes)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerCta + warp;  // t * 4 + g
   if (row >= p.T * 4) return;
@@ -329,7 +330,9 @@ extern "C" msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* 
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
-  k_topk<<<ceil_div(batch->T * 4, kRowsPerCta), 32 * kRowsPerCta, 0, stream>>>(p);
+  if (launch_after_previous(k_topk, dim3(ceil_div(batch->T * 4, kRowsPerCta)), dim3(32 * kRowsPerCta), 0, stream, p) !=
+      cudaSuccess)
+    return MSA_ERR_CUDA;
   return launch_status();
 }
 

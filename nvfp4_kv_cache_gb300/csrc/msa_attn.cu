@@ -392,7 +392,8 @@ struct Smem {
   static constexpr int kBars = 2 * kStages + 2 * kVTiles + 2 * 12 + 3;
   static constexpr size_t kOffLut = kOffBar + 8 * 48;
   static constexpr size_t kOffRed = kOffLut + 256 * 8;   // [2][4 warps][16] fp32
-  static constexpr size_t kOffMeta = kOffRed + 2 * 4 * 16 * 4;
+  static constexpr size_t kOffCf = kOffRed + 2 * 4 * 16 * 4;   // [128 softmax threads][16] fp32
+  static constexpr size_t kOffMeta = kOffCf + 128 * 16 * 4;
   static constexpr size_t kOffMisc = kOffMeta + 2 * sizeof(UnitMeta);
   static constexpr size_t kBytes = 1024 + kOffMisc + 64;  // + alignment slack
 };
@@ -400,6 +401,28 @@ static_assert(Smem::kBars <= 48, "barrier area");
 static_assert(Smem::kOffStage % 1024 == 0 && Smem::kOffV % 1024 == 0 && Smem::kOffP % 1024 == 0,
               "swizzled tiles sit on 1024-B boundaries");
 static_assert(Smem::kBytes <= 232448, "shared memory per CTA");
+static_assert(Smem::kOffCf % 16 == 0, "the rescale factors are read as float4");
+
+// O^T(os) *= cf for this thread's lane: the rare path of the lazy reference, out of line so that
+// its registers do not count against the softmax loop
+__device__ __noinline__ void o_rescale(uint32_t taddr, const float4* cfp) {
+#pragma unroll
+  for (int xx = 0; xx < 2; ++xx) {
+    uint32_t o[16];
+    tmem_ld16(taddr + 16 * xx, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h4 = 0; h4 < 4; ++h4) {
+      const float4 f = cfp[h4];
+      o[4 * h4 + 0] = __float_as_uint(__uint_as_float(o[4 * h4 + 0]) * f.x);
+      o[4 * h4 + 1] = __float_as_uint(__uint_as_float(o[4 * h4 + 1]) * f.y);
+      o[4 * h4 + 2] = __float_as_uint(__uint_as_float(o[4 * h4 + 2]) * f.z);
+      o[4 * h4 + 3] = __float_as_uint(__uint_as_float(o[4 * h4 + 3]) * f.w);
+    }
+    tmem_st16(taddr + 16 * xx, o);
+    tmem_wait_st();
+  }
+}
 
 // Op-reduce v[0..15] over the 32 lanes: afterwards lanes 2h and 2h + 1 hold head h's result.
 template <bool kMax>
@@ -852,22 +875,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref[h] = mn;
             l[h] *= cf[h];
           }
+          {  // this thread's copy of the factors (the same in all 128 threads) for the O rescale
+            float4* cfp = reinterpret_cast<float4*>(smem + S::kOffCf) + 4 * kr;
+#pragma unroll
+            for (int h4 = 0; h4 < 4; ++h4) cfp[h4] = make_float4(cf[4 * h4], cf[4 * h4 + 1], cf[4 * h4 + 2], cf[4 * h4 + 3]);
+          }
           // both accumulators *= cf once PV(jg - 1) and PV(jg - 2) have landed (PV(jg) waits for
           // this block's P); one not yet written in this unit is rescaled harmlessly: its first
           // PV of the unit overwrites it
           if (moved && j > 0 && wait_ok(&p_empty[(jg - 1) & 1], static_cast<uint32_t>((jg - 1) >> 1) & 1u) &&
               (j < 2 || wait_ok(&p_empty[jg & 1], (static_cast<uint32_t>(jg >> 1) & 1u) ^ 1u))) {
             tc_fence_after();
-#pragma unroll
-            for (int xx = 0; xx < 2; ++xx) {
-              uint32_t o[16];
-              tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * xx, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * cf[h]);
-              tmem_st16(tmem + lanes + kColO + 32 * os + 16 * xx, o);
-              tmem_wait_st();
-            }
+            o_rescale(tmem + lanes + kColO + 32 * os, reinterpret_cast<const float4*>(smem + S::kOffCf) + 4 * kr);
             tc_fence_before();
           }
         }

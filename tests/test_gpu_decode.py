@@ -112,6 +112,51 @@ def test_standalone_stages_and_splits(msa, splits, case):
     compare_case(w, dl, dict(out=out, scores=o["scores"], sel=sel))
 
 
+@pytest.mark.parametrize("case", ["decode1", "many_tokens"])
+def test_sharp_softmax(msa, case):
+    """softmax_scale 1.0 instead of 1/sqrt(128): logits about 11x wider, so later blocks exceed
+    the first block's maximum by far more than 2^8 (in exp2 units) and the many-token kernel's
+    lazily moved reference must rescale its accumulators (checked on the oracle's scores
+    below); both attention kernels against the oracle at the same scale."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small(case, **CASES[case])
+    dl = DeviceLayer(w, 0)
+    o = dl.outputs()
+    ws = dl.workspace()
+    scale = 1.0
+    msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, scale, ws, o["out"], o["scores"], o["sel"])
+    assert msa.msa_read_device_status(ws) == msa.MSA_OK
+    qsl = w.query_start_loc()
+    sel = o["sel"].cpu().numpy()
+    out = bf16_to_f32(o["out"]).cpu().numpy()
+    moves = 0
+    for b in range(w.B):
+        ql, L = w.q_lens[b], w.seq_lens[b]
+        if ql == 0:
+            continue
+        rows = slice(int(qsl[b]), int(qsl[b]) + ql)
+        gsel = sel[rows]
+        ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(gsel[gsel >= 0]))
+        check_attention(out[rows], ref.attention(gsel, scale), f"seq {b}")
+        # the reference moves: per (token, head), block maxima of s * scale * log2(e) in slot
+        # order, a later block more than 8 above the running reference
+        q = oracle.e4m3_decode(ref.q8).reshape(ql, 64, 128)
+        kvals, kscales = ref.kv[0], ref.kv[1]
+        for t in range(ql):
+            p_tok = L - ql + t
+            for g in range(4):
+                blocks = list(dict.fromkeys(int(x) for x in gsel[t, g] if x >= 0))  # distinct, slot order
+                per_block = [np.arange(128 * k, min(128 * k + 128, L, p_tok + 1)) for k in blocks]
+                keys = np.concatenate(per_block)
+                kd = oracle.e4m3_decode(oracle.dequant_nvfp4(kvals[keys, g], kscales[keys, g]))
+                z = q[t, 16 * g:16 * g + 16] @ kd.T * scale * np.log2(np.e)
+                first = z[:, : len(per_block[0])].max(axis=1)
+                moves += int((z.max(axis=1) > first + 8.0).sum())
+    if case == "many_tokens":
+        assert moves > 0, "the case does not exercise the reference move"
+
+
 def test_topk_on_crafted_scores(msa):
     """Ties, NaN, -inf, -0/+0, fewer than 15 candidates: GPU == the oracle's stable sort."""
     rng = np.random.default_rng(5)

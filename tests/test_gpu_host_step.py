@@ -94,3 +94,44 @@ def test_host_step_rejects_pageable_buffers(msa):
                                          ctypes.byref(io2), msa._ptr(dl.q8), msa._ptr(dl.iq8), float(dl.softmax_scale),
                                          msa._ptr(ws), ws.numel(), None, msa.MSA_HOST_STEP_DIRECT_OUT, s, s)
     assert code == msa.MSA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("direct", [False, True])
+def test_host_step_in_a_cuda_graph(msa, direct):
+    """msa_decode_step_host captured once (both streams, the copies and the kernels) replays with
+    new host contents and equals msa_decode_step on them."""
+    from workloads.device import DeviceLayer
+
+    case = "tc_split"
+    w = W.small(case, **CASES[case])
+    dl = DeviceLayer(w, 0)
+    b = dl.batch
+    h = [pinned(x) for x in (b.query_start_loc, b.seq_lens, b.block_table, dl.q8, dl.iq8)]
+    o = dl.outputs()
+    h_out = torch.zeros(tuple(o["out"].shape), dtype=o["out"].dtype).pin_memory()
+    d = [torch.zeros_like(x) for x in (b.query_start_loc, b.seq_lens, b.block_table, dl.q8, dl.iq8)]
+    batch2 = msa.Batch(d[0], d[1], d[2], b.max_q_len, T=b.T)
+    out2 = None if direct else torch.zeros_like(o["out"])
+    ws2 = dl.workspace()
+    copy = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            msa.msa_decode_step_host(batch2, dl.cache, h[0], h[1], h[2], h[3], h[4], h_out, d[3], d[4],
+                                     dl.softmax_scale, ws2, out2, copy, direct_out=direct)
+    torch.cuda.current_stream().wait_stream(s)
+    for it in range(2):
+        if it == 1:  # new query contents on the host, same graph
+            h[3].copy_(torch.roll(h[3], 1, dims=1))
+            dl.q8.copy_(h[3])
+        ws = dl.workspace()
+        msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"])
+        torch.cuda.synchronize()
+        ref = o["out"].view(torch.int16).cpu()
+        h_out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert msa.msa_read_device_status(ws2) == msa.MSA_OK
+        assert torch.equal(h_out.view(torch.int16), ref), it

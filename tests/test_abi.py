@@ -71,3 +71,37 @@ def test_host_checks_without_gpu(lib):
                   ctypes.c_void_p]
     assert g(ctypes.byref(bad), None, None, None, None, None) == 2
     assert g(ctypes.byref(good), None, None, None, None, None) == 1
+
+
+def test_host_step_checks_without_gpu(lib):
+    """msa_decode_step_host rejects bad geometry, a missing batch or host description and
+    unknown flags before it makes any CUDA call."""
+
+    class Geo(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int32) for n in "abcdefgh"]
+
+    class Batch(ctypes.Structure):
+        _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("qsl", ctypes.c_void_p),
+                    ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("maxb", ctypes.c_int32),
+                    ("max_q_len", ctypes.c_int32)]
+
+    class Cache(ctypes.Structure):
+        _fields_ = [("kv", ctypes.c_void_p), ("ix", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                    ("pages", ctypes.c_int32)]
+
+    f = lib.msa_decode_step_host
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    bad = Geo(64, 8, 128, 128, 128, 16, 1, 0)
+    good = Geo(64, 4, 128, 128, 128, 16, 1, 0)
+    dummy = ctypes.c_void_p(0x1000)  # never dereferenced: the checks stop before any access
+    batch = Batch(1, 1, dummy, dummy, dummy, 1, 1)
+    cache = Cache(dummy, dummy, 0, 1)
+    args = lambda geo, b, c, host, flags: (ctypes.byref(geo), b, c, host, None, None, 0.1, dummy, 1 << 20, None,
+                                           flags, None, None)
+    assert f(*args(bad, ctypes.byref(batch), ctypes.byref(cache), None, 0)) == 2          # unsupported geometry
+    assert f(*args(good, None, ctypes.byref(cache), None, 0)) == 1                        # no batch
+    assert f(*args(good, ctypes.byref(batch), ctypes.byref(cache), None, 0)) == 1         # no host description
+    io = (ctypes.c_void_p * 6)(*([0x2000] * 6))
+    assert f(*args(good, ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(io), 4)) == 1  # unknown flag

@@ -352,7 +352,8 @@ typedef struct msa_host_step_io {
 /* Flags of msa_decode_step_host. */
 enum { MSA_HOST_STEP_DIRECT_OUT = 1 };
 
-/* msa_decode_step from host buffers: copies `host`'s inputs into the device buffers (batch's
+/* msa_decode_step from host buffers (this library's own entry point: the pages run the step
+ * on device-resident inputs): copies `host`'s inputs into the device buffers (batch's
  * three arrays, q, index_q), runs the step, and delivers the output into host->out, with the
  * copies on `copy_stream` and `stream` overlapping the kernels. The block table goes first on
  * the copy stream while the other batch arrays and the index queries go on `stream`; the

@@ -1,0 +1,48 @@
+"""The bench's algorithmic byte model (host logic, no GPU): the index scan counts every valid
+token of every distinct page once and every query's index query; the step adds each (sequence,
+group)'s distinct selected valid tokens x 144 B plus per query token its Q and bf16 output.
+Checked against counts made by hand on small workloads, shared pages included."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_index_bytes_counts_each_page_once():
+    # 300 tokens (3 pages, last 44 valid), 129 (2 pages, last 1 valid); NVFP4 index: 72 B a token
+    w = W.make("bytes", [300, 129], [2, 1], seed=5, identity=True)
+    assert bench.index_bytes(w, 0) == (300 + 129) * 72 + 3 * 512
+    f = W.make("bytes8", [300, 129], [2, 1], seed=5, identity=True, index_dtype=W.INDEX_FP8)
+    assert bench.index_bytes(f, 0) == (300 + 129) * 128 + 3 * 512
+    # a sequence with no query tokens is not scanned
+    z = W.make("bytes0", [300, 129], [2, 0], seed=5, identity=True)
+    assert bench.index_bytes(z, 0) == 300 * 72 + 2 * 512
+
+
+def test_index_bytes_shared_prefix_pages():
+    # two sequences share a 256-token (2-page) prefix: those pages are read once
+    w = W.make("share", [256 + 10, 256 + 130], [1, 1], seed=6, prefix_len=256, prefix_seqs=2)
+    assert w.block_table[0, 0] == w.block_table[1, 0] and w.block_table[0, 1] == w.block_table[1, 1]
+    assert bench.index_bytes(w, 0) == (256 + 10 + 130) * 72 + 2 * 512
+
+
+def test_step_bytes_distinct_selected_tokens():
+    w = W.make("step", [300, 129], [2, 1], seed=7, identity=True)
+    T = w.T
+    sel = -np.ones((T, 4, 16), np.int32)
+    # sequence 0 (tokens 0, 1): group 0 selects blocks {2, 0} and {2, 1}: distinct {0, 1, 2} =
+    # 128 + 128 + 44 tokens; group 1 selects block 2 twice (44 tokens); groups 2, 3 nothing
+    sel[0, 0, :2] = [2, 0]
+    sel[1, 0, :2] = [2, 1]
+    sel[0, 1, 0] = 2
+    sel[1, 1, 0] = 2
+    # sequence 1 (token 2): group 3 selects block 1 (1 valid token) and block 0
+    sel[2, 3, :2] = [1, 0]
+    kv = ((128 + 128 + 44) + 44 + (1 + 128)) * 144
+    assert bench.step_bytes(w, 0, sel) == bench.index_bytes(w, 0) + kv + T * (8192 + 16384)

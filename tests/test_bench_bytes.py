@@ -46,3 +46,22 @@ def test_step_bytes_distinct_selected_tokens():
     sel[2, 3, :2] = [1, 0]
     kv = ((128 + 128 + 44) + 44 + (1 + 128)) * 144
     assert bench.step_bytes(w, 0, sel) == bench.index_bytes(w, 0) + kv + T * (8192 + 16384)
+
+
+def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic is the committed DRAM count only while the kernel source it was taken
+    from is unchanged (its hash), else None."""
+    import hashlib
+    import json
+
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles" / "traffic.json").write_text(
+        json.dumps({"k@w": {"source_sha": sha, "bytes_per_launch": 1234}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k@w", "k.cu") == 1234
+    assert bench.recorded_traffic("other", "k.cu") is None
+    src.write_text("kernel v2\n")
+    assert bench.recorded_traffic("k@w", "k.cu") is None

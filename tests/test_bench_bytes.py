@@ -65,3 +65,22 @@ def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("other", "k.cu") is None
     src.write_text("kernel v2\n")
     assert bench.recorded_traffic("k@w", "k.cu") is None
+
+
+def test_clock_sampler_parses_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """The bench's clock record from nvidia-smi's CSV lines: median SM clock, the maximum, and
+    every throttle reason seen Active (a fake nvidia-smi on PATH stands in for the real one)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '1980, 2070, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '2010, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo 'garbage line'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ.get("PATH", ""))
+    c = bench.ClockSampler(0)
+    rec = c.stop()
+    assert rec is not None
+    assert rec["sm_mhz"] == 2010.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] == 3

@@ -21,6 +21,7 @@ indexer, and the attention storing the output into the pinned host buffer);
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import math
@@ -97,6 +98,13 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+        if self.proc is not None:
+            atexit.register(self._end)  # an exception before stop() must not leave it running
+
+    def _end(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
+            self.proc.wait()
 
     def stop(self):
         if self.proc is None:

@@ -86,15 +86,23 @@ def step_bytes(w: W.Workload, layer: int, sel: np.ndarray) -> int:
 
 
 class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 100 ms, each stamped with the time
+    nvidia-smi took it; `stop(window)` summarises every sample and, separately, those inside
+    the given (start, end) host-clock window (the timed loop, which can be shorter than one
+    sampling period: the samples nearest to it are then the ones reported for it)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
     def __init__(self, index: int):
         self.proc = None
         self.index = index
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -106,7 +114,40 @@ class ClockSampler:
             self.proc.kill()
             self.proc.wait()
 
-    def stop(self):
+    @staticmethod
+    def _stamp(text: str):
+        """nvidia-smi's local-time stamp ("2026/12/02 13:25:00.123") as epoch seconds."""
+        try:
+            return time.mktime(time.strptime(text.split(".")[0], "%Y/%m/%d %H:%M:%S")) + (
+                float("0." + text.split(".")[1]) if "." in text else 0.0)
+        except (ValueError, IndexError):
+            return None
+
+    @classmethod
+    def summarise(cls, samples):
+        if not samples:
+            return None
+        reasons = sorted({n for s in samples for n in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in samples), "sm_max_mhz": max(s[2] for s in samples),
+                "reasons": reasons, "samples": len(samples)}
+
+    @classmethod
+    def parse(cls, out: str):
+        """(stamp or None, sm MHz, max MHz, active reasons) per well-formed line."""
+        samples = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            act = {n for n, v in zip(cls.REASONS, f[4:8]) if v.lower() == "active"}
+            samples.append((cls._stamp(f[0]), sm, mx, act))
+        return samples
+
+    def stop(self, window=None):
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -116,24 +157,21 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        mhz, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                mhz.append(float(f[0]))
-                mx = max(mx, float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not mhz:
-            return None
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(mhz)}
+        samples = self.parse(out)
+        rec = self.summarise(samples)
+        if rec is None or window is None:
+            return rec
+        t0, t1 = window
+        stamped = [s for s in samples if s[0] is not None]
+        inside = [s for s in stamped if t0 <= s[0] <= t1]
+        if not inside and stamped:  # the loop fell between two samples: the two around it
+            before = [s for s in stamped if s[0] < t0]
+            after = [s for s in stamped if s[0] > t1]
+            inside = before[-1:] + after[:1]
+        rec["timed_loop"] = self.summarise(inside)
+        if rec["timed_loop"] is not None:
+            rec["timed_loop"]["loop_s"] = t1 - t0
+        return rec
 
 
 def recorded_traffic(kernel: str, source: str):
@@ -300,6 +338,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    t_epoch = time.time()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
@@ -402,9 +441,10 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
 
     # clocks sampled from the start of the timed loop through the stage, exact-indexer, prefill and
     # end-to-end loops that follow it (the timed loop alone is shorter than the sampling period)
-    clk = clocks.stop() if clocks else None
+    clk = clocks.stop((t_epoch, t_epoch + wall)) if clocks else None
     if clk is not None:
-        clk["window"] = "timed loop through the end-to-end loops"
+        clk["window"] = ("all samples: the timed loop through the end-to-end loops; timed_loop: the samples "
+                         "inside the timed loop, or the two around it when it fell between samples")
     if rank != 0:
         return
     peak_gbs, peak_kind = peaks()

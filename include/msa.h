@@ -23,9 +23,12 @@
  *
  * Conventions for every function:
  *  - Pointers named device are CUDA device pointers; structs are passed by host pointer and
- *    read during the call only. The caller allocates and owns every buffer; the library
- *    allocates no memory and keeps no state between calls (it is re-entrant). Buffers must
- *    not alias unless stated.
+ *    read during the call only. The caller allocates and owns every buffer, and the library
+ *    allocates no device memory of its own. It keeps exactly two pieces of state between
+ *    calls, each documented where it is declared: msa_decode_step_host keeps a few CUDA
+ *    events per host thread and device, and msa_sparse_attn_decode_noalloc uses one
+ *    file-scope device array shared by all its calls. Every other entry point keeps no state
+ *    and is re-entrant. Buffers must not alias unless stated.
  *  - Every call is asynchronous on the given stream and never synchronises the host, except
  *    msa_read_device_status.
  *  - Problems found on the host (null pointers, sizes, alignment, unsupported geometry)

@@ -68,19 +68,43 @@ def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
 
 
 def test_clock_sampler_parses_a_fake_nvidia_smi(tmp_path, monkeypatch):
-    """The bench's clock record from nvidia-smi's CSV lines: median SM clock, the maximum, and
-    every throttle reason seen Active (a fake nvidia-smi on PATH stands in for the real one)."""
+    """The bench's clock record from nvidia-smi's CSV lines: median SM clock, the maximum, every
+    throttle reason seen Active, and the samples inside the timed loop's window (a fake
+    nvidia-smi on PATH stands in for the real one)."""
+    import time
+
     fake = tmp_path / "nvidia-smi"
+    marker = tmp_path / "printed"
     fake.write_text("#!/bin/sh\n"
-                    "echo '2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
-                    "echo '1980, 2070, 0x4, Not Active, Not Active, Not Active, Active'\n"
-                    "echo '2010, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '2026/12/02 10:00:00.100, 2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '2026/12/02 10:00:00.200, 1980, 2070, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '2026/12/02 10:00:00.300, 2010, 2070, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
                     "echo 'garbage line'\n"
+                    f"touch '{marker}'\n"
                     "exec sleep 30\n")
     fake.chmod(0o755)
     monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ.get("PATH", ""))
     c = bench.ClockSampler(0)
-    rec = c.stop()
+    t_end = time.time() + 20
+    while not marker.exists() and time.time() < t_end:  # the fake has printed its lines
+        time.sleep(0.01)
+    assert marker.exists()
+    t0 = time.mktime(time.strptime("2026/12/02 10:00:00", "%Y/%m/%d %H:%M:%S"))
+    rec = c.stop((t0 + 0.15, t0 + 0.25))
     assert rec is not None
     assert rec["sm_mhz"] == 2010.0 and rec["sm_max_mhz"] == 2070.0
     assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] == 3
+    assert rec["timed_loop"]["samples"] == 1 and rec["timed_loop"]["sm_mhz"] == 1980.0
+    assert rec["timed_loop"]["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_window_between_samples():
+    """A timed loop shorter than the sampling period: the two samples around it stand for it."""
+    import time
+
+    t0 = time.mktime(time.strptime("2026/12/02 10:00:00", "%Y/%m/%d %H:%M:%S"))
+    out = "\n".join(f"2026/12/02 10:00:00.{ms:03d}, {mhz}, 2070, 0x0, Not Active, Not Active, Not Active, Not Active"
+                    for ms, mhz in ((100, 2070), (200, 1500), (300, 2000), (400, 1000)))
+    s = bench.ClockSampler.parse(out)
+    assert [x[1] for x in s] == [2070.0, 1500.0, 2000.0, 1000.0]
+    assert abs(s[1][0] - (t0 + 0.2)) < 1e-6

@@ -478,7 +478,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     line = {
         "metric": METRIC, "value": ms_max * 1e3, "unit": "us/layer-step", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 MMA, fp32 accumulate/softmax, f16 PV", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3 MMA, fp32 accumulate/softmax, e4m3 PV (P as hi + lo E4M3 parts)", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "seq_len": max(w.seq_lens), "q_len": max(w.q_lens), "T": T,
                    "index_dtype": "nvfp4" if w.layers[0].index_dtype == 0 else "fp8", "layers": 1,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

@@ -258,8 +258,10 @@ size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, in
  * of token t (group g = h / 16): the keys are the cache positions j <= p_t of the distinct
  * blocks listed in sel[t][g][0..15] (entries < 0 ignored); z_j = softmax_scale * q . k_j with
  * K dequantised to E4M3; out = sum_j softmax(z)_j v_j with V dequantised to E4M3; written
- * as bf16. QK^T runs as an FP8 MMA with fp32 accumulation; the softmax is fp32; PV runs
- * with P in f16 and V widened exactly from E4M3 to f16.
+ * as bf16. QK^T runs as an FP8 MMA with fp32 accumulation; the softmax is fp32. For batches
+ * of up to 76 query tokens PV runs with P in f16 and V widened exactly from E4M3 to f16; for
+ * larger batches it runs as an FP8 MMA on the E4M3 V with P split into two E4M3 parts,
+ * hi = E4M3(P) and lo = E4M3(16 (P - hi)), so P is carried to within 2^-8 of itself.
  *   q          [T][64][128] E4M3, device
  *   sel        [T][4][16] int32, device
  *   num_splits 0 = automatic; else 1..16 splits of each (sequence, group)'s block list,

@@ -334,262 +334,185 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnParams p, co
 }
 
 // ------------------------------------------------------------------------------------------
-// Batches of many tokens, on the 5th-generation tensor cores: a persistent CTA of 12 warps per
-// SM walks units of one (query token, group, split) each. The keys of a block are the M = 128 rows of both tcgen05 MMAs, so the
-// accumulators live in TMEM and the CUDA cores only dequantise and run the softmax:
-//  * S^T = K Q^T: kind::f8f6f4, A = the block's 128 x 128 E4M3 K tile in TMEM (the K dequant
-//    threads store their key row with tcgen05.st), B = the token's 16 x 128 E4M3 query tile
-//    (K-major, 128-byte swizzle, one tensor copy), N = 16 heads, into a ring of two TMEM
-//    score buffers; one warp issues these;
-//  * O^T += V^T P^T: kind::f16, A = the block's V tile as f16 (E4M3 -> f16 exact) in shared
-//    memory, MN-major with 128-byte swizzle, B = P^T (16 heads x 128 keys, K-major, 128-byte
-//    swizzle), N = 16, into one TMEM accumulator of 128 dims x 16 heads; another warp issues
-//    these (an MMA costs ~80 cycles of issue, so S and PV each get their own issuer);
-//  * two groups of four warps, thread = key = TMEM lane: K and V dequant, and softmax. A
-//    softmax thread reads its key's 16 head scores and writes P = exp2(s - m). The reference
-//    maximum m of a head only moves when some score of a block exceeds it by more than 2^8 (a
-//    vote of the four softmax warps), so P <= 256 in f16, the block maximum is reduced across
-//    the 128 threads only then, and O^T is rescaled in TMEM only then (after the PV MMA in
-//    flight has landed);
-//  * the output is O^T / l, the per-head sum l reduced across the 128 threads once.
+// Batches of many tokens, on the 5th-generation tensor cores: a persistent CTA per SM runs three
+// worker warpgroups side by side, each owning whole units (one unit = one (query token, group,
+// split): the token's selected blocks of the group) from start to finish, so a unit's dequant,
+// softmax and output never change hands between warp groups. Per block of 128 keys, the four
+// warps of a warpgroup (thread = key row):
+//  * dequantise the block's K rows from NVFP4 to E4M3 straight into a TMEM tile (tcgen05.st),
+//    the A operand of S^T = K Q^T (kind::f8f6f4, N = 16 heads, keys on the M = 128 rows);
+//  * dequantise its V rows to E4M3 over the stage buffer the copy brought them in (in place:
+//    every raw row is read before the first E4M3 row is written), the MN-major A operand of
+//    O^T += V^T P^T (kind::f8f6f4, N = 32);
+//  * run the softmax on S^T: P = exp2(s c - m) with m a per-head reference that only moves when
+//    a score exceeds it by more than 2^8 (a vote of the four warps; the first block of a unit
+//    always sets it), so P <= 256 fits E4M3; P is split into hi = E4M3(P) and lo =
+//    E4M3(16 (P - hi)) (error <= 2^-8 P), stored as rows 0..15 and 16..31 of the 32 x 128 B
+//    operand P^T, so one MMA per 32 keys accumulates both parts of the sum into two column
+//    groups of O^T;
+//  * at the unit's end, read O^T (thread = dim), add hi + lo / 16, divide by the per-head sum.
+// The softmax thread takes S^T with the 16x256b TMEM load shape (four keys x four heads a
+// thread), so its four keys of one head are four consecutive key positions of P^T, stored as one
+// 32-bit word: the K rows go to TMEM lanes in an order that makes this hold (kappa below) and
+// the V rows go to the P^T key position of their key.
+// One issuer warp per warpgroup issues its MMAs and its tensor copies (a 3-deep ring of K+V
+// stages of one (page, group) each, and the unit's query tile); one warp resolves units (the
+// selected blocks, their pages) into a ring of records for the three warpgroups.
 namespace tc {
 
-constexpr int kWarpProd = 0, kWarpMmaS = 1, kWarpMmaO = 2;  // PV issuers: warps 2 (even blocks), 3 (odd)
-constexpr int kWarpDq = 4, kWarpSm = 12;                    // two dequant groups, one softmax group
-constexpr int kThreads = 32 * 16;
-constexpr int kStages = 4;                                   // NVFP4 K+V stage ring
-constexpr int kStageBytes = 2 * kRegion;                     // K region then V region of one (page, group)
-constexpr int kQTile = kHPG * kD;                            // 16 heads x 128 E4M3
-constexpr int kVTile = kBS * kD * 2;                         // 128 keys x 128 f16
-constexpr int kPTile = kHPG * kBS * 2;                       // 16 heads x 128 keys f16
-constexpr int kVTiles = 3;                                   // f16 V tile ring
-constexpr uint32_t kVLbo = 16384;                            // V tile: the two 64-dim atom columns
-constexpr uint32_t kVSbo = 1024;                             //         8-key groups
-constexpr float kRescaleLog2 = 8.0f;                         // m moves when a score exceeds it by this
-constexpr int kBarWork = 4;                                  // named barrier of the softmax warps
-// TMEM columns: K tiles [2] 0..63, S^T [2] 64..95, O^T [2 unit parities][2 block parities] 96..159
-constexpr uint32_t kColK = 0, kColS = 64, kColO = 96;
-constexpr int kTmemCols = 256;
+constexpr int kWgs = 3;                               // worker warpgroups (warps 4w .. 4w + 3)
+constexpr int kWarpIss = 4 * kWgs;                    // warp 12 + w: issuer of warpgroup w
+constexpr int kWarpRes = kWarpIss + kWgs;             // warp 15: unit resolver, TMEM owner
+constexpr int kThreads = 32 * (kWarpRes + 1);         // 512
+constexpr int kStages = 3;                            // K+V stage ring of a warpgroup
+constexpr int kStageBytes = 2 * kRegion;              // 18,432 (the E4M3 V tile is written over it)
+constexpr int kQTile = kHPG * kD;                     // 16 heads x 128 E4M3
+constexpr int kPTile = 2 * kHPG * kBS;                // P^T: 32 rows (hi, lo) x 128 keys E4M3
+constexpr int kMeta = 4;                              // unit records in a warpgroup's ring
+constexpr size_t kWgBytes = static_cast<size_t>(kStages) * kStageBytes + kPTile + 2 * kQTile;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kWgCols = 128;                     // TMEM columns of a warpgroup:
+constexpr uint32_t kColK = 0, kColS = 32, kColO = 64;  // K tile (32), S^T (16), O^T [2 parities] (2 x 32)
+constexpr float kRescaleLog2 = 8.0f;                  // P <= 2^8 < 448, the E4M3 maximum
+constexpr float kLoScale = 16.0f;                     // P^T lo rows hold kLoScale (P - hi)
+constexpr uint32_t kLoScale2 = 0x4C004C00u;           // f16x2 {16, 16}
+constexpr int kBarVote = 1, kBarX = 4;                // named barriers 1 + w and 4 + w of warpgroup w
+static_assert(kWgBytes % 1024 == 0 && kStageBytes % 1024 == 0 && kPTile % 1024 == 0 && kQTile % 1024 == 0,
+              "swizzled tiles sit on 1024-B boundaries");
 
-// One unit of work = one (query token, group, split); a CTA walks units c, c + G, c + 2G, ...
-// The producer resolves each unit's selected blocks into a 2-deep ring of these records.
+// The key row of a 32-row quarter that TMEM lane `lam` (0..31) of the K tile holds:
+// 8a + rotl3((b - 2a) mod 8) for lam = 8a + b. The softmax thread t reads lanes t/4 + 8i
+// (i = 0..3) and stores them as P^T key positions 4 (t/4) + i; with this order both the K rows
+// (thread lam reads row kappa(lam)) and the V rows (thread mu reads the row whose key position
+// is mu) are read from the staged page without shared-memory bank conflicts.
+__device__ __forceinline__ int kappa(int lam) {
+  const int a = lam >> 3, x = ((lam & 7) - 2 * a) & 7;
+  return 8 * a + (((x << 1) | (x >> 2)) & 7);
+}
+
 struct UnitMeta {
   int t, g, split, p_tok;  // token, group, split, the token's position
-  int n, valid, bad;       // blocks of this split; 0 = batch description inconsistent; a bad entry
+  int n;                   // blocks of this split (>= 1); -1 ends the warpgroup's work
+  int pad[3];
   int blk[kSel];           // the split's blocks (block ids), in slot order
   int phys[kSel];          // and their pages
-  int pad;
 };
 
 struct Smem {
-  static constexpr size_t kOffQ = 0;                                                     // 2 x 2 KB
-  static constexpr size_t kOffStage = 1024 * 4;                                           // 4 x 18 KB
-  static constexpr size_t kOffV = kOffStage + static_cast<size_t>(kStages) * kStageBytes;  // 3 x 32 KB
-  static constexpr size_t kOffP = kOffV + kVTiles * static_cast<size_t>(kVTile);          // 2 x 4 KB
-  static constexpr size_t kOffBar = kOffP + 2 * static_cast<size_t>(kPTile);
-  // st_full, st_empty [kStages]; v_full, v_empty [kVTiles]; ka_full, ka_empty, s_full, s_empty,
-  // p_full, p_empty, q_full, q_empty, o_final, o_free, meta_full, meta_empty [2]; fin_s; fin_o [2]
-  static constexpr int kBars = 2 * kStages + 2 * kVTiles + 2 * 12 + 3;
-  static constexpr size_t kOffLut = kOffBar + 8 * 48;
-  static constexpr size_t kOffRed = kOffLut + 256 * 8;   // [2][4 warps][16] fp32
-  static constexpr size_t kOffCf = kOffRed + 2 * 4 * 16 * 4;   // [128 softmax threads][16] fp32
-  static constexpr size_t kOffMeta = kOffCf + 128 * 16 * 4;
-  static constexpr size_t kOffMisc = kOffMeta + 2 * sizeof(UnitMeta);
+  static constexpr size_t kOffWg = 0;                                             // [3] x 62 KB
+  static constexpr size_t kOffBar = kOffWg + kWgs * kWgBytes;
+  // per warpgroup: st_full[3], q_full[2], q_empty[2], ka_full, s_full, pv_ready, pv_done,
+  // o_free[2], meta_full[4], meta_empty[4], fin
+  static constexpr int kBarsPerWg = kStages + 2 + 2 + 4 + 2 + 2 * kMeta + 1;
+  static constexpr size_t kOffLut = kOffBar + 8 * ((kBarsPerWg * kWgs + 1) & ~1);
+  static constexpr size_t kOffRed = kOffLut + 256 * 8;              // [3][2][4 warps][16] fp32 block maxima
+  static constexpr size_t kOffMref = kOffRed + kWgs * 2 * 64 * 4;   // [3][2][16] fp32 reference maxima
+  static constexpr size_t kOffRedL = kOffMref + kWgs * 2 * 16 * 4;  // [3][4 warps][16] fp32 sums
+  static constexpr size_t kOffMeta = kOffRedL + kWgs * 64 * 4;
+  static constexpr size_t kOffQsl = kOffMeta + kWgs * kMeta * sizeof(UnitMeta);
+  static constexpr size_t kOffMisc = kOffQsl + 4 * (kMaxB + 4);
   static constexpr size_t kBytes = 1024 + kOffMisc + 64;  // + alignment slack
 };
-static_assert(Smem::kBars <= 48, "barrier area");
-static_assert(Smem::kOffStage % 1024 == 0 && Smem::kOffV % 1024 == 0 && Smem::kOffP % 1024 == 0,
-              "swizzled tiles sit on 1024-B boundaries");
 static_assert(Smem::kBytes <= 232448, "shared memory per CTA");
-static_assert(Smem::kOffCf % 16 == 0, "the rescale factors are read as float4");
-
-// O^T(os) *= cf for this thread's lane: the rare path of the lazy reference, out of line so that
-// its registers do not count against the softmax loop
-__device__ __noinline__ void o_rescale(uint32_t taddr, const float4* cfp) {
-#pragma unroll
-  for (int xx = 0; xx < 2; ++xx) {
-    uint32_t o[16];
-    tmem_ld16(taddr + 16 * xx, o);
-    tmem_wait_ld();
-#pragma unroll
-    for (int h4 = 0; h4 < 4; ++h4) {
-      const float4 f = cfp[h4];
-      o[4 * h4 + 0] = __float_as_uint(__uint_as_float(o[4 * h4 + 0]) * f.x);
-      o[4 * h4 + 1] = __float_as_uint(__uint_as_float(o[4 * h4 + 1]) * f.y);
-      o[4 * h4 + 2] = __float_as_uint(__uint_as_float(o[4 * h4 + 2]) * f.z);
-      o[4 * h4 + 3] = __float_as_uint(__uint_as_float(o[4 * h4 + 3]) * f.w);
-    }
-    tmem_st16(taddr + 16 * xx, o);
-    tmem_wait_st();
-  }
-}
-
-// Op-reduce v[0..15] over the 32 lanes: afterwards lanes 2h and 2h + 1 hold head h's result.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  float a8[8], a4[4], a2[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {  // keep heads 8..15 in lanes with bit 4 set
-    const float send = u16 ? v[i] : v[i + 8], keep = u16 ? v[i + 8] : v[i];
-    a8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = u8 ? a8[i] : a8[i + 4], keep = u8 ? a8[i + 4] : a8[i];
-    a4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = u4 ? a4[i] : a4[i + 2], keep = u4 ? a4[i + 2] : a4[i];
-    a2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  const float send = u2 ? a2[0] : a2[1], keep = u2 ? a2[1] : a2[0];
-  const float a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
-}
-
-// Op-reduce v[0..15] over the 128 worker threads into out[0..15] (the same in every thread).
-// red: [4][16] fp32 shared scratch, not reused before every worker has passed the next call's
-// barrier (the caller alternates two of them).
-template <bool kMax>
-__device__ __forceinline__ void group_reduce16(const float (&v)[16], float (&out)[16], float* red, int wq, int lane) {
-  const float r = warp_reduce16<kMax>(v, lane);
-  if ((lane & 1) == 0) red[wq * 16 + (lane >> 1)] = r;
-  named_barrier(kBarWork, 128);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float4 x0 = *reinterpret_cast<const float4*>(red + 4 * c);
-    const float4 x1 = *reinterpret_cast<const float4*>(red + 16 + 4 * c);
-    const float4 x2 = *reinterpret_cast<const float4*>(red + 32 + 4 * c);
-    const float4 x3 = *reinterpret_cast<const float4*>(red + 48 + 4 * c);
-    if (kMax) {
-      out[4 * c + 0] = fmaxf(fmaxf(x0.x, x1.x), fmaxf(x2.x, x3.x));
-      out[4 * c + 1] = fmaxf(fmaxf(x0.y, x1.y), fmaxf(x2.y, x3.y));
-      out[4 * c + 2] = fmaxf(fmaxf(x0.z, x1.z), fmaxf(x2.z, x3.z));
-      out[4 * c + 3] = fmaxf(fmaxf(x0.w, x1.w), fmaxf(x2.w, x3.w));
-    } else {
-      out[4 * c + 0] = (x0.x + x1.x) + (x2.x + x3.x);
-      out[4 * c + 1] = (x0.y + x1.y) + (x2.y + x3.y);
-      out[4 * c + 2] = (x0.z + x1.z) + (x2.z + x3.z);
-      out[4 * c + 3] = (x0.w + x1.w) + (x2.w + x3.w);
-    }
-  }
-}
+static_assert(Smem::kOffRed % 16 == 0 && Smem::kOffMref % 16 == 0 && Smem::kOffRedL % 16 == 0, "float4 reads");
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const AttnParams p, const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map) {
   using S = Smem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  uint64_t* st_full = bars;
-  uint64_t* st_empty = st_full + kStages;
-  uint64_t* v_full = st_empty + kStages;
-  uint64_t* v_empty = v_full + kVTiles;
-  uint64_t* ka_full = v_empty + kVTiles;
-  uint64_t* ka_empty = ka_full + 2;
-  uint64_t* s_full = ka_empty + 2;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 2;
-  uint64_t* q_full = p_empty + 2;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* o_final = q_empty + 2;
-  uint64_t* o_free = o_final + 2;
-  uint64_t* meta_full = o_free + 2;
-  uint64_t* meta_empty = meta_full + 2;
-  uint64_t* fin_s = meta_empty + 2;
-  uint64_t* fin_o = fin_s + 1;
   uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
-  float* red = reinterpret_cast<float*>(smem + S::kOffRed);
   UnitMeta* metas = reinterpret_cast<UnitMeta*>(smem + S::kOffMeta);
+  int* qsl_s = reinterpret_cast<int*>(smem + S::kOffQsl);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int units = p.nt * 4 * p.splits;
-  constexpr int kMetaUsers = 15;  // the S and two PV issuers, two dequant groups and the softmax group
+  // this warp's warpgroup (workers and issuers; the resolver serves all three)
+  const int w = warp < kWarpIss ? (warp >> 2) : (warp < kWarpRes ? warp - kWarpIss : 0);
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + S::kOffBar) + S::kBarsPerWg * w;
+  uint64_t* st_full = wbar;
+  uint64_t* q_full = st_full + kStages;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* ka_full = q_empty + 2;
+  uint64_t* s_full = ka_full + 1;
+  uint64_t* pv_ready = s_full + 1;
+  uint64_t* pv_done = pv_ready + 1;
+  uint64_t* o_free = pv_done + 1;
+  uint64_t* meta_full = o_free + 2;
+  uint64_t* meta_empty = meta_full + kMeta;
+  uint64_t* fin = meta_empty + kMeta;
+  uint8_t* wgb = smem + S::kOffWg + static_cast<size_t>(w) * kWgBytes;
+  uint8_t* ptile = wgb + static_cast<size_t>(kStages) * kStageBytes;
+  uint8_t* qtile = ptile + kPTile;
+  UnitMeta* wmeta = metas + kMeta * w;
 
   // ---- prologue --------------------------------------------------------------------------
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&st_full[i], 1);
-      mbar_init(&st_empty[i], 4);  // the dequant group of the stage's blocks
+    for (int x = 0; x < kWgs; ++x) {
+      uint64_t* b = reinterpret_cast<uint64_t*>(smem + S::kOffBar) + S::kBarsPerWg * x;
+      for (int i = 0; i < kStages; ++i) mbar_init(b + i, 1);              // st_full
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(b + kStages + i, 1);                                     // q_full
+        mbar_init(b + kStages + 2 + i, 1);                                 // q_empty (commit)
+      }
+      mbar_init(b + kStages + 4, 4);                                       // ka_full: the 4 workers
+      mbar_init(b + kStages + 5, 1);                                       // s_full (commit)
+      mbar_init(b + kStages + 6, 4);                                       // pv_ready
+      mbar_init(b + kStages + 7, 1);                                       // pv_done (commit)
+      for (int i = 0; i < 2; ++i) mbar_init(b + kStages + 8 + i, 4);       // o_free
+      for (int i = 0; i < kMeta; ++i) {
+        mbar_init(b + kStages + 10 + i, 1);                                // meta_full (resolver)
+        mbar_init(b + kStages + 10 + kMeta + i, 4);                        // meta_empty (workers)
+      }
+      mbar_init(b + kStages + 10 + 2 * kMeta, 1);                          // fin (commit)
     }
-    for (int i = 0; i < kVTiles; ++i) {
-      mbar_init(&v_full[i], 4);
-      mbar_init(&v_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ka_full[i], 4);
-      mbar_init(&ka_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&p_empty[i], 1);
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
-      mbar_init(&o_final[i], 2);  // both PV issuers
-      mbar_init(&o_free[i], 4);
-      mbar_init(&meta_full[i], 1);
-      mbar_init(&meta_empty[i], kMetaUsers);
-    }
-    mbar_init(fin_s, 1);
-    mbar_init(fin_o, 1);
-    mbar_init(fin_o + 1, 1);
     fence_mbar_init();
     *abort_flag = 0;
   }
-  if (warp == kWarpMmaS) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kWarpRes) tmem_alloc(tmem_slot, kTmemCols);
   build_dequant_lut(lut, tid, kThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tw = tmem + kWgCols * static_cast<uint32_t>(w);
   bool ok = true;
   auto give_up = [&]() {
-    if (lane == 0) {
-      if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-      *abort_flag = 1;
-    }
+    if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+    *abort_flag = 1;
   };
-  // a give-up stops this warp's work at once; every later wait is skipped
-  auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+  auto wait1 = [&](uint64_t* bar, uint32_t parity) {  // one thread's bounded wait
     if (!ok) return false;
-    ok = warp_wait(bar, parity, abort_flag);
+    ok = mbar_wait(bar, parity, abort_flag);
     if (!ok) give_up();
     return ok;
   };
-  // unit k of this CTA: its record (waited for) and, when done, its release
-  auto meta_get = [&](int k) -> const UnitMeta* {
-    if (!wait_ok(&meta_full[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) return nullptr;
-    return &metas[k & 1];
-  };
-  auto meta_put = [&](int k) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&meta_empty[k & 1]);
+  auto waitw = [&](uint64_t* bar, uint32_t parity) {  // a whole warp's bounded wait
+    if (!ok) return false;
+    ok = warp_wait(bar, parity, abort_flag);
+    if (!ok && lane == 0) give_up();
+    return ok;
   };
 
-  if (warp == kWarpProd) {
-    // ---- producer: resolve each unit, then copy its query tile and its blocks -------------
-    int jg = 0, nq = 0;  // blocks and query tiles issued so far (ring positions)
-    if (lane == 0) {
-      prefetch_tensormap(&kv_map);
-      prefetch_tensormap(&q_map);
-    }
-    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
-      if (!wait_ok(&meta_empty[k & 1], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
-      UnitMeta& m = metas[k & 1];
+  if (warp == kWarpRes) {
+    // ---- resolver: the CTA's units c, c + G, ... in order, the non-empty ones dealt to the
+    // warpgroups in turn; an empty unit (a bad selection or page, or a split with no blocks) has
+    // its output zero-filled here, an invalid one (an inconsistent batch) is left as it is ------
+    for (int i = lane; i <= p.B; i += 32) qsl_s[i] = p.qsl[i];
+    __syncwarp();
+    int written0 = 0, written1 = 0, written2 = 0;  // records dealt to each warpgroup
+    int turn = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int split = u % p.splits, tg = u / p.splits, t = p.t0 + (tg >> 2), g = tg & 3;
       int lo = 0, hi = p.B - 1;  // the sequence of token t (largest b with qsl[b] <= t)
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.qsl[mid] <= t) lo = mid; else hi = mid - 1;
+        if (qsl_s[mid] <= t) lo = mid; else hi = mid - 1;
       }
       const int b = lo;
-      const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0;
+      const int q0 = qsl_s[b], ql = qsl_s[b + 1] - q0;
       const int L = p.seq_lens[b];
       const bool valid = t - q0 >= 0 && t - q0 < ql && ql <= p.max_q_len && L >= ql && L <= p.maxb * kBS;
       if (!valid && lane == 0 && split == 0 && g == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
@@ -611,12 +534,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad_page = !(ph >= 0 && ph < p.num_pages);
       }
       const bool bad = __any_sync(0xffffffffu, out_of_range || bad_page);
-      if ((out_of_range || bad_page)) set_status(p.status, MSA_ERR_DEVICE_FAULT);
+      if (out_of_range || bad_page) set_status(p.status, MSA_ERR_DEVICE_FAULT);
       const int nsel = bad ? 0 : __popc(msk);
       const int i0 = (nsel * split) / p.splits, i1 = (nsel * (split + 1)) / p.splits;
+      if (i1 == i0) {
+        if (valid) {  // nothing to attend: zero output (or an empty partial)
+          const int64_t row0 = static_cast<int64_t>(t) * kQHeads + g * kHPG;
+          if (p.splits == 1) {
+            uint4* o = reinterpret_cast<uint4*>(p.out + row0 * kD);
+            for (int e = lane; e < kHPG * kD / 8; e += 32) o[e] = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            const int64_t prow0 = static_cast<int64_t>(split) * p.T * kQHeads + row0;
+            float4* o = reinterpret_cast<float4*>(p.part_o + prow0 * kD);
+            for (int e = lane; e < kHPG * kD / 4; e += 32) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane < kHPG) p.part_lse[prow0 + lane] = -CUDART_INF_F;
+          }
+        }
+        continue;
+      }
+      const int x = turn;
+      turn = turn + 1 == kWgs ? 0 : turn + 1;
+      uint64_t* xb = reinterpret_cast<uint64_t*>(smem + S::kOffBar) + S::kBarsPerWg * x;
+      uint64_t* x_meta_full = xb + kStages + 10;
+      uint64_t* x_meta_empty = x_meta_full + kMeta;
+      const int k = x == 0 ? written0++ : (x == 1 ? written1++ : written2++);
+      if (!waitw(&x_meta_empty[k % kMeta], (static_cast<uint32_t>(k / kMeta) & 1u) ^ 1u)) break;
+      UnitMeta& m = metas[kMeta * x + k % kMeta];
       if (keep && lane < kSel && pos >= i0 && pos < i1) {
         m.blk[pos - i0] = v;
-        m.phys[pos - i0] = bad_page ? 0 : ph;
+        m.phys[pos - i0] = ph;
       }
       if (lane == 0) {
         m.t = t;
@@ -624,332 +570,390 @@ __global__ void __launch_bounds__(kThreads, 1)
         m.split = split;
         m.p_tok = L - ql + (t - q0);
         m.n = i1 - i0;
-        m.valid = valid ? 1 : 0;
-        m.bad = bad ? 1 : 0;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&meta_full[k & 1]);  // release: the record is visible to the waiters
-      const int n = i1 - i0;
-      if (n == 0) continue;
-      // the query tile of the unit (free once the S MMAs of the unit two query tiles back landed)
-      if (!wait_ok(&q_empty[nq & 1], (static_cast<uint32_t>(nq >> 1) & 1u) ^ 1u)) break;
+      if (lane == 0) mbar_arrive(&x_meta_full[k % kMeta]);  // release: the record is visible to the waiters
+    }
+    // the end of every warpgroup's list
+    for (int x = 0; x < kWgs && ok; ++x) {
+      uint64_t* xb = reinterpret_cast<uint64_t*>(smem + S::kOffBar) + S::kBarsPerWg * x;
+      uint64_t* x_meta_full = xb + kStages + 10;
+      uint64_t* x_meta_empty = x_meta_full + kMeta;
+      const int k = x == 0 ? written0 : (x == 1 ? written1 : written2);
+      if (!waitw(&x_meta_empty[k % kMeta], (static_cast<uint32_t>(k / kMeta) & 1u) ^ 1u)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&q_full[nq & 1], kQTile);
-        tma_load_2d(smem + S::kOffQ + static_cast<size_t>(nq & 1) * kQTile, &q_map, 0, t * kQHeads + g * kHPG,
-                    &q_full[nq & 1], policy_evict_first());
+        metas[kMeta * x + k % kMeta].n = -1;
+        mbar_arrive(&x_meta_full[k % kMeta]);
       }
-      ++nq;
-      for (int j = 0; j < n; ++j, ++jg) {
-        const int s = jg % kStages;
-        if (!wait_ok(&st_empty[s], (static_cast<uint32_t>(jg / kStages) & 1u) ^ 1u)) break;
-        if (lane == 0) {
+      __syncwarp();
+    }
+  } else if (warp >= kWarpIss) {
+    // ---- issuer of warpgroup w (lane 0): S and PV MMAs, and the copies of the blocks
+    // (kStages ahead of the PVs) and of each unit's query tile -------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_e4m3_f32(128, kHPG);
+      constexpr uint32_t idesc_pv = idesc_e4m3_f32_amn(128, 2 * kHPG);
+      prefetch_tensormap(&kv_map);
+      prefetch_tensormap(&q_map);
+      const uint64_t qpol = policy_evict_first();
+      // copy cursor: record kt, its block jt; jg_t blocks issued. It copies a record's query tile
+      // when it enters the record and may enter record kt only while the MMAs are at record
+      // kt - 1 or later: the query buffer it refills was then released by record kt - 2's last
+      // S, which has been issued, so the wait for it always ends.
+      int kt = 0, jt = 0, jg_t = 0;
+      bool t_end = false, t_in = false;
+      auto copy_fill = [&](int upto, int k_mma) {  // copies of blocks jg_t .. upto - 1 (stages free)
+        while (jg_t < upto && !t_end && ok) {
+          if (!t_in) {
+            if (kt >= k_mma + 2) return;
+            if (!wait1(&meta_full[kt % kMeta], static_cast<uint32_t>(kt / kMeta) & 1u)) return;
+            const UnitMeta& m = wmeta[kt % kMeta];
+            if (m.n < 0) {
+              t_end = true;
+              return;
+            }
+            if (!wait1(&q_empty[kt & 1], (static_cast<uint32_t>(kt >> 1) & 1u) ^ 1u)) return;
+            mbar_arrive_expect_tx(&q_full[kt & 1], kQTile);
+            tma_load_2d(qtile + (kt & 1) * kQTile, &q_map, 0, m.t * kQHeads + m.g * kHPG, &q_full[kt & 1], qpol);
+            t_in = true;
+            jt = 0;
+          }
+          const UnitMeta& m = wmeta[kt % kMeta];
+          const int s = jg_t % kStages;
           mbar_arrive_expect_tx(&st_full[s], kStageBytes);
-          tma_load_3d(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, &kv_map, 0,
-                      2 * g * (kRegion / kD), m.phys[j], &st_full[s]);
+          tma_load_3d(wgb + static_cast<size_t>(s) * kStageBytes, &kv_map, 0, 2 * m.g * (kRegion / kD), m.phys[jt],
+                      &st_full[s]);
+          ++jg_t;
+          if (++jt == m.n) {
+            t_in = false;
+            ++kt;
+          }
+        }
+      };
+      int jg = 0;
+      for (int k = 0; ok; ++k) {
+        copy_fill(jg + kStages, k);  // the stages of blocks before jg + kStages are free
+        if (!wait1(&meta_full[k % kMeta], static_cast<uint32_t>(k / kMeta) & 1u)) break;
+        const int n = wmeta[k % kMeta].n;
+        if (n < 0) break;
+        const int x = k & 1;  // query buffer and O^T accumulator of the unit
+        const uint64_t dq = sw128_kmajor_desc(smem_u32(qtile + x * kQTile));
+        auto issue_s = [&](int jb, bool last) {  // S^T = K(jb) Q^T
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 32 E4M3 per MMA: 8 TMEM columns of A, +32 B of B
+            tc_mma_f8_ta(tw + kColS, tw + kColK + 8 * kk, dq + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+          tc_commit(s_full);
+          if (last) tc_commit(&q_empty[x]);  // the query tile is free once these MMAs landed
+        };
+        if (!wait1(&q_full[x], static_cast<uint32_t>(k >> 1) & 1u) || !wait1(ka_full, static_cast<uint32_t>(jg) & 1u))
+          break;
+        issue_s(jg, n == 1);
+        for (int j = 0; j < n; ++j, ++jg) {
+          if (j + 1 < n) {  // S of the next block as soon as its K tile is in TMEM
+            if (!wait1(ka_full, static_cast<uint32_t>(jg + 1) & 1u)) break;
+            issue_s(jg + 1, j + 2 == n);
+          }
+          // O^T[x] was read out by the workers for record k - 2
+          if (j == 0 && !wait1(&o_free[x], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
+          if (!wait1(pv_ready, static_cast<uint32_t>(jg) & 1u)) break;
+          tc_fence_after();
+          {
+            const uint32_t vaddr = smem_u32(wgb + static_cast<size_t>(jg % kStages) * kStageBytes);
+            const uint64_t dp = sw128_kmajor_desc(smem_u32(ptile));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K = 32 keys per MMA: four 8-key groups of V (4 KB), +32 B of P^T
+              tc_mma_f8(tw + kColO + 32 * x, sw128_mnmajor8_desc(vaddr + 4096 * kk), dp + 2 * kk, idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(pv_done);
+          // the block's stage is free once PV(jg) has landed: refill it
+          if (!wait1(pv_done, static_cast<uint32_t>(jg) & 1u)) break;
+          copy_fill(jg + 1 + kStages, k);
         }
       }
-      if (!ok) break;
-    }
-    // copies that nobody waited for (after a give-up): wait before the CTA's memory goes
-    if (lane == 0) {
-      for (int j = jg > kStages ? jg - kStages : 0; j < jg; ++j)
+      // nothing of this thread's is in flight when the CTA ends: its MMAs, then its copies
+      tc_commit(fin);
+      if (!mbar_wait_bounded(fin, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+      for (int j = jg_t > kStages ? jg_t - kStages : 0; j < jg_t; ++j)
         if (!mbar_wait_bounded(&st_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, kWaitLimitNs, nullptr))
           set_status(p.status, MSA_ERR_TIMEOUT);
+      const int nq = kt + (t_in ? 1 : 0);  // query tiles issued
       for (int j = nq > 2 ? nq - 2 : 0; j < nq; ++j)
         if (!mbar_wait_bounded(&q_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
           set_status(p.status, MSA_ERR_TIMEOUT);
     }
-  } else if (warp == kWarpMmaS) {
-    // ---- S(j) = K(j) Q^T; the whole warp runs the loop, lane 0 issues ------------------------
-    constexpr uint32_t idesc_s = idesc_e4m3_f32(128, kHPG);
-    int jg = 0, nq = 0;
-    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
-      const UnitMeta* m = meta_get(k);
-      if (m == nullptr) break;
-      const int n = m->n;
-      meta_put(k);
-      if (n == 0) continue;
-      const int qs = nq & 1;
-      if (!wait_ok(&q_full[qs], static_cast<uint32_t>(nq >> 1) & 1u)) break;
-      const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + S::kOffQ + static_cast<size_t>(qs) * kQTile));
-      for (int j = 0; j < n; ++j, ++jg) {
-        const int x = jg & 1;
-        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
-        if (!wait_ok(&ka_full[x], par) || !wait_ok(&s_empty[x], par ^ 1u)) break;
-        tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // K = 32 E4M3 per MMA: 8 TMEM columns of A, +32 B of B
-            tc_mma_f8_ta(tmem + kColS + 16 * x, tmem + kColK + 32 * x + 8 * kk, dq + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
-          tc_commit(&s_full[x]);
-          tc_commit(&ka_empty[x]);
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&q_empty[qs]);  // the query tile is free once these MMAs landed
-      __syncwarp();
-      ++nq;
-    }
-    if (lane == 0) {  // nothing of this warp's is in flight when TMEM is released
-      tc_commit(fin_s);
-      if (!mbar_wait_bounded(fin_s, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == kWarpMmaO || warp == kWarpMmaO + 1) {
-    // ---- O^T(unit, x) += V(j)^T P(j)^T for the blocks j of parity x = warp - kWarpMmaO: two
-    // issuers, two accumulators (an MMA costs ~80 cycles of issue; the softmax adds the two) --
-    constexpr uint32_t idesc_o = idesc_f16_f32_amn(128, kHPG);
-    const int x = warp - kWarpMmaO;
-    int jg = 0;
-    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
-      const UnitMeta* m = meta_get(k);
-      if (m == nullptr) break;
-      const int n = m->n;
-      meta_put(k);
-      const int os = k & 1;
-      // O^T[os] was read out by the softmax warps for unit k - 2
-      if (!wait_ok(&o_free[os], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
-      bool first = true;
-      for (int j = 0; j < n; ++j, ++jg) {
-        if ((jg & 1) != x) continue;
-        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
-        const int y = jg % kVTiles;
-        if (!wait_ok(&v_full[y], static_cast<uint32_t>(jg / kVTiles) & 1u) || !wait_ok(&p_full[x], par)) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t dv = sw128_mnmajor_desc(smem_u32(smem + S::kOffV + static_cast<size_t>(y) * kVTile), kVLbo, kVSbo);
-          const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + S::kOffP + static_cast<size_t>(x) * kPTile));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // K = 16 keys per MMA: two 8-key groups of V; 32 B (or the next atom) of P
-            tc_mma_f16(tmem + kColO + 32 * os + 16 * x, dv + ((2 * kVSbo) >> 4) * kk,
-                       dp + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o, (!first || kk > 0) ? 1u : 0u);
-          tc_commit(&v_empty[y]);
-          tc_commit(&p_empty[x]);
-        }
-        __syncwarp();
-        first = false;
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&o_final[os]);  // every PV of this issuer for the unit has landed
-      __syncwarp();
-    }
-    if (lane == 0) {
-      tc_commit(fin_o + x);
-      if (!mbar_wait_bounded(fin_o + x, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp >= kWarpDq && warp < kWarpSm) {
-    // ---- dequant, two groups taking alternate blocks: thread = key kr = TMEM lane; K row -> K
-    // tile x in TMEM, V row -> f16 V tile y in shared memory (MN-major: key kr is K row kr) ---
-    const int kr = 32 * (warp & 3) + lane;
-    const uint32_t lanes = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    int jg = 0;  // blocks started (K side)
-    auto do_k = [&](int jb) {  // K of block jb (stage jb % kStages stays held for its V)
-      const int s = jb % kStages, x = jb & 1;
-      if (!wait_ok(&st_full[s], static_cast<uint32_t>(jb / kStages) & 1u)) return;
+  } else {
+    // ---- worker warp q of warpgroup w ------------------------------------------------------
+    const int q = warp & 3;
+    const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
+    const int key_k = 32 * q + kappa(lane);                                // K row -> TMEM lane 32 q + lane
+    const int vrow = 32 * q + lane;                                        // V tile row (key position)
+    const int key_v = 32 * q + kappa((lane >> 2) + 8 * (lane & 3));       // the key at that position
+    const int hb = 2 * (lane & 3);  // this thread's heads: hb, hb + 1, hb + 8, hb + 9 (slot hh)
+    // P^T row n = head (hi) or 16 + head (lo) sits at (n / 8) KB + (n % 8) x 128 B; this thread's
+    // word (keys 32 q + 4 (lane / 4) .. + 3) is in chunk 2 q + lane / 16 of the row, swizzled by
+    // n % 8 (= hb or hb + 1): two offsets, the rest are immediates
+    const int pch = 2 * q + (lane >> 4), pb = 4 * ((lane >> 2) & 3);
+    const uint32_t psw0 = static_cast<uint32_t>(hb * 128 + ((pch ^ hb) << 4) + pb);
+    const uint32_t psw1 = static_cast<uint32_t>((hb + 1) * 128 + ((pch ^ (hb + 1)) << 4) + pb);
+    const float c = p.scale_log2;
+    float* redm = reinterpret_cast<float*>(smem + S::kOffRed) + w * 128;    // [2][4][16]
+    float* mref = reinterpret_cast<float*>(smem + S::kOffMref) + w * 32;    // [2][16]
+    float* redl = reinterpret_cast<float*>(smem + S::kOffRedL) + w * 64;    // [4][16]
+    const int bar_vote = kBarVote + w, bar_x = kBarX + w;
+    int jg = 0, nre = 0;  // blocks seen; rescale events (alternate the two reduction buffers)
+
+    auto do_k = [&](int jb) {  // K rows of block jb -> the TMEM K tile
+      if (!waitw(&st_full[jb % kStages], static_cast<uint32_t>(jb / kStages) & 1u)) return;
       RawRow rk;
-      load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes, kr, rk);
-      if (!wait_ok(&ka_empty[x], (static_cast<uint32_t>(jb >> 1) & 1u) ^ 1u)) return;  // S(jb - 2) has landed
-      uint32_t w[32];
+      load_row(wgb + static_cast<size_t>(jb % kStages) * kStageBytes, key_k, rk);
+      uint32_t wk[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int qq = 0; qq < 4; ++qq) {
         uint32_t uu[8];
-        dequant_quarter(rk, q, lut, uu);
+        dequant_quarter(rk, qq, lut, uu);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[8 * q + e] = uu[e];
+        for (int e = 0; e < 8; ++e) wk[8 * qq + e] = uu[e];
       }
-      tc_fence_after();
-      tmem_st32(tmem + lanes + kColK + 32 * x, w);
+      tmem_st32(tw + lanes + kColK, wk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ka_full[x]);
+      if (lane == 0) mbar_arrive(ka_full);
     };
-    auto do_v = [&](int jb) {  // V of block jb, then its stage is free
-      const int s = jb % kStages, y = jb % kVTiles;
-      if (!ok) return;
-      RawRow rv;
-      load_row(smem + S::kOffStage + static_cast<size_t>(s) * kStageBytes + kRegion, kr, rv);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&st_empty[s]);
-      // PV(jb - kVTiles) has landed
-      if (!wait_ok(&v_empty[y], (static_cast<uint32_t>(jb / kVTiles) & 1u) ^ 1u)) return;
-      uint8_t* vt = smem + S::kOffV + static_cast<size_t>(y) * kVTile + (kr >> 3) * kVSbo + (kr & 7) * 128;
+
+    for (int k = 0;; ++k) {
+      const bool got = waitw(&meta_full[k % kMeta], static_cast<uint32_t>(k / kMeta) & 1u);
+      if (named_barrier_or(bar_vote, 128, !got)) break;  // one of the four gave up: all leave
+      const UnitMeta& m = wmeta[k % kMeta];
+      const int n = m.n;
+      if (n < 0) break;
+      const int t = m.t, g = m.g, split = m.split, p_tok = m.p_tok;
+      const int x = k & 1;
+      float m_ref[4], l[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t uu[8];
-        dequant_quarter(rv, q, lut, uu);
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {  // dims 32 q + 8 hh .. +7 = chunk cc = 4 q + hh
-          const int cc = 4 * q + hh;
-          const uint4 vv = make_uint4(cvt_f16x2_e4m3x2(uu[2 * hh]), cvt_f16x2_e4m3x2(uu[2 * hh] >> 16),
-                                      cvt_f16x2_e4m3x2(uu[2 * hh + 1]), cvt_f16x2_e4m3x2(uu[2 * hh + 1] >> 16));
-          *reinterpret_cast<uint4*>(vt + (cc >> 3) * kVLbo + (((cc & 7) ^ (kr & 7)) << 4)) = vv;
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&v_full[y]);
-    };
-    const int gq = (warp - kWarpDq) >> 2;  // this group's blocks: jg % 2 == gq
-    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
-      const UnitMeta* m = meta_get(k);
-      if (m == nullptr) break;
-      const int n = m->n;
-      meta_put(k);
-      for (int j = 0; j < n && ok; ++j, ++jg) {
-        if ((jg & 1) != gq) continue;
-        do_k(jg);
-        do_v(jg);
-      }
-      if (!ok) break;
-    }
-  } else if (warp >= kWarpSm) {
-    // ---- softmax: thread = key kr = TMEM lane ----------------------------------------------
-    const int wq = warp & 3;
-    const int kr = 32 * wq + lane;
-    const uint32_t lanes = static_cast<uint32_t>(32 * wq) << 16;
-    const float c = p.scale_log2;
-    int jg = 0, nred = 0;  // blocks seen; reductions done (alternates the two scratch buffers)
-    for (int k = 0, u = blockIdx.x; u < units; ++k, u += gridDim.x) {
-      // every softmax warp takes the same path through a unit (the named barriers need all
-      // four): a warp whose wait gave up inside the unit keeps walking with its work skipped
-      const UnitMeta* m = meta_get(k);
-      if (named_barrier_or(kBarWork, 128, m == nullptr)) {  // one of the four gave up: all leave
-        ok = false;
-        give_up();
-        break;
-      }
-      const int n = m->n;
-      const int t = m->t, g = m->g, split = m->split, p_tok = m->p_tok;
-      const bool valid = m->valid != 0, bad = m->bad != 0;
-      const int os = k & 1;
-      // m_ref starts at a large negative finite value rather than -inf, so that the exponent
-      // argument s * c - m_ref is large for any real score (the vote below takes the block's
-      // maximum then) and -inf for a masked key (P = 0), with no special case for the first
-      // block; 2^14 keeps s * c = d + m_ref within 2^-9 of the score (fp32 at 2^14), which only
-      // shifts the reference, never a P beyond the vote's bound
-      constexpr float kNoRef = -16384.0f;
-      float m_ref[16], l[16];
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        m_ref[h] = kNoRef;
-        l[h] = 0.f;
-      }
+      for (int hh = 0; hh < 4; ++hh) m_ref[hh] = l[hh] = 0.f;
+      do_k(jg);
+      bool quit = false;
       for (int j = 0; j < n; ++j, ++jg) {
-        const int x = jg & 1;
-        const uint32_t par = static_cast<uint32_t>(jg >> 1) & 1u;
-        float d[16];  // exponent arguments s * c - m_ref against the current reference
-        if (wait_ok(&s_full[x], par)) {
+        uint8_t* stg = wgb + static_cast<size_t>(jg % kStages) * kStageBytes;
+        RawRow rv;
+        if (ok) load_row(stg + kRegion, key_v, rv);  // V raw row, read before anyone overwrites the stage
+        float d[4][4];  // [key i][head slot hh]: exponent arguments s c - m_ref
+        if (waitw(s_full, static_cast<uint32_t>(jg) & 1u)) {
           tc_fence_after();
-          uint32_t r[16];
-          tmem_ld16(tmem + lanes + kColS + 16 * x, r);
+          uint32_t ra[8], rb[8];
+          tmem_ld16x256_x2(tw + lanes + kColS, ra);
+          tmem_ld16x256_x2(tw + lanes + (16u << 16) + kColS, rb);
           tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[x]);
-          const bool kvalid = m->blk[j] * kBS + kr <= p_tok;  // keys after the query position: -inf
 #pragma unroll
-          for (int h = 0; h < 16; ++h) d[h] = kvalid ? fmaf(__uint_as_float(r[h]), c, -m_ref[h]) : -CUDART_INF_F;
+          for (int o = 0; o < 2; ++o)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              d[e >> 1][2 * o + (e & 1)] = fmaf(__uint_as_float(ra[4 * o + e]), c, -m_ref[2 * o + (e & 1)]);
+              d[2 + (e >> 1)][2 * o + (e & 1)] = fmaf(__uint_as_float(rb[4 * o + e]), c, -m_ref[2 * o + (e & 1)]);
+            }
+          const int base = m.blk[j] * kBS;
+          if (base + kBS - 1 > p_tok) {  // the local block: keys after the query position get P = 0
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (base + 32 * q + kappa((lane >> 2) + 8 * i) > p_tok) {
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) d[i][hh] = -CUDART_INF_F;
+              }
+          }
         } else {
 #pragma unroll
-          for (int h = 0; h < 16; ++h) d[h] = -CUDART_INF_F;
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) d[i][hh] = -CUDART_INF_F;
         }
-        bool need = false;
+        bool need = j == 0;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) need |= d[h] > kRescaleLog2;
-        if (named_barrier_or(kBarWork, 128, need)) {  // the same answer in all four warps
-          float cf[16];  // the block maxima of s * c, then the rescale factors
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int h = 0; h < 16; ++h) cf[h] = d[h] + m_ref[h];
-          group_reduce16<true>(cf, cf, red + 64 * (nred & 1), wq, lane);
-          ++nred;
+          for (int hh = 0; hh < 4; ++hh) need |= d[i][hh] > kRescaleLog2;
+        // every raw row of the stage has been read, every warp has its scores (the same answer in
+        // all four warps)
+        if (named_barrier_or(bar_vote, 128, need || !ok || *abort_flag != 0)) {
+          if (named_barrier_or(bar_x, 128, !ok || *abort_flag != 0)) {  // a give-up, decided alike in all four
+            quit = true;
+            break;
+          }
+          // ---- the reference moves: block maxima of s c per head over the 128 keys
+          const bool first = j == 0;
+          float* rm = redm + 64 * (nre & 1);
+          const float* mr_old = mref + 16 * (nre & 1);
+          float* mr_new = mref + 16 * ((nre & 1) ^ 1);
+          ++nre;
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            float bm = fmaxf(fmaxf(d[0][hh], d[1][hh]), fmaxf(d[2][hh], d[3][hh])) + m_ref[hh];
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            if (lane < 4) rm[16 * q + hb + (hh & 1) + 8 * (hh >> 1)] = bm;
+          }
+          named_barrier(bar_x, 128);
+          // the new reference of a head: the block maximum (first block) or the larger of the two
+          auto new_ref = [&](int h, float& mo, float& cf) {
+            const float bx = fmaxf(fmaxf(rm[h], rm[16 + h]), fmaxf(rm[32 + h], rm[48 + h]));
+            mo = first ? 0.f : mr_old[h];
+            float mn = first ? bx : fmaxf(mo, bx);
+            if (!(mn > -CUDART_INF_F)) mn = mo;  // no valid key in the block (cannot happen): keep it finite
+            cf = first ? 0.f : fast_exp2(mo - mn);
+            return mn;
+          };
           bool moved = false;
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float mn = fmaxf(m_ref[h], cf[h]);
-            moved |= mn != m_ref[h];
-            d[h] += m_ref[h] - mn;              // the same arguments against the new reference
-            cf[h] = fast_exp2(m_ref[h] - mn);  // 0 when there was no reference yet
-            m_ref[h] = mn;
-            l[h] *= cf[h];
-          }
-          {  // this thread's copy of the factors (the same in all 128 threads) for the O rescale
-            float4* cfp = reinterpret_cast<float4*>(smem + S::kOffCf) + 4 * kr;
+          for (int hh = 0; hh < 4; ++hh) {  // this thread's own heads
+            const int h = hb + (hh & 1) + 8 * (hh >> 1);
+            float mo, cf;
+            const float mn = new_ref(h, mo, cf);
+            moved |= mn != mo;
 #pragma unroll
-            for (int h4 = 0; h4 < 4; ++h4) cfp[h4] = make_float4(cf[4 * h4], cf[4 * h4 + 1], cf[4 * h4 + 2], cf[4 * h4 + 3]);
+            for (int i = 0; i < 4; ++i) d[i][hh] += m_ref[hh] - mn;
+            l[hh] *= cf;
+            m_ref[hh] = mn;
+            if (q == 0 && lane < 4) mr_new[h] = mn;
           }
-          // both accumulators *= cf once PV(jg - 1) and PV(jg - 2) have landed (PV(jg) waits for
-          // this block's P); one not yet written in this unit is rescaled harmlessly: its first
-          // PV of the unit overwrites it
-          if (moved && j > 0 && wait_ok(&p_empty[(jg - 1) & 1], static_cast<uint32_t>((jg - 1) >> 1) & 1u) &&
-              (j < 2 || wait_ok(&p_empty[jg & 1], (static_cast<uint32_t>(jg >> 1) & 1u) ^ 1u))) {
+          // O^T *= cf once PV(jg - 1) has landed (this thread's lane = dim 32 q + lane), four heads
+          // (their hi and lo columns) at a time; every thread of the group takes the same branch
+          if (__any_sync(0xffffffffu, moved) && !first && waitw(pv_done, static_cast<uint32_t>(jg - 1) & 1u)) {
             tc_fence_after();
-            o_rescale(tmem + lanes + kColO + 32 * os, reinterpret_cast<const float4*>(smem + S::kOffCf) + 4 * kr);
+#pragma unroll 1
+            for (int h4 = 0; h4 < 4; ++h4) {
+              float cf4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float mo;
+                new_ref(4 * h4 + e, mo, cf4[e]);
+              }
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const uint32_t ta = tw + lanes + kColO + 32 * x + 16 * z + 4 * h4;
+                uint32_t o4[4];
+                tmem_ld4(ta, o4);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o4[e] = __float_as_uint(__uint_as_float(o4[e]) * cf4[e]);
+                tmem_st4(ta, o4);
+              }
+            }
+            tmem_wait_st();
             tc_fence_before();
           }
         }
-        // P = exp2(s c - m) -> P^T tile x (free once PV(jg - 2) has landed): row h, key kr
-        if (wait_ok(&p_empty[x], par ^ 1u)) {
-          uint8_t* pt = smem + S::kOffP + static_cast<size_t>(x) * kPTile + (kr >> 6) * 2048 + (kr & 7) * 2;
-          const int ch = (kr & 63) >> 3;
+        // ---- K of the next block (its S MMA runs while this block's V and P are made)
+        if (j + 1 < n) do_k(jg + 1);
+        // ---- V rows -> the E4M3 V tile over the stage: row vrow = key position, MN-major
+        if (ok) {
+          uint8_t* vt = stg + (vrow >> 3) * 1024 + (vrow & 7) * 128;
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float pv = fast_exp2(d[h]);
-            l[h] += pv;
-            *reinterpret_cast<__half*>(pt + (h >> 3) * 1024 + (h & 7) * 128 + ((ch ^ (h & 7)) << 4)) =
-                __float2half_rn(pv);
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t uu[8];
+            dequant_quarter(rv, qq, lut, uu);
+            *reinterpret_cast<uint4*>(vt + (((2 * qq) ^ (vrow & 7)) << 4)) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
+            *reinterpret_cast<uint4*>(vt + (((2 * qq + 1) ^ (vrow & 7)) << 4)) = make_uint4(uu[4], uu[5], uu[6], uu[7]);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&p_full[x]);
         }
+        // ---- P = exp2(d) -> P^T hi / lo (the tile is free once PV(jg - 1) has landed)
+        if (waitw(pv_done, static_cast<uint32_t>(jg - 1) & 1u)) {
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            float pv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pv[i] = fast_exp2(d[i][hh]);
+            l[hh] += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+            const uint32_t h01 = cvt_e4m3x2(pv[0], pv[1]), h23 = cvt_e4m3x2(pv[2], pv[3]);
+            const uint32_t r01 = sub_f16x2(pack_f16x2(pv[0], pv[1]), cvt_f16x2_e4m3x2(h01));
+            const uint32_t r23 = sub_f16x2(pack_f16x2(pv[2], pv[3]), cvt_f16x2_e4m3x2(h23));
+            // lo carries 16 (P - hi): |P - hi| <= P / 16, so it stays <= 448 and out of the E4M3
+            // subnormals for every P that matters
+            const uint32_t l01 = cvt_e4m3x2_f16x2(mul_f16x2(r01, kLoScale2)), l23 = cvt_e4m3x2_f16x2(mul_f16x2(r23, kLoScale2));
+            uint8_t* pw = ptile + ((hh & 1) ? psw1 : psw0) + 1024 * (hh >> 1);
+            *reinterpret_cast<uint32_t*>(pw) = h01 | (h23 << 16);
+            *reinterpret_cast<uint32_t*>(pw + 2048) = l01 | (l23 << 16);
+          }
+        }
+        fence_proxy_async_smem();  // the V tile and P^T are read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pv_ready);
       }
-      // ---- the unit's output: lane kr = dim kr of O^T; l summed over the 128 keys' threads --
-      float (&lt)[16] = l;  // the per-head sums, reduced in place
-      group_reduce16<false>(l, lt, red + 64 * (nred & 1), wq, lane);
-      ++nred;
+      if (quit) break;
+      // ---- the unit's output: thread = dim 32 q + lane of O^T; l summed over the 128 keys
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 4);
+        l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 8);
+        l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 16);
+      }
+      if (lane < 4) {
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) redl[16 * q + hb + (hh & 1) + 8 * (hh >> 1)] = l[hh];
+      }
+      const bool have = waitw(pv_done, static_cast<uint32_t>(jg - 1) & 1u);  // the last PV has landed
       uint32_t o[16];
-      const bool have = n > 0 && wait_ok(&o_final[os], static_cast<uint32_t>(k >> 1) & 1u);
-      if (have) {  // the accumulator of the unit's first block, plus the other one if it was used
-        const int x0 = (jg - n) & 1;
+      if (have) {  // hi + lo halves of the sum
         tc_fence_after();
-        tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * x0, o);
+        uint32_t o2[16];
+        tmem_ld16(tw + lanes + kColO + 32 * x, o);
+        tmem_ld16(tw + lanes + kColO + 32 * x + 16, o2);
         tmem_wait_ld();
-        if (n > 1) {
-          uint32_t o2[16];
-          tmem_ld16(tmem + lanes + kColO + 32 * os + 16 * (x0 ^ 1), o2);
-          tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) + __uint_as_float(o2[h]));
-        }
-        tc_fence_before();
+        for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(fmaf(__uint_as_float(o2[h]), 1.0f / kLoScale, __uint_as_float(o[h])));
       }
+      tc_fence_before();
+      named_barrier(bar_x, 128);  // every warp's sums are in redl; every warp has read O^T
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[os]);  // O^T[os] may be overwritten
-      if (valid) {
-        const bool zero = !have || bad || *abort_flag != 0;
+      if (lane == 0) mbar_arrive(&o_free[x]);  // O^T[x] may be overwritten
+      float lt[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const bool z = zero || !(lt[h] > 0.f);
-          const float val = z ? 0.f : __uint_as_float(o[h]) / lt[h];
-          const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
-          if (p.splits == 1) {
-            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * kD + kr] = __float2bfloat16_rn(val);
-          } else {
-            const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
-            p.part_o[prow * kD + kr] = val;
-            if (kr == 0) p.part_lse[prow] = z ? -CUDART_INF_F : m_ref[h] + __log2f(lt[h]);
-          }
+      for (int h4 = 0; h4 < 4; ++h4) {
+        const float4 a0 = *reinterpret_cast<const float4*>(redl + 4 * h4);
+        const float4 a1 = *reinterpret_cast<const float4*>(redl + 16 + 4 * h4);
+        const float4 a2 = *reinterpret_cast<const float4*>(redl + 32 + 4 * h4);
+        const float4 a3 = *reinterpret_cast<const float4*>(redl + 48 + 4 * h4);
+        lt[4 * h4 + 0] = (a0.x + a1.x) + (a2.x + a3.x);
+        lt[4 * h4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
+        lt[4 * h4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
+        lt[4 * h4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
+      }
+      const bool zero = !have || *abort_flag != 0;
+      const int dim = 32 * q + lane;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const bool z = zero || !(lt[h] > 0.f);
+        const float val = z ? 0.f : __uint_as_float(o[h]) / lt[h];
+        const int64_t orow = static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
+        if (p.splits == 1) {
+          reinterpret_cast<__nv_bfloat16*>(p.out)[orow * kD + dim] = __float2bfloat16_rn(val);
+        } else {
+          const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + orow;
+          p.part_o[prow * kD + dim] = val;
         }
       }
-      meta_put(k);
+      if (p.splits > 1 && q == 0 && lane < 4) {  // lse of this thread's four heads
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const int h = hb + (hh & 1) + 8 * (hh >> 1);
+          float lh = 0.f;
+#pragma unroll
+          for (int hx = 0; hx < 16; ++hx) lh = hx == h ? lt[hx] : lh;
+          const bool z = zero || !(lh > 0.f);
+          const int64_t prow = static_cast<int64_t>(split) * p.T * kQHeads + static_cast<int64_t>(t) * kQHeads + g * kHPG + h;
+          p.part_lse[prow] = z ? -CUDART_INF_F : m_ref[hh] + __log2f(lh);
+        }
+      }
+      named_barrier(bar_x, 128);  // redl may be written again
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&meta_empty[k % kMeta]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMmaS) {
+  if (warp == kWarpRes) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -990,8 +994,9 @@ __global__ void __launch_bounds__(256) k_attn_merge(const float* __restrict__ pa
 // SM (the keys of each block over four mma.sync warps, the dequant over eight), so a batch of
 // few tokens finishes in one short wave; tc::k_attn_tc runs one persistent CTA per SM over all
 // the (token, group) units with the contractions on tcgen05, which keeps the SM busier once
-// there are several waves of units. The many-token kernel takes more than two units per SM.
-bool use_tc_kernel(int T) { return 4 * T > 2 * 152; }
+// there are several waves of units. The many-token kernel takes more than two units per SM
+// (of msa_host::kTunedSms SMs: the choice depends on the arguments alone).
+bool use_tc_kernel(int T) { return 4 * T > 2 * msa_host::kTunedSms; }
 
 size_t attn_ws_bytes(int T, int splits) {
   if (splits <= 1) return 0;

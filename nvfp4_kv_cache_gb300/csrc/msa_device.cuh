@@ -230,6 +230,25 @@ __device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint32_t two_bytes) {
   return r;
 }
 
+// f16x2 -> two E4M3 bytes (round to nearest even, saturating): the low half in bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   const uint32_t h2 = cvt_f16x2_e4m3x2(byte & 0xFFu);
   float f;
@@ -448,6 +467,61 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_f16_f32_amn(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: E4M3 x E4M3 -> F32, A MN-major, B K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32_amn(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory descriptor of an MN-major operand of 8-bit elements whose MN extent is one
+// 128-byte swizzle atom (128 elements): K-rows of 128 B, 16-byte chunk c of K-row r stored at
+// chunk c ^ (r & 7), 8-row groups 1024 B apart along K.
+__device__ __forceinline__ uint64_t sw128_mnmajor8_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (one atom along MN: unused)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8-row groups along K
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// 32 lanes x 32 consecutive 32-bit columns into registers: thread i gets lane (base lane + i).
+// Completes at tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 16 lanes x 16 columns (shape 16x256b, two repeats): thread t gets, for o = 0..1 and e = 0..3,
+// r[4o + e] = lane (base + t/4 + 8*(e/2)), column (8o + 2*(t%4) + e%2). Completes at tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns into / from registers: thread i, lane (base lane + i).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns into registers: thread i gets lane (base lane + i).

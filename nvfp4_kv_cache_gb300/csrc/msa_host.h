@@ -73,13 +73,18 @@ inline int num_sms() {
   return n;
 }
 
-// Splits of each (query token, group)'s selected blocks, chosen from T alone (so workspace
-// sizes are a pure function of the arguments): as many as keep the T x 4 x splits CTAs (one
-// per SM) within one wave of a 152-SM GB300, at least 1, at most 16.
+// The SM count the automatic choices below are tuned for: a GB300's 152. They are taken from
+// the arguments alone, not from the device, so that workspace sizes are a pure function of the
+// arguments; on a part with another SM count they still give correct results, only tuned for
+// the wrong machine.
+constexpr int kTunedSms = 152;
+
+// Splits of each (query token, group)'s selected blocks: as many as keep the T x 4 x splits
+// CTAs (one per SM) within one wave of kTunedSms SMs, at least 1, at most 16.
 inline int auto_splits(int T) {
   const int items = 4 * T;
   if (items <= 0) return 1;
-  const int s = 152 / items;
+  const int s = kTunedSms / items;
   return s < 1 ? 1 : (s > 16 ? 16 : s);
 }
 

@@ -14,7 +14,9 @@ timed region (pinned H2D of the step's queries and metadata on two streams, q be
 indexer, and the attention storing the output into the pinned host buffer);
 `e2e.copy_back_us` is the same call with the output copied back on the copy stream instead, and
 `e2e.serial_copies_us` the same copies issued one after another around msa_decode_step;
-`cpu_baseline` times the oracle on a bounded sample on the host cores.
+`cpu_baseline` times the oracle on a bounded sample on the host cores; `per_config` repeats the
+measurement (fewer steps, stated in each entry) on every other configuration: tiny, decode,
+long and the four layers of the ragged serving batch, each with its own sampled oracle time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config spec] [--impl ours|reference]
 """
@@ -302,6 +304,98 @@ def time_prefill(msa, steps: int, warmup: int, flush, dev):
             "selections": "local block + 15 distinct earlier blocks drawn uniformly per (token, group)"}
 
 
+PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 8, 3
+
+
+def measure_config(msa, w: W.Workload, layer: int, flush, dev, with_cpu: bool):
+    """One configuration (one layer of it) the way the headline is measured, with fewer steps:
+    the fused step's µs (L2 flushed before each step), the three stages timed one by one,
+    algorithmic bytes from the step's own selection, and the oracle on one sequence x B."""
+    import torch
+
+    from workloads.device import DeviceLayer
+
+    dl = DeviceLayer(w, layer, device=dev)
+    o = dl.outputs()
+    ws = dl.workspace()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"], o["scores"], o["sel"])
+
+    for _ in range(PER_CONFIG_WARMUP):
+        step()
+    torch.cuda.synchronize()
+    if msa.msa_read_device_status(ws) != msa.MSA_OK:
+        raise RuntimeError(f"{w.name} layer {layer}: device status not OK")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(PER_CONFIG_STEPS)]
+    for i in range(PER_CONFIG_STEPS):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    sel = o["sel"].cpu().numpy()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    aws = torch.empty(max(msa.msa_attn_workspace_size(w.B, w.T, 0), 256), dtype=torch.uint8, device=dev)
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(PER_CONFIG_STEPS)]
+    for i in range(PER_CONFIG_STEPS):
+        flush.fill_(i & 0xFF)
+        e = st_ev[i]
+        e[0].record(stream)
+        msa.msa_indexer_decode(dl.batch, dl.cache, dl.iq8, o["scores"], status)
+        e[1].record(stream)
+        msa.msa_topk_blocks(dl.batch, o["scores"], o["sel"], status)
+        e[2].record(stream)
+        msa.msa_sparse_attn_decode(dl.batch, dl.cache, dl.q8, o["sel"], dl.softmax_scale, o["out"], 0, aws, status)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if msa.status_bits(status) != 0:
+        raise RuntimeError(f"{w.name} layer {layer}: stage status not OK")
+    stage_ms = [statistics.mean(st_ev[i][j].elapsed_time(st_ev[i][j + 1]) for i in range(PER_CONFIG_STEPS))
+                for j in range(3)]
+    peak_gbs, peak_kind = peaks()
+    idx_bytes = index_bytes(w, layer)
+    total = step_bytes(w, layer, sel)
+    attn_bytes = total - idx_bytes
+    stage_frac = {"indexer": idx_bytes / (stage_ms[0] * 1e-3) / 1e9 / peak_gbs,
+                  "attention": attn_bytes / (stage_ms[2] * 1e-3) / 1e9 / peak_gbs}
+    dominant = "attention" if stage_ms[2] >= stage_ms[0] else "indexer"
+    rec = {"workload": w.name, "layer": layer,
+           "index_dtype": "nvfp4" if w.layers[layer].index_dtype == W.INDEX_NVFP4 else "fp8",
+           "B": w.B, "T": w.T, "steps": PER_CONFIG_STEPS, "warmup": PER_CONFIG_WARMUP,
+           "us_per_layer_step": step_ms * 1e3,
+           "stages_us": {"indexer": stage_ms[0] * 1e3, "topk": stage_ms[1] * 1e3, "attention": stage_ms[2] * 1e3},
+           "step_bytes": total, "achieved_tbps": total / (step_ms * 1e-3) / 1e12,
+           "step_frac_of_hbm_peak": total / (step_ms * 1e-3) / 1e9 / peak_gbs,
+           "stage_frac_of_hbm_peak": stage_frac, "dominant_stage": dominant,
+           "dominant_frac": stage_frac[dominant], "peak_kind": f"{peak_kind} hbm_gbs"}
+    if with_cpu:
+        active = [b for b in range(w.B) if w.q_lens[b] > 0]
+        b0 = active[0]
+        dt, cores = oracle_sample(w, layer, b0, dev)
+        rec["cpu_baseline"] = {"value": dt * len(active) * 1e6, "unit": "us/layer-step", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"sequence {b0} ({w.seq_lens[b0]} tokens, {w.q_lens[b0]} query tokens, 4 "
+                                         f"groups, 64 heads): oracle indexer+selection+attention wall time x "
+                                         f"{len(active)}"}
+    del dl, o, ws, aws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def per_config_lines(msa, flush, dev, with_cpu: bool):
+    """Every configuration besides the headline one: tiny, decode, long and the four ragged layers."""
+    out = []
+    for name in ("tiny", "decode", "long"):
+        out.append(measure_config(msa, W.CONFIGS[name](), 0, flush, dev, with_cpu))
+    rw = W.CONFIGS["ragged"]()
+    for layer in range(len(rw.layers)):
+        out.append(measure_config(msa, rw, layer, flush, dev, with_cpu))
+    return out
+
+
 def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -439,6 +533,12 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
     e2e_copy_back_ms = time_e2e(host_step_copy_back)
     e2e_serial_ms = time_e2e(serial_step)
 
+    # every other configuration, one line each (rank 0, one GPU, the default headline run only)
+    per_config = None
+    if rank == 0 and world == 1 and args.config == "spec" and not args.no_per_config:
+        del q_h, iq_h, meta_h, out_h
+        per_config = per_config_lines(msa, flush, dev, not args.no_cpu_baseline)
+
     # clocks sampled from the start of the timed loop through the stage, exact-indexer, prefill and
     # end-to-end loops that follow it (the timed loop alone is shorter than the sampling period)
     clk = clocks.stop((t_epoch, t_epoch + wall)) if clocks else None
@@ -498,6 +598,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "per_config": per_config,
         "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)
@@ -511,6 +612,7 @@ def main():
     ap.add_argument("--config", default="spec", choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the lines of the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

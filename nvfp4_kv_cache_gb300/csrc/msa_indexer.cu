@@ -14,16 +14,18 @@
 //    block-table loads in flight while lane 0 issues one 2-D tensor copy per 128-token index
 //    page into the stage ring (L2 evict-first: every byte is read once). The copy applies the
 //    128-byte swizzle, so the per-row loads below are free of bank conflicts;
-//  * two dequant groups of four warps take alternate pages, thread = key row = TMEM lane. An
+//  * three dequant groups of four warps take pages in turn, thread = key row = TMEM lane. An
 //    NVFP4 row becomes 128 E4M3 bytes (LUT + byte-permute) stored straight into a TMEM key
 //    tile (tcgen05.st): the tile never makes a round trip through shared memory. An FP8 page
 //    is already the tensor core's swizzled K-major tile and stays in its stage. The groups
 //    also keep each tile slot's copy of the sequence's index queries (a 32 x 128 B swizzled
 //    shared tile) current;
-//  * one MMA thread: four tcgen05.mma kind::f8f6f4 per page (M = 128 keys, N = 16 or 32
+//  * three MMA warps take pages in turn, one thread each issuing (a burst of four MMAs costs the
+//    issuing thread ~450 cycles): four tcgen05.mma kind::f8f6f4 per page (M = 128 keys, N = 16 or 32
 //    (token, group) columns, K = 4 x 32) into a ring of TMEM accumulators, then commits that
 //    free the key tile and publish the scores;
-//  * eight max-pool warps, two per TMEM lane quarter, take alternate pages: the 16x256b TMEM
+//  * three max-pool groups of four warps (one per TMEM lane quarter) take pages in turn (a page's
+//    pooling is a chain of dependent steps, so the groups overlap several pages): the 16x256b TMEM
 //    load hands every thread four keys of eight columns, so a warp needs a 4-key register max
 //    and a 3-step shuffle transpose-reduce. Each quarter stores its partial maxima in shared
 //    memory and counts itself in; the page's last quarter combines the four and stores the block
@@ -45,7 +47,7 @@ namespace msa {
 namespace {
 
 constexpr int kDqGroups = 3;                     // dequant groups (4 warps each)
-constexpr int kEpGroups = 2;                     // max-pool groups (4 warps each)
+constexpr int kEpGroups = 3;                     // max-pool groups (4 warps each)
 constexpr int kMmaWarps = 3;                     // MMA-issuing warps (pages in turn)
 constexpr int kWarpDq = 1 + kMmaWarps;           // first dequant warp
 constexpr int kWarpEp = kWarpDq + 4 * kDqGroups; // first max-pool warp
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       if (lane == 0) mbar_arrive(&a_full[a]);
     }
   } else {
-    // ---- max-pool warps: warp (ep, wq) pools TMEM lane quarter wq of pages ep, ep + 2, ...;
+    // ---- max-pool warps: warp (ep, wq) pools TMEM lane quarter wq of pages ep, ep + 3, ...;
     // the quarter that finishes a page last (a shared counter) combines the four partial
     // maxima, so the quarters never wait for one another ----------------------------------------
     const int ep = (warp - kWarpEp) >> 2;

@@ -249,6 +249,51 @@ msa_status msa_topk_candidates_host(const float* block_scores, int64_t rows,
 msa_status msa_topk_merge_host(const uint64_t* cand, int32_t n_shards, int64_t rows,
                                const int32_t* local, int32_t* sel);
 
+/* The K/V of the selected blocks, brought to the rank that owns the query tokens
+ * ("Indexador NVFP4 DCP": each rank holds the blocks of its context range; the merged selection
+ * names blocks on several ranks, and the owner's sparse attention needs their K/V locally).
+ * The owner's copy is a pool of gathered pages in the KV page layout (73,728 B each) with its own
+ * block table, so msa_sparse_attn_decode runs on it unchanged.
+ *
+ * msa_kv_gather_map: number the distinct (sequence, block) pairs that any query token of the
+ * sequence selected in any group: sequence by sequence, in block order.
+ *   sel           [T][4][16] int32, device (the merged selection; negative entries ignored; an
+ *                 entry at or past the sequence's block count sets MSA_ERR_DEVICE_FAULT and is
+ *                 ignored)
+ *   map           [B][max_blocks_per_seq] int32, device, written: the gathered page of the pair,
+ *                 or -1 -- the owner's block table into the gathered pool
+ *   masks         [B][max_blocks_per_seq] uint8, device, written: bit g set when group g selected
+ *                 the pair (only those groups' regions are gathered and read)
+ *   num_gathered  [1] int32, device, written: the pool's page count */
+msa_status msa_kv_gather_map(const msa_geometry* geo, const msa_batch* batch, const int32_t* sel,
+                             int32_t* map, uint8_t* masks, int32_t* num_gathered, uint32_t* status,
+                             cudaStream_t stream);
+
+/* msa_kv_gather_pages: on a rank holding blocks [block_begin, block_end) of every sequence
+ * (batch->block_table and cache describe that rank's own pages), copy the K and V regions of every
+ * selected (sequence, block, group) it holds into page map[b][block] of gathered_kv. Ranks
+ * whose ranges partition the blocks fill disjoint pages; each rank may write straight into the
+ * owner's pool (one GPU) or into a pool of its own whose filled pages are then copied to the
+ * owner. A page id outside the cache or a gathered page >= max_gathered sets
+ * MSA_ERR_DEVICE_FAULT and is skipped.
+ *   map, masks    as written by msa_kv_gather_map, device
+ *   gathered_kv   [max_gathered][73,728 B], device, 16-byte aligned */
+msa_status msa_kv_gather_pages(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
+                               const int32_t* map, const uint8_t* masks, int32_t block_begin,
+                               int32_t block_end, uint8_t* gathered_kv, int32_t max_gathered,
+                               uint32_t* status, cudaStream_t stream);
+
+/* Host-memory versions of the two (synchronous, no GPU; arrays as above, in host memory).
+ * msa_kv_gather_map_host returns the gathered page count, or -1 on a bad argument or a
+ * selected block past its sequence. */
+int32_t msa_kv_gather_map_host(int32_t B, int32_t T, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, int32_t max_blocks_per_seq, const int32_t* sel,
+                               int32_t* map, uint8_t* masks);
+msa_status msa_kv_gather_pages_host(int32_t B, int32_t max_blocks_per_seq, const int32_t* block_table,
+                                    const uint8_t* kv_pages, int32_t num_pages, const int32_t* map,
+                                    const uint8_t* masks, int32_t block_begin, int32_t block_end,
+                                    uint8_t* gathered_kv, int32_t max_gathered);
+
 /* Workspace bytes msa_sparse_attn_decode needs for num_splits partial results per token
  * (num_splits 0 = the automatic choice, which never exceeds 16). */
 size_t msa_attn_workspace_size(const msa_geometry* geo, int32_t B, int32_t T, int32_t num_splits);

@@ -89,6 +89,10 @@ _SIGS = {
     "msa_topk_merge": (_I32, [_GP, _BP, _P, _I32, _P, _P, _P]),
     "msa_topk_candidates_host": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P]),
     "msa_topk_merge_host": (_I32, [_P, _I32, _I64, _P, _P]),
+    "msa_kv_gather_map": (_I32, [_GP, _BP, _P, _P, _P, _P, _P, _P]),
+    "msa_kv_gather_pages": (_I32, [_GP, _BP, _CP, _P, _P, _I32, _I32, _P, _I32, _P, _P]),
+    "msa_kv_gather_map_host": (_I32, [_I32, _I32, _P, _P, _I32, _P, _P, _P]),
+    "msa_kv_gather_pages_host": (_I32, [_I32, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _I32]),
     "msa_attn_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_sparse_attn_decode": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _SZ, _P, _P, _P]),
     "msa_sparse_attn_decode_noalloc": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _I32, _P, _P, _P]),
@@ -281,6 +285,53 @@ def msa_topk_merge_host(cand: np.ndarray, local: np.ndarray) -> np.ndarray:
     _check(_lib.msa_topk_merge_host(cd.ctypes.data, cd.shape[0], cd.shape[1], lc.ctypes.data, out.ctypes.data),
            "msa_topk_merge_host")
     return out
+
+
+def msa_kv_gather_map(batch: Batch, sel: torch.Tensor, map_out: torch.Tensor, masks: torch.Tensor,
+                      num_gathered: torch.Tensor, status: Optional[torch.Tensor] = None) -> None:
+    """map_out int32 [B, max_blocks], masks uint8 [B, max_blocks], num_gathered int32 [1] (device)."""
+    _check(_lib.msa_kv_gather_map(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(sel), _ptr(map_out),
+                                  _ptr(masks), _ptr(num_gathered), _ptr(status), _stream()), "msa_kv_gather_map")
+
+
+def msa_kv_gather_pages(batch: Batch, cache: Cache, map_in: torch.Tensor, masks: torch.Tensor, block_begin: int,
+                        block_end: int, gathered_kv: torch.Tensor, max_gathered: int,
+                        status: Optional[torch.Tensor] = None) -> None:
+    """Copy the selected K/V regions this shard holds (blocks [block_begin, block_end)) into the
+    gathered pool gathered_kv (uint8, max_gathered x 73,728 B, device)."""
+    _check(_lib.msa_kv_gather_pages(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c), _ptr(map_in),
+                                    _ptr(masks), int(block_begin), int(block_end), _ptr(gathered_kv),
+                                    int(max_gathered), _ptr(status), _stream()), "msa_kv_gather_pages")
+
+
+def msa_kv_gather_map_host(query_start_loc: np.ndarray, seq_lens: np.ndarray, max_blocks: int,
+                           sel: np.ndarray):
+    """Host version of msa_kv_gather_map: returns (map int32 [B, max_blocks], masks uint8, count)."""
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    sl_ = np.ascontiguousarray(sel, dtype=np.int32)
+    B = sl.shape[0]
+    mp = np.zeros((B, max_blocks), dtype=np.int32)
+    mk = np.zeros((B, max_blocks), dtype=np.uint8)
+    n = int(_lib.msa_kv_gather_map_host(B, int(qsl[-1]), qsl.ctypes.data, sl.ctypes.data, int(max_blocks),
+                                        sl_.ctypes.data, mp.ctypes.data, mk.ctypes.data))
+    if n < 0:
+        raise MsaError(MSA_ERR_INVALID_ARG, "msa_kv_gather_map_host")
+    return mp, mk, n
+
+
+def msa_kv_gather_pages_host(block_table: np.ndarray, kv_pages: np.ndarray, num_pages: int, map_in: np.ndarray,
+                             masks: np.ndarray, block_begin: int, block_end: int, gathered_kv: np.ndarray) -> None:
+    """Host version of msa_kv_gather_pages (numpy arrays; gathered_kv uint8 [n, 73,728] is filled)."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    kv = np.ascontiguousarray(kv_pages, dtype=np.uint8)
+    mp = np.ascontiguousarray(map_in, dtype=np.int32)
+    mk = np.ascontiguousarray(masks, dtype=np.uint8)
+    assert gathered_kv.dtype == np.uint8 and gathered_kv.flags.c_contiguous
+    _check(_lib.msa_kv_gather_pages_host(bt.shape[0], bt.shape[1], bt.ctypes.data, kv.ctypes.data, int(num_pages),
+                                         mp.ctypes.data, mk.ctypes.data, int(block_begin), int(block_end),
+                                         gathered_kv.ctypes.data, gathered_kv.size // KV_PAGE_BYTES),
+           "msa_kv_gather_pages_host")
 
 
 def msa_attn_workspace_size(B: int, T: int, num_splits: int = 0) -> int:

@@ -117,3 +117,102 @@ def test_gloo_two_ranks_exchange_and_merge(orc):
         assert p.exitcode == 0
     for r in range(s.shape[0]):
         assert np.array_equal(sel[r], orc.select_row(s[r].astype(np.float64), int(local[r])))
+
+
+# ---- the K/V side: each rank packs the selected pages it holds; the owner assembles them ---
+def _gather_case(seed: int):
+    """A small batch with its own page pool (random bytes), a permuted block table and a valid
+    selection (local block first, then distinct earlier blocks, -1 padded)."""
+    rng = np.random.default_rng(seed)
+    seq_lens = np.array([1500, 700, 128 * 9 + 5, 300], dtype=np.int32)
+    q_lens = np.array([3, 1, 8, 2], dtype=np.int32)
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    maxb = int(((seq_lens + 127) // 128).max())
+    B, T = len(seq_lens), int(qsl[-1])
+    num_pages = B * maxb
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, maxb)
+    kv = rng.integers(0, 256, size=(num_pages, 73728), dtype=np.uint8)
+    sel = np.full((T, 4, 16), -1, dtype=np.int32)
+    for b in range(B):
+        for i in range(q_lens[b]):
+            local = (seq_lens[b] - q_lens[b] + i) // 128
+            for g in range(4):
+                sel[qsl[b] + i, g, 0] = local
+                k = min(15, local)
+                if k:
+                    sel[qsl[b] + i, g, 1:1 + k] = rng.choice(local, size=k, replace=False)
+    return qsl, seq_lens, bt, kv, num_pages, sel, maxb
+
+
+def test_host_gather_map_numbers_the_selected_blocks(msa):
+    qsl, seq_lens, bt, kv, num_pages, sel, maxb = _gather_case(3)
+    mp, mk, n = msa.msa_kv_gather_map_host(qsl, seq_lens, maxb, sel)
+    want = np.zeros_like(mk)
+    for b in range(len(seq_lens)):
+        for t in range(qsl[b], qsl[b + 1]):
+            for g in range(4):
+                for v in sel[t, g]:
+                    if v >= 0:
+                        want[b, v] |= 1 << g
+    assert np.array_equal(mk, want)
+    on = want.reshape(-1) != 0
+    assert n == on.sum() and np.array_equal(mp.reshape(-1)[on], np.arange(n))
+    assert np.all(mp.reshape(-1)[~on] == -1)
+    bad = sel.copy()
+    bad[0, 0, 1] = 99  # past sequence 0's blocks
+    with pytest.raises(msa.MsaError):
+        msa.msa_kv_gather_map_host(qsl, seq_lens, maxb, bad)
+
+
+def _gather_rank(rank: int, world: int, port: int, q: "mp.Queue") -> None:
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import nvfp4_kv_cache_gb300 as m
+
+        qsl, seq_lens, bt, kv, num_pages, sel, maxb = _gather_case(3)  # the same on every rank
+        mp, mk, n = m.msa_kv_gather_map_host(qsl, seq_lens, maxb, sel)
+        a, b = _shards(maxb, world)[rank]
+        # this rank holds only the pages of blocks [a, b): its own pool, its own block table
+        held = np.unique(bt[:, a:b])
+        mine_kv = kv[held]
+        local_bt = np.full_like(bt, -1)
+        local_bt[:, a:b] = np.searchsorted(held, bt[:, a:b])
+        pool = np.zeros((max(n, 1), 73728), dtype=np.uint8)
+        m.msa_kv_gather_pages_host(local_bt, mine_kv, len(held), mp, mk, a, b, pool)
+        mine = mp[:, a:b][mp[:, a:b] >= 0]  # the gathered pages this rank filled
+        got = [None] * world
+        dist.all_gather_object(got, (mine, pool[mine]))  # the exchange: only the filled pages move
+        if rank == 0:
+            owner = np.zeros_like(pool)
+            for idx, pages in got:
+                owner[idx] = pages
+            full = np.zeros_like(pool)
+            m.msa_kv_gather_pages_host(bt, kv, num_pages, mp, mk, 0, maxb, full)
+            q.put((owner, full, mp, mk, bt, kv))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gloo_two_ranks_gather_the_selected_pages():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    owner, full, gmap, masks, bt, kv = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # the owner's pool equals the unsharded gather, and every selected region is the source page's
+    assert np.array_equal(owner, full)
+    B, maxb = gmap.shape
+    for b in range(B):
+        for blk in range(maxb):
+            for g in range(4):
+                if masks[b, blk] & (1 << g):
+                    r = slice(g * 18432, (g + 1) * 18432)
+                    assert np.array_equal(owner[gmap[b, blk], r], kv[bt[b, blk], r])

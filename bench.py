@@ -298,9 +298,15 @@ def time_prefill(msa, steps: int, warmup: int, flush, dev):
     torch.cuda.synchronize()
     assert msa.status_bits(st) == 0
     us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
-    blocks = len({(g, int(k)) for g in range(4) for k in np.unique(sel_np[:, g][sel_np[:, g] >= 0])})
+    rows, chunks, entries, _ = wsp[:16].view(torch.int32).cpu().tolist()
+    # algorithmic bytes: each (page, group) block's K and V once, the query heads once, the
+    # per-selection partials written and read back (4 KB of f16 o + 128 B of (m, l)), the output
+    partial = entries * (4096 + 128)
+    algo = rows * 18432 + wp.T * 64 * 128 + 2 * partial + wp.T * 64 * 128 * 2
     return {"workload": wp.name, "us_per_call": us, "tokens_per_s": wp.T / us * 1e6,
-            "distinct_blocks_read": blocks, "kv_bytes_algorithmic": blocks * 18432,
+            "distinct_blocks_read": rows, "kv_dequantisations": chunks, "selections_served": entries,
+            "kv_bytes_algorithmic": rows * 18432, "bytes_algorithmic": algo,
+            f"hbm_frac_of_{peaks()[1]}": algo / (us * 1e-6) / 1e9 / peaks()[0],
             "selections": "local block + 15 distinct earlier blocks drawn uniformly per (token, group)"}
 
 

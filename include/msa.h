@@ -346,23 +346,30 @@ msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_bat
 /* Size in bytes of the device array msa_sparse_attn_decode_noalloc uses. */
 size_t msa_noalloc_scratch_bytes(void);
 
-/* Workspace bytes msa_prefill_attn needs: the block -> query map (B x 4 x max_blocks_per_seq
- * rows, T x 64 entries) and the per-(token, group, slot) partial results, about 1 MB a query
- * token (T up to 2^22). 0 for invalid arguments. */
+/* Workspace bytes msa_prefill_attn needs: a hash table and the selection lists of the key-block
+ * -> query map, and the per-(token, group, slot) partial results (4 KB of unnormalised output and
+ * 128 B of (max, sum) per slot): about 300 KB a query token, a function of T alone (T up to
+ * 2^22; B and max_blocks_per_seq are checked only). 0 for invalid arguments. */
 size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B, int32_t T,
                                   int32_t max_blocks_per_seq);
 
 /* Sparse GQA attention for any number of query tokens per sequence (the prefill / many-query
  * path: "MiniMax M3 in vLLM ...", "预填充": block-major, a block's K and V read and dequantised
- * once for all the queries that selected it, per-block results merged by log-sum-exp). Same
- * result as msa_sparse_attn_decode for the same inputs (up to summation order); the batch may
- * hold up to 2^20 query tokens per sequence (max_q_len) and 2^22 in all (T).
+ * once for all the queries that selected it, per-block results merged by log-sum-exp). The map
+ * is keyed by the physical page, so a page that several sequences share through a common prefix
+ * is dequantised once for up to 64 of the (token, group) selections of all of them ("vLLM ofrece
+ * soporte en día 0 ...", "NVFP4 MSA kernel"). Same result as msa_sparse_attn_decode for the same
+ * inputs (up to summation order); the batch may hold up to 2^20 query tokens per sequence
+ * (max_q_len) and 2^22 in all (T).
  *   q, sel      as for msa_sparse_attn_decode ([T][64][128] E4M3, [T][4][16] int32)
- *   workspace   device, 256-B aligned, >= msa_prefill_workspace_size(...) bytes
+ *   workspace   device, 256-B aligned, >= msa_prefill_workspace_size(...) bytes. When the call's
+ *               work has run, its first four int32 hold the map's counts: distinct (page, group)
+ *               blocks selected, chunks of at most 64 selections (one K/V dequantisation each),
+ *               selections served, and a chunk counter of the kernel's own
  *   out         [T][64][128] bf16, device
  *   status      nullable; an out-of-range selected block or a bad page id sets
  *               MSA_ERR_DEVICE_FAULT and zero-fills that (token, group); an inconsistent batch
- *               row sets MSA_ERR_INVALID_ARG
+ *               row sets MSA_ERR_INVALID_ARG; a device wait that gives up sets MSA_ERR_TIMEOUT
  * Host-checkable errors return before any launch. */
 msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
                             const uint8_t* q, const int32_t* sel, float softmax_scale,

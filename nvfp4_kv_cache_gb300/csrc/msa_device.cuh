@@ -121,6 +121,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// L2 policy for data that several CTAs read again soon (evict last).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 2-D tiled tensor copy global -> shared of the tensor map's box at element (x, y), completing
 // its bytes on `bar`, with an L2 cache hint. x * element size must be a multiple of 16 B.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,

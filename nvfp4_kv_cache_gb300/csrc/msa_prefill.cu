@@ -1,5 +1,5 @@
-// msa_prefill.cu — the many-query (prefill) sparse attention: block-major, with a key -> query
-// map and a log-sum-exp merge.
+// msa_prefill.cu — the many-query (prefill) sparse attention: block-major, with a key-block ->
+// query map and a log-sum-exp merge, on the fifth-generation tensor cores.
 //
 // What it computes: the same exact sparse GQA attention as msa_sparse_attn_decode ("vLLM ofrece
 // soporte en día 0 para MiniMax-M3.1-Flash", "MSA primer": every query head of a group attends
@@ -7,16 +7,22 @@
 // for any number of query tokens per sequence. The pages' prefill kernel is block-major ("MiniMax
 // M3 in vLLM ...", "预填充": a block's keys are read and dequantised once for all the queries that
 // selected it, through a key-block -> query map, and each query's per-block results are merged
-// by log-sum-exp); so is this one:
-//  1. k_map_count / k_map_scan / k_map_fill: the CSR map from every (sequence, group, block) to
-//     the (token, slot) entries that selected it (a token's repeated block counts once; an
-//     out-of-range block or a bad page marks the (token, group) bad);
-//  2. k_prefill_attn: one CTA of 8 warps per (sequence, group, block) with entries: one 3-D
-//     tensor copy of the block's K and V regions, the K rows dequantised to an E4M3 tile and
-//     the V rows to an f16 tile (shared memory, swizzled) once, then each warp takes entries:
-//     the 16 heads of the entry's token attend over the block's 128 keys (mma.sync e4m3 QK^T,
-//     online softmax, mma.sync f16 PV) and the (lse, o) partial goes to the entry's slot (o
-//     normalised, in f16: half the partial traffic of fp32);
+// by log-sum-exp), and their NVFP4 attention kernel dequantises a page that several requests
+// share through a common prefix once for up to 64 of them ("vLLM ofrece soporte en día 0 ...",
+// "NVFP4 MSA kernel"). Both hold here because the map is keyed by the physical page:
+//  1. k_map_count / k_map_alloc / k_map_fill: every valid (token, group, slot) selection (a
+//     token's repeated block counts once; an out-of-range block or a bad page marks the (token,
+//     group) bad) is filed under the key (physical page, group) through an open-addressing hash
+//     table, so the selections of every sequence whose block table points at the same page land
+//     in one row. Each row's selections are cut into chunks of at most 64;
+//  2. k_prefill_tc: one persistent CTA per SM takes chunks in turn. A chunk's K and V regions are
+//     copied (one 3-D tensor copy) and dequantised once, K to an E4M3 K-major tile and V to an
+//     E4M3 tile in place of the MN-major operand; then each tile of 8 selections (8 x 16 query
+//     heads = M 128) runs S = Q K^T (tcgen05.mma kind::f8f6f4, both operands in shared memory,
+//     N = 128 keys), a softmax over the block's 128 keys (one thread per query-head row), and
+//     O^T = V^T P^T with P split into hi = E4M3(P) and lo = E4M3(16 (P - hi)) (N = 256: the hi
+//     and the lo rows of all 128 heads). The (m, l) of every row and its unnormalised o go to
+//     the selection's slot;
 //  3. k_prefill_merge: per (token, group), the log-sum-exp merge of its up to 16 partials.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -33,13 +39,34 @@
 namespace msa {
 namespace {
 
-constexpr int kPfWarps = 8;
-constexpr int kPfThreads = 32 * kPfWarps;
-constexpr int kStage = 2 * kRegion;   // K region then V region of one (page, group)
-constexpr int kKTile = kBS * kD;      // 128 keys x 128 E4M3
-constexpr int kVTile = kBS * kD * 2;  // 128 keys x 128 f16
-constexpr int kMaxQ = 1 << 20;        // query tokens per sequence
-constexpr int kMaxT = 1 << 22;        // query tokens per call (entries pack t << 4 | slot)
+constexpr int kChunk = 64;             // selections served by one dequantised (page, group) block
+constexpr int kTileSel = 8;            // selections per MMA tile: 8 x 16 query heads = M 128
+constexpr int kMaxQ = 1 << 20;         // query tokens per sequence
+constexpr int kMaxT = 1 << 22;         // query tokens per call (entries pack t << 4 | slot)
+constexpr uint64_t kNoKey = ~0ull;     // an empty hash slot
+constexpr float kLoScale = 16.0f;      // the lo rows of P hold kLoScale (P - hi)
+constexpr uint32_t kLoScale2 = 0x4C004C00u;  // f16x2 {16, 16}
+
+// Warp roles of k_prefill_tc. A warp reads the TMEM lanes 32 (warp % 4) .. + 31, so the softmax
+// and epilogue groups are aligned sets of four warps.
+constexpr int kWarpProd = 0;   // chunk fetch, entry lists, tensor copies (lane 0)
+constexpr int kWarpIss = 1;    // MMA issue (lane 0); allocates TMEM
+constexpr int kWarpDq = 2;     // two dequant warps
+constexpr int kDqWarps = 2;
+constexpr int kWarpSm = 4;     // two softmax warpgroups (warps 4-7, 8-11): even and odd tiles
+constexpr int kWarpEp = 12;    // two epilogue warpgroups (warps 12-15, 16-19): heads 0-63, 64-127
+constexpr int kThreads = 640;
+constexpr int kMetaSlots = 4;
+// Arrivals that release a chunk's entry list: every dequant, softmax and epilogue warp and the
+// issuer, each after its last use of it.
+constexpr int kMetaUsers = kDqWarps + 8 + 8 + 1;
+
+constexpr int kStage = 2 * kRegion;      // K region then V region of one (page, group), raw
+constexpr int kKTile = kBS * kD;         // 128 keys x 128 E4M3, K-major, 128-byte swizzle
+constexpr int kQTile = kTileSel * kHPG * kD;  // 128 query-head rows x 128 E4M3
+constexpr int kPTile = 2 * 128 * kBS;    // 256 rows (hi heads, then lo heads) x 128 keys E4M3
+constexpr uint32_t kTmemCols = 512;      // S double buffer (2 x 128) + O^T (256)
+constexpr uint32_t kColO = 256;
 
 struct PfParams {
   int32_t B, T, maxb, num_pages;
@@ -51,25 +78,20 @@ struct PfParams {
   float scale_log2;
   uint16_t* out;
   // workspace
-  int32_t* count;    // [B * 4 * maxb] entries of each (sequence, group, block); then fill cursors
-  int32_t* offset;   // [B * 4 * maxb + 1] exclusive prefix of count
-  int32_t* entries;  // [T * 4 * 16] t << 4 | slot, grouped by (sequence, group, block)
-  int32_t* tg_bad;   // [T * 4] the (token, group) saw a bad selection or page: zero output
-  uint32_t* part_o;  // [T * 4 * 16 slots][16 heads][64] normalised partial outputs, f16 pairs
-  float* part_lse;   // [T * 4 * 16 slots][16 heads] their log2-sum-exp (-inf: no partial)
+  int32_t* hdr;        // [0] rows, [1] chunks, [2] entries, [3] chunk fetch counter
+  uint64_t* hkeys;     // [H] page * 4 + group, kNoKey when free
+  int32_t* hcnt;       // [H] selections of the slot's row; then its fill cursor
+  int32_t* rowh;       // [T * 64] hash slot of row r (rows numbered in order of appearance)
+  int32_t* ehash;      // [T * 64] hash slot of each selection, -1: none
+  int2* entries;       // [T * 64] {t << 4 | slot, p_tok - 128 block}, grouped by row
+  int4* chunks;        // [T * 65] {first entry, count, page, group}
+  int32_t* tg_bad;     // [T * 4] the (token, group) saw a bad selection or page: zero output
+  uint32_t* part_o;    // [T * 64 slots][128 dims][16 heads] unnormalised partial o, f16 pairs
+  float2* part_ml;     // [T * 64 slots][16 heads] {m (log2 domain), l}; m = -inf: no partial
+  uint32_t hmask;      // H - 1 (H a power of two)
+  int32_t hbits;       // log2 H
   uint32_t* status;
 };
-
-struct PfSmem {
-  static constexpr size_t kOffStage = 0;
-  static constexpr size_t kOffK = kOffStage + kStage;   // 18,432 = 18 x 1024
-  static constexpr size_t kOffV = kOffK + kKTile;
-  static constexpr size_t kOffLut = kOffV + kVTile;
-  static constexpr size_t kOffBar = kOffLut + 256 * 8;
-  static constexpr size_t kOffMisc = kOffBar + 16;
-  static constexpr size_t kBytes = 1024 + kOffMisc + 16;
-};
-static_assert(PfSmem::kOffK % 1024 == 0, "the stage is 1024-B aligned for the swizzled copy");
 
 // The sequence of token t (largest b with qsl[b] <= t) and whether the batch rows around it are
 // consistent; p_tok = the token's position.
@@ -86,15 +108,16 @@ __device__ __forceinline__ bool token_seq(const PfParams& p, int t, int* b_out, 
   return t - q0 >= 0 && t - q0 < ql && L >= ql && L <= p.maxb * kBS;
 }
 
-// One thread per (token, group, slot): count the first occurrence of each valid selected block.
-// A partial slot starts as "none" (lse -inf); k_prefill_attn overwrites the slots it serves.
+// One thread per (token, group, slot): validate the selection, and file the first occurrence of
+// each valid block under its (page, group) row. Every partial slot starts as "none" (m = -inf).
 __global__ void __launch_bounds__(256) k_map_count(const PfParams p) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
   const int t = static_cast<int>(e / (4 * kSel)), g = static_cast<int>((e / kSel) % 4), slot = static_cast<int>(e % kSel);
-  float* lse = p.part_lse + e * kHPG;
+  float2* ml = p.part_ml + e * kHPG;
 #pragma unroll
-  for (int h = 0; h < kHPG; ++h) lse[h] = -CUDART_INF_F;
+  for (int h = 0; h < kHPG; ++h) ml[h] = make_float2(-CUDART_INF_F, 0.f);
+  p.ehash[e] = -1;
   int b, p_tok, nb;
   if (!token_seq(p, t, &b, &p_tok, &nb)) {
     set_status(p.status, MSA_ERR_INVALID_ARG);
@@ -117,205 +140,621 @@ __global__ void __launch_bounds__(256) k_map_count(const PfParams p) {
     p.tg_bad[t * 4 + g] = 1;
     return;
   }
-  atomicAdd(&p.count[(static_cast<int64_t>(b) * 4 + g) * p.maxb + v], 1);
+  // linear probing from a multiplicative hash; the table has at least twice as many slots as
+  // there are selections, so a free or matching slot is always found
+  const uint64_t key = static_cast<uint64_t>(ph) * 4 + static_cast<uint64_t>(g);
+  uint32_t h = static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> (64 - p.hbits)) & p.hmask;
+  for (uint32_t probe = 0; probe <= p.hmask; ++probe) {
+    const uint64_t old = atomicCAS(reinterpret_cast<unsigned long long*>(p.hkeys + h), kNoKey, key);
+    if (old == kNoKey) {
+      p.rowh[atomicAdd(&p.hdr[0], 1)] = static_cast<int32_t>(h);
+      break;
+    }
+    if (old == key) break;
+    h = (h + 1) & p.hmask;
+  }
+  atomicAdd(&p.hcnt[h], 1);
+  p.ehash[e] = static_cast<int32_t>(h);
 }
 
-// Exclusive scan of count into offset (one CTA of 1024 threads, each a contiguous run), then
-// count := 0 so that k_map_fill can use it as the rows' cursors.
-__global__ void __launch_bounds__(1024) k_map_scan(const PfParams p, int64_t rows) {
-  __shared__ int64_t part[1024];
-  const int tid = threadIdx.x;
-  const int64_t per = (rows + 1023) / 1024, r0 = tid * per, r1 = rows < r0 + per ? rows : r0 + per;
-  int64_t sum = 0;
-  for (int64_t r = r0; r < r1; ++r) sum += p.count[r];
-  part[tid] = sum;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {  // inclusive Hillis-Steele scan of the 1024 run totals
-    const int64_t v = tid >= o ? part[tid - o] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
+// One thread per row: the row's place in the entry list and its chunks, allocated with one
+// atomic per warp (rows and chunks land in arbitrary order; only their grouping matters).
+__global__ void __launch_bounds__(256) k_map_alloc(const PfParams p) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int nrows = p.hdr[0];
+  if (r - lane >= nrows) return;  // the whole warp is past the last row
+  const bool mine = r < nrows;
+  const int h = mine ? p.rowh[r] : 0;
+  const int c = mine ? p.hcnt[h] : 0;
+  const int nch = (c + kChunk - 1) / kChunk;
+  int ic = c, in = nch;  // inclusive warp scans
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, o), b = __shfl_up_sync(0xffffffffu, in, o);
+    if (lane >= o) {
+      ic += a;
+      in += b;
+    }
   }
-  int64_t run = part[tid] - sum;
-  for (int64_t r = r0; r < r1; ++r) {
-    const int c = p.count[r];
-    p.offset[r] = static_cast<int32_t>(run);
-    run += c;
-    p.count[r] = 0;
+  int base_e = 0, base_c = 0;
+  if (lane == 31) {
+    base_e = atomicAdd(&p.hdr[2], ic);
+    base_c = atomicAdd(&p.hdr[1], in);
   }
-  if (tid == 1023) p.offset[rows] = static_cast<int32_t>(part[1023]);
+  base_e = __shfl_sync(0xffffffffu, base_e, 31);
+  base_c = __shfl_sync(0xffffffffu, base_c, 31);
+  if (!mine) return;
+  const int off = base_e + ic - c, ch0 = base_c + in - nch;
+  p.hcnt[h] = off;  // the fill cursor
+  const uint64_t key = p.hkeys[h];
+  const int ph = static_cast<int>(key >> 2), g = static_cast<int>(key & 3);
+  for (int j = 0; j < nch; ++j) p.chunks[ch0 + j] = make_int4(off + kChunk * j, min(kChunk, c - kChunk * j), ph, g);
 }
 
-// The same threads as k_map_count place their entry in its row.
+// The same threads as k_map_count place their selection in its row: the token and slot, and
+// the query position relative to the block's first key (the mask of the block's keys).
 __global__ void __launch_bounds__(256) k_map_fill(const PfParams p) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
+  const int h = p.ehash[e];
+  if (h < 0) return;
   const int t = static_cast<int>(e / (4 * kSel)), g = static_cast<int>((e / kSel) % 4), slot = static_cast<int>(e % kSel);
   int b, p_tok, nb;
-  if (!token_seq(p, t, &b, &p_tok, &nb)) return;
-  const int32_t* row = p.sel + (static_cast<int64_t>(t) * 4 + g) * kSel;
-  const int v = row[slot];
-  if (v < 0 || v >= nb) return;
-  for (int j = 0; j < slot; ++j)
-    if (row[j] == v) return;
-  const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];
-  if (!(ph >= 0 && ph < p.num_pages)) return;
-  const int64_t r = (static_cast<int64_t>(b) * 4 + g) * p.maxb + v;
-  const int pos = atomicAdd(&p.count[r], 1);
-  p.entries[p.offset[r] + pos] = (t << 4) | slot;
+  token_seq(p, t, &b, &p_tok, &nb);
+  const int v = p.sel[(static_cast<int64_t>(t) * 4 + g) * kSel + slot];
+  const int pos = atomicAdd(&p.hcnt[h], 1);
+  p.entries[pos] = make_int2((t << 4) | slot, p_tok - v * kBS);
 }
 
-// One CTA per (sequence, group, block) row of the map.
-__global__ void __launch_bounds__(kPfThreads) k_prefill_attn(const PfParams p, const __grid_constant__ CUtensorMap tmap) {
-  using S = PfSmem;
+struct ChunkMeta {
+  int32_t n, ph, g, pad;
+  int2 e[kChunk];
+};
+
+struct Smem {
+  static constexpr size_t kOffStage = 0;                                  // [2] raw K+V regions
+  static constexpr size_t kOffK = kOffStage + 2 * static_cast<size_t>(kStage);  // [2] K tiles
+  static constexpr size_t kOffV = kOffK + 2 * static_cast<size_t>(kKTile);      // [2] V tiles
+  static constexpr size_t kOffQ = kOffV + 2 * static_cast<size_t>(kKTile);      // [2] Q tiles
+  static constexpr size_t kOffP = kOffQ + 2 * static_cast<size_t>(kQTile);      // [2] P tiles
+  static constexpr size_t kOffLut = kOffP + 2 * static_cast<size_t>(kPTile);
+  static constexpr size_t kOffMeta = kOffLut + 256 * 8;
+  static constexpr size_t kOffBar = kOffMeta + kMetaSlots * sizeof(ChunkMeta);
+  // barriers: meta full/empty, stage full/empty, tile full/empty, q full/empty, s full/free,
+  // p full/empty (two of each but the meta ring), o full/free, fin
+  static constexpr int kNumBars = 2 * kMetaSlots + 2 * 2 * 5 + 3;
+  static constexpr size_t kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr size_t kBytes = 1024 + kOffMisc + 16;
+};
+static_assert(Smem::kOffK % 1024 == 0 && Smem::kOffQ % 1024 == 0 && Smem::kOffP % 1024 == 0 &&
+                  kRegion % 1024 == 0,
+              "swizzled tiles and copies start on 1024-B boundaries");
+static_assert(Smem::kOffBar % 8 == 0 && Smem::kBytes <= 232448, "shared memory budget");
+
+struct Bars {
+  uint64_t* meta_full;
+  uint64_t* meta_empty;
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* kt_full;
+  uint64_t* kt_empty;
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* s_full;
+  uint64_t* s_free;
+  uint64_t* p_full;
+  uint64_t* p_empty;
+  uint64_t* o_full;
+  uint64_t* o_free;
+  uint64_t* fin;
+  __device__ explicit Bars(uint8_t* smem) {
+    uint64_t* b = reinterpret_cast<uint64_t*>(smem + Smem::kOffBar);
+    meta_full = b;
+    meta_empty = b + kMetaSlots;
+    b += 2 * kMetaSlots;
+    kv_full = b;
+    kv_empty = b + 2;
+    kt_full = b + 4;
+    kt_empty = b + 6;
+    q_full = b + 8;
+    q_empty = b + 10;
+    s_full = b + 12;
+    s_free = b + 14;
+    p_full = b + 16;
+    p_empty = b + 18;
+    o_full = b + 20;
+    o_free = b + 21;
+    fin = b + 22;
+    static_assert(2 * kMetaSlots + 23 == Smem::kNumBars, "barrier area");
+  }
+};
+
+__device__ __forceinline__ int ntiles_of(int n) { return (n + kTileSel - 1) / kTileSel; }
+
+// Persistent: one CTA per SM takes chunks in turn (a global counter). Warp roles:
+//  producer — the chunk's entry list into the meta ring, one tensor copy of its K and V regions,
+//             and per tile one 2 KB tensor copy per selection of its token's 16 query heads;
+//  dequant  — the K rows to an E4M3 K-major tile, the V rows to an E4M3 tile read as the
+//             MN-major A operand of O^T (rows of 128 dims, 128-byte swizzle);
+//  issuer   — S(i) = Q K^T (M 128 heads x N 128 keys) one tile ahead of O^T(i - 1) = V^T P^T
+//             (M 128 dims x N 256 hi/lo head rows);
+//  softmax  — thread = query-head row: the row's max and sum over the block's unmasked keys, P as
+//             hi and lo E4M3 rows, and the row's (m, l) to its slot;
+//  epilogue — thread = dim: o = hi + lo / 16 of every head to its slot, f16.
+// Every wait is bounded (MSA_ERR_TIMEOUT, then every role leaves); nothing traps.
+__global__ void __launch_bounds__(kThreads, 1)
+    k_prefill_tc(const PfParams p, const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  const int64_t r = blockIdx.x;
-  const int e0 = p.offset[r], n = p.offset[r + 1] - e0;
-  if (n == 0) return;
-  const int v = static_cast<int>(r % p.maxb);
-  const int g = static_cast<int>((r / p.maxb) % 4);
-  const int b = static_cast<int>(r / (4 * static_cast<int64_t>(p.maxb)));
-  const int ph = p.block_table[static_cast<int64_t>(b) * p.maxb + v];  // checked by k_map_count
+  const Bars bars(smem);
+  ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + Smem::kOffMeta);
+  uint2* lut = reinterpret_cast<uint2*>(smem + Smem::kOffLut);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::kOffMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  volatile int* fail = reinterpret_cast<volatile int*>(smem + S::kOffMisc);
-  uint2* lut = reinterpret_cast<uint2*>(smem + S::kOffLut);
+  const int nchunks = p.hdr[1];
+
   if (tid == 0) {
-    mbar_init(bar, 1);
+    for (int i = 0; i < kMetaSlots; ++i) {
+      mbar_init(&bars.meta_full[i], 1);
+      mbar_init(&bars.meta_empty[i], kMetaUsers);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_empty[i], kDqWarps);
+      mbar_init(&bars.kt_full[i], kDqWarps);
+      mbar_init(&bars.kt_empty[i], 1);
+      mbar_init(&bars.q_full[i], 1);
+      mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], 4);  // the four warps of the tile's softmax warpgroup
+      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.p_empty[i], 1);
+    }
+    mbar_init(bars.o_full, 1);
+    mbar_init(bars.o_free, 8);  // both epilogue warpgroups
+    mbar_init(bars.fin, 1);
     fence_mbar_init();
-    *fail = 0;
-    mbar_arrive_expect_tx(bar, kStage);
-    tma_load_3d(smem + S::kOffStage, &tmap, 0, 2 * g * (kRegion / kD), ph, bar);
+    *abort_flag = 0;
   }
-  build_dequant_lut(lut, tid, kPfThreads);
+  {
+    // Q tiles start as zeros: rows of a short tile's missing selections then hold finite values
+    uint4* qz = reinterpret_cast<uint4*>(smem + Smem::kOffQ);
+    for (int i = tid; i < 2 * kQTile / 16; i += kThreads) qz[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == kWarpIss) tmem_alloc(tmem_slot, kTmemCols);
+  build_dequant_lut(lut, tid, kThreads);
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  // thread = key row: K rows (threads 0..127) -> E4M3 tile, V rows (128..255) -> f16 tile
-  const bool ok_copy = mbar_wait(bar, 0u, nullptr);
-  if (!ok_copy) *fail = 1;
-  if (ok_copy) {
-    const int kr = tid & 127;
-    RawRow raw;
-    if (tid < 128) {
-      load_row(smem + S::kOffStage, kr, raw);
-      uint8_t* kt = smem + S::kOffK;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[8];
-        dequant_quarter(raw, q, lut, w);
-        *reinterpret_cast<uint4*>(kt + kr * kD + (((2 * q) ^ (kr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(kt + kr * kD + (((2 * q + 1) ^ (kr & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // A warp's bounded wait; on a time-out the first to notice reports it and every role leaves.
+  auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (warp_wait(bar, parity, abort_flag)) return true;
+    if (lane == 0) {
+      if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    return false;
+  };
+
+  if (warp == kWarpProd) {
+    // ---- producer ---------------------------------------------------------------------------
+    if (lane == 0) {
+      prefetch_tensormap(&kv_map);
+      prefetch_tensormap(&q_map);
+    }
+    const uint64_t pol = policy_evict_last();  // a token's query heads serve up to 16 chunks
+    int k = 0, i = 0, kvn = 0;  // chunks taken, query tiles and K/V copies issued
+    for (;; ++k) {
+      int c = 0;
+      if (lane == 0) c = atomicAdd(&p.hdr[3], 1);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_empty[ms], (static_cast<uint32_t>(k / kMetaSlots) & 1u) ^ 1u)) break;
+      ChunkMeta& m = meta[ms];
+      if (c >= nchunks) {
+        if (lane == 0) {
+          m.n = -1;
+          mbar_arrive(&bars.meta_full[ms]);
+        }
+        break;
       }
-    } else {
-      load_row(smem + S::kOffStage + kRegion, kr, raw);
-      uint8_t* vt = smem + S::kOffV;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[8];
-        dequant_quarter(raw, q, lut, w);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint4 x = make_uint4(cvt_f16x2_e4m3x2(w[2 * h]), cvt_f16x2_e4m3x2(w[2 * h] >> 16),
-                                     cvt_f16x2_e4m3x2(w[2 * h + 1]), cvt_f16x2_e4m3x2(w[2 * h + 1] >> 16));
-          *reinterpret_cast<uint4*>(vt + kr * (2 * kD) + (((4 * q + h) ^ (kr & 7)) << 4)) = x;
+      const int4 ch = p.chunks[c];
+      for (int e = lane; e < ch.y; e += 32) m.e[e] = p.entries[ch.x + e];
+      if (lane == 0) {
+        m.n = ch.y;
+        m.ph = ch.z;
+        m.g = ch.w;
+      }
+      __syncwarp();
+      bool ok = true;
+      if (lane == 0) {
+        __threadfence_block();
+        mbar_arrive(&bars.meta_full[ms]);
+        const int s = k & 1;
+        ok = mbar_wait(&bars.kv_empty[s], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars.kv_full[s], kStage);
+          tma_load_3d(smem + Smem::kOffStage + static_cast<size_t>(s) * kStage, &kv_map, 0, 2 * ch.w * (kRegion / kD),
+                      ch.z, &bars.kv_full[s]);
+          ++kvn;
+        }
+        for (int j = 0; ok && j < ntiles_of(ch.y); ++j, ++i) {
+          ok = mbar_wait(&bars.q_empty[i & 1], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag);
+          if (!ok) break;
+          const int ne = min(kTileSel, ch.y - kTileSel * j);
+          mbar_arrive_expect_tx(&bars.q_full[i & 1], static_cast<uint32_t>(ne) * kHPG * kD);
+          uint8_t* qt = smem + Smem::kOffQ + static_cast<size_t>(i & 1) * kQTile;
+          for (int e = 0; e < ne; ++e) {
+            const int t = m.e[kTileSel * j + e].x >> 4;
+            tma_load_2d(qt + e * kHPG * kD, &q_map, 0, t * kQHeads + ch.w * kHPG, &bars.q_full[i & 1], pol);
+          }
+        }
+        if (!ok) {
+          if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
+          *abort_flag = 1;
         }
       }
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
     }
-  }
-  __syncthreads();
-  if (*fail) {
-    if (tid == 0) set_status(p.status, MSA_ERR_TIMEOUT);
-    return;
-  }
-  const int gid = lane >> 2, tq = lane & 3;
-  const int q0 = p.qsl[b], ql = p.qsl[b + 1] - q0, L = p.seq_lens[b];
-  for (int e = warp; e < n; e += kPfWarps) {
-    const int ent = p.entries[e0 + e];
-    const int t = ent >> 4, slot = ent & 15;
-    const int p_tok = L - ql + (t - q0);
-    WarpState st;
-    st.m[0] = st.m[1] = -CUDART_INF_F;
-    st.l[0] = st.l[1] = 0.f;
+    // never leave while a copy into this CTA's shared memory may still be in flight
+    if (lane == 0) {
+      for (int j = kvn > 2 ? kvn - 2 : 0; j < kvn; ++j)
+        if (!mbar_wait_bounded(&bars.kv_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
+      for (int j = i > 2 ? i - 2 : 0; j < i; ++j)
+        if (!mbar_wait_bounded(&bars.q_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
+          set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+  } else if (warp == kWarpIss) {
+    // ---- MMA issuer: S one tile ahead of O^T ----------------------------------------------------
+    constexpr uint32_t idesc_s = idesc_e4m3_f32(128, 128);
+    constexpr uint32_t idesc_o = idesc_e4m3_f32_amn(128, 256);
+    struct Tile {
+      int k, j, nt, i;
+    };
+    bool ok = true, issued = false;
+    // the next tile after `t` (t.nt == 0: before the first chunk); false at the end or on abort
+    auto next = [&](Tile& t) -> bool {
+      if (t.nt > 0 && t.j + 1 < t.nt) {
+        ++t.j;
+        ++t.i;
+        return true;
+      }
+      const int k = t.nt > 0 ? t.k + 1 : 0;
+      if (!wwait(&bars.meta_full[k % kMetaSlots], static_cast<uint32_t>(k / kMetaSlots) & 1u)) {
+        ok = false;
+        return false;
+      }
+      const int n = meta[k % kMetaSlots].n;
+      if (n < 0) return false;
+      t.i = t.nt > 0 ? t.i + 1 : 0;
+      t.k = k;
+      t.j = 0;
+      t.nt = ntiles_of(n);
+      return true;
+    };
+    auto issue_s = [&](const Tile& t) -> bool {
+      if (t.j == 0 && !wwait(&bars.kt_full[t.k & 1], static_cast<uint32_t>(t.k >> 1) & 1u)) return false;
+      if (!wwait(&bars.q_full[t.i & 1], static_cast<uint32_t>(t.i >> 1) & 1u)) return false;
+      if (!wwait(&bars.s_free[t.i & 1], (static_cast<uint32_t>(t.i >> 1) & 1u) ^ 1u)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + Smem::kOffQ + static_cast<size_t>(t.i & 1) * kQTile));
+        const uint64_t dk = sw128_kmajor_desc(smem_u32(smem + Smem::kOffK + static_cast<size_t>(t.k & 1) * kKTile));
 #pragma unroll
-    for (int k = 0; k < 16; ++k) st.o[k][0] = st.o[k][1] = st.o[k][2] = st.o[k][3] = 0.f;
-    uint32_t qa[4][4];
-    {
-      const uint8_t* qrow0 = p.q + (static_cast<int64_t>(t) * kQHeads + g * kHPG + gid) * kD + 4 * tq;
-      const uint8_t* qrow1 = qrow0 + 8 * kD;
+        for (int kk = 0; kk < 4; ++kk)  // K = 32 dims per MMA: +32 B in both operands' atoms
+          tc_mma_f8(tmem + 128u * static_cast<uint32_t>(t.i & 1), dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+        tc_commit(&bars.s_full[t.i & 1]);
+        tc_commit(&bars.q_empty[t.i & 1]);
+      }
+      __syncwarp();
+      issued = true;
+      return true;
+    };
+    auto issue_o = [&](const Tile& t) -> bool {
+      if (!wwait(&bars.p_full[t.i & 1], static_cast<uint32_t>(t.i >> 1) & 1u)) return false;
+      if (!wwait(bars.o_free, (static_cast<uint32_t>(t.i) & 1u) ^ 1u)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t va = smem_u32(smem + Smem::kOffV + static_cast<size_t>(t.k & 1) * kKTile);
+        const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + Smem::kOffP + static_cast<size_t>(t.i & 1) * kPTile));
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        qa[s][0] = ldg_nc32(qrow0 + 32 * s);
-        qa[s][1] = ldg_nc32(qrow1 + 32 * s);
-        qa[s][2] = ldg_nc32(qrow0 + 32 * s + 16);
-        qa[s][3] = ldg_nc32(qrow1 + 32 * s + 16);
+        for (int kk = 0; kk < 4; ++kk)  // K = 32 keys per MMA: 32 rows (4 KB) of V, +32 B of P
+          tc_mma_f8(tmem + kColO, sw128_mnmajor8_desc(va + 4096 * kk), dp + 2 * kk, idesc_o, kk > 0 ? 1u : 0u);
+        tc_commit(bars.o_full);
+        tc_commit(&bars.p_empty[t.i & 1]);
+        if (t.j + 1 == t.nt) tc_commit(&bars.kt_empty[t.k & 1]);  // the chunk's tiles are free
+      }
+      __syncwarp();
+      if (t.j + 1 == t.nt && lane == 0) mbar_arrive(&bars.meta_empty[t.k % kMetaSlots]);
+      return true;
+    };
+    Tile cur = {0, 0, 0, 0};
+    bool have = next(cur);
+    if (have) ok = issue_s(cur);
+    while (have && ok) {
+      Tile prev = cur;
+      have = next(cur);
+      if (have && ok) ok = issue_s(cur);
+      if (ok) ok = issue_o(prev);
+    }
+    // nothing of this thread's is in flight when the CTA ends
+    if (lane == 0 && issued) {
+      tc_commit(bars.fin);
+      if (!mbar_wait_bounded(bars.fin, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+  } else if (warp < kWarpSm) {
+    // ---- dequant warps: K rows to the K tile, V rows to the V tile ---------------------------------
+    const int dt = tid - 32 * kWarpDq;
+    for (int k = 0;; ++k) {
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_full[ms], static_cast<uint32_t>(k / kMetaSlots) & 1u)) break;
+      const int n = meta[ms].n;
+      if (n < 0) break;
+      const int s = k & 1;
+      if (!wwait(&bars.kv_full[s], static_cast<uint32_t>(k >> 1) & 1u)) break;
+      if (!wwait(&bars.kt_empty[s], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
+      const uint8_t* stage = smem + Smem::kOffStage + static_cast<size_t>(s) * kStage;
+      for (int r = dt; r < 2 * kBS; r += 32 * kDqWarps) {  // 4 rows a thread
+        const int rr = r & (kBS - 1);
+        RawRow raw;
+        load_row(stage + (r < kBS ? 0 : kRegion), rr, raw);
+        uint8_t* tile = smem + (r < kBS ? Smem::kOffK : Smem::kOffV) + static_cast<size_t>(s) * kKTile;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          uint32_t w[8];
+          dequant_quarter(raw, qd, lut, w);
+          *reinterpret_cast<uint4*>(tile + sw128_chunk_off(rr, 2 * qd)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(tile + sw128_chunk_off(rr, 2 * qd + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+      fence_proxy_async_smem();  // the tiles are read by the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars.kv_empty[s]);
+        mbar_arrive(&bars.kt_full[s]);
+        mbar_arrive(&bars.meta_empty[ms]);
       }
     }
-    attend_tile(st, qa, smem + S::kOffK, smem + S::kOffV, v * kBS, p_tok, p.scale_log2, 0, 4, lane);
-    // the partial of (t, g, slot): o / l per head and log2(sum) + m
-    const float l0 = quad_sum(st.l[0]), l1 = quad_sum(st.l[1]);
-    const int64_t base = (static_cast<int64_t>(t) * 4 + g) * kSel + slot;
-    uint32_t* po = p.part_o + base * kHPG * (kD / 2);  // f16 pairs: dims 2c, 2c + 1 in word c
-    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  } else if (warp < kWarpEp) {
+    // ---- softmax warpgroup x (tiles i with i % 2 == x): thread = query-head row 32 q + lane ------
+    const int x = (warp - kWarpSm) >> 2, qw = warp & 3;
+    const int row = 32 * qw + lane, sel_in_tile = row >> 4, head = row & 15;
+    const uint32_t lanes = static_cast<uint32_t>(32 * qw) << 16;
+    const float c = p.scale_log2;
+    int i = 0;
+    for (int k = 0;; ++k) {
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_full[ms], static_cast<uint32_t>(k / kMetaSlots) & 1u)) break;
+      const ChunkMeta& m = meta[ms];
+      const int n = m.n;
+      if (n < 0) break;
+      bool ok = true;
+      for (int j = 0; j < ntiles_of(n); ++j, ++i) {
+        if ((i & 1) != x) continue;
+        const int idx = kTileSel * j + sel_in_tile;
+        const bool valid = idx < n;
+        const int2 ent = valid ? m.e[idx] : make_int2(0, -1);
+        const int rel = ent.y;  // keys after rel are masked (all of them when rel < 0)
+        if (!(ok = wwait(&bars.s_full[x], static_cast<uint32_t>(i >> 1) & 1u))) break;
+        tc_fence_after();
+        const uint32_t ts = tmem + 128u * static_cast<uint32_t>(x) + lanes;
+        const bool full = __all_sync(0xffffffffu, rel >= kBS - 1);  // no key of the warp's rows masked
+        float mr = -CUDART_INF_F;  // the row's max raw score over its unmasked keys
+#pragma unroll 1
+        for (int cc = 0; cc < 4; cc += 2) {  // two loads in flight per wait
+          uint32_t r[2][32];
+          tmem_ld32(ts + 32 * cc, r[0]);
+          tmem_ld32(ts + 32 * cc + 32, r[1]);
+          tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      po[gid * (kD / 2) + 4 * k + tq] = pack_f16x2(st.o[k][0] * i0, st.o[k][1] * i0);
-      po[(gid + 8) * (kD / 2) + 4 * k + tq] = pack_f16x2(st.o[k][2] * i1, st.o[k][3] * i1);
+          for (int h = 0; h < 2; ++h) {
+            if (full) {
+#pragma unroll
+              for (int u = 0; u < 32; u += 4)
+                mr = fmaxf(mr, max3f(__uint_as_float(r[h][u]), __uint_as_float(r[h][u + 1]),
+                                     fmaxf(__uint_as_float(r[h][u + 2]), __uint_as_float(r[h][u + 3]))));
+            } else {
+#pragma unroll
+              for (int u = 0; u < 32; ++u)
+                if (32 * (cc + h) + u <= rel) mr = fmaxf(mr, __uint_as_float(r[h][u]));
+            }
+          }
+        }
+        const float mx = mr * c;  // c > 0: the max of the scaled scores
+        const float mu = mx == -CUDART_INF_F ? 0.f : mx;
+        if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+        uint8_t* pt = smem + Smem::kOffP + static_cast<size_t>(x) * kPTile;
+        float l = 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[1][32];
+          tmem_ld32(ts + 32 * cc, r[0]);
+          tmem_wait_ld();
+          {
+            constexpr int h = 0;
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {  // 16 keys: one 16-byte chunk of the hi row and of the lo row
+              uint32_t hw[4], lw[4];
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                const int u = 16 * hq + 4 * u4;
+                float pv[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  pv[v] = fast_exp2(fmaf(__uint_as_float(r[h][u + v]), c, -mu));
+                  if (!full && 32 * cc + u + v > rel) pv[v] = 0.f;
+                }
+                l += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                const uint32_t h01 = cvt_e4m3x2(pv[0], pv[1]), h23 = cvt_e4m3x2(pv[2], pv[3]);
+                const uint32_t r01 = sub_f16x2(pack_f16x2(pv[0], pv[1]), cvt_f16x2_e4m3x2(h01));
+                const uint32_t r23 = sub_f16x2(pack_f16x2(pv[2], pv[3]), cvt_f16x2_e4m3x2(h23));
+                const uint32_t l01 = cvt_e4m3x2_f16x2(mul_f16x2(r01, kLoScale2));
+                const uint32_t l23 = cvt_e4m3x2_f16x2(mul_f16x2(r23, kLoScale2));
+                hw[u4] = h01 | (h23 << 16);
+                lw[u4] = l01 | (l23 << 16);
+              }
+              *reinterpret_cast<uint4*>(pt + sw128_chunk_off(row, 2 * cc + hq)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(pt + sw128_chunk_off(128 + row, 2 * cc + hq)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();  // P is read by the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars.s_free[x]);
+          mbar_arrive(&bars.p_full[x]);
+        }
+        if (valid) {
+          const int t = ent.x >> 4, slot = ent.x & 15;
+          const int64_t base = (static_cast<int64_t>(t) * 4 + m.g) * kSel + slot;
+          p.part_ml[base * kHPG + head] = make_float2(l > 0.f ? mx : -CUDART_INF_F, l);
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bars.meta_empty[ms]);
     }
-    if (tq == 0) {
-      p.part_lse[base * kHPG + gid] = l0 > 0.f ? st.m[0] + __log2f(l0) : -CUDART_INF_F;
-      p.part_lse[base * kHPG + gid + 8] = l1 > 0.f ? st.m[1] + __log2f(l1) : -CUDART_INF_F;
+  } else {
+    // ---- epilogue warpgroup y (heads 64 y .. 64 y + 63): thread = dim 32 q + lane, o = hi + lo / 16
+    const int y = (warp - kWarpEp) >> 2, qw = warp & 3;
+    const int d = 32 * qw + lane;
+    const uint32_t lanes = static_cast<uint32_t>(32 * qw) << 16;
+    int i = 0;
+    for (int k = 0;; ++k) {
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_full[ms], static_cast<uint32_t>(k / kMetaSlots) & 1u)) break;
+      const ChunkMeta& m = meta[ms];
+      const int n = m.n;
+      if (n < 0) break;
+      bool ok = true;
+      for (int j = 0; j < ntiles_of(n); ++j, ++i) {
+        if (!(ok = wwait(bars.o_full, static_cast<uint32_t>(i) & 1u))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {  // heads 32 hc .. 32 hc + 31: selections 2 hc, 2 hc + 1
+          const int hc = 2 * y + hh;
+          uint32_t hi[32], lo[32];
+          tmem_ld32(tmem + kColO + 32 * hc + lanes, hi);
+          tmem_ld32(tmem + kColO + 128 + 32 * hc + lanes, lo);
+          tmem_wait_ld();
+          if (hh == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_free);
+          }
+#pragma unroll
+          for (int ee = 0; ee < 2; ++ee) {
+            const int idx = kTileSel * j + 2 * hc + ee;
+            if (idx >= n) continue;
+            const int2 ent = m.e[idx];
+            const int t = ent.x >> 4, slot = ent.x & 15;
+            const int64_t base = (static_cast<int64_t>(t) * 4 + m.g) * kSel + slot;
+            uint32_t w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float o0 = fmaf(__uint_as_float(lo[16 * ee + 2 * u]), 1.0f / kLoScale, __uint_as_float(hi[16 * ee + 2 * u]));
+              const float o1 =
+                  fmaf(__uint_as_float(lo[16 * ee + 2 * u + 1]), 1.0f / kLoScale, __uint_as_float(hi[16 * ee + 2 * u + 1]));
+              w[u] = pack_f16x2(o0, o1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.part_o + (base * kD + d) * (kHPG / 2));
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bars.meta_empty[ms]);
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpIss) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// One warp per (token, head): out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) over the
-// token's partials; zero when the (token, group) is bad or has none.
-__global__ void __launch_bounds__(256) k_prefill_merge(const PfParams p) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // t * 64 + h
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<int64_t>(p.T) * kQHeads) return;
-  const int t = static_cast<int>(row / kQHeads), h = static_cast<int>(row % kQHeads), g = h / kHPG, hh = h % kHPG;
-  const int64_t base = (static_cast<int64_t>(t) * 4 + g) * kSel;
-  float M = -CUDART_INF_F;
-  for (int s = 0; s < kSel; ++s) M = fmaxf(M, p.part_lse[(base + s) * kHPG + hh]);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float W = 0.f;
-  if (M != -CUDART_INF_F && !p.tg_bad[t * 4 + g]) {
+// One CTA of 128 threads (thread = dim) per (token, group): out = sum_s 2^(m_s - M) o_s /
+// sum_s 2^(m_s - M) l_s per head over the selection's partials; zero when the (token, group) is
+// bad or has none.
+__global__ void __launch_bounds__(128) k_prefill_merge(const PfParams p) {
+  __shared__ float2 ml[kSel][kHPG];
+  __shared__ float wt[kSel][kHPG];
+  __shared__ float winv[kHPG];
+  __shared__ int any[kSel];
+  const int tg = blockIdx.x, t = tg >> 2, g = tg & 3, d = threadIdx.x;
+  const int64_t base = static_cast<int64_t>(tg) * kSel;
+  for (int x = d; x < kSel * kHPG; x += 128) ml[x / kHPG][x % kHPG] = p.part_ml[base * kHPG + x];
+  __syncthreads();
+  const bool bad = p.tg_bad[tg] != 0;
+  if (d < kHPG) {
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < kSel; ++s) M = fmaxf(M, ml[s][d].x);
+    float W = 0.f;
     for (int s = 0; s < kSel; ++s) {
-      const float lse = p.part_lse[(base + s) * kHPG + hh];
-      if (lse == -CUDART_INF_F) continue;
-      const float w = fast_exp2(lse - M);
-      const uint2 ov = *reinterpret_cast<const uint2*>(p.part_o + ((base + s) * kHPG + hh) * (kD / 2) + 2 * lane);
-      const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&ov.x));
-      const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&ov.y));
-      acc.x += w * o01.x;
-      acc.y += w * o01.y;
-      acc.z += w * o23.x;
-      acc.w += w * o23.y;
-      W += w;
+      const float w = (M == -CUDART_INF_F || ml[s][d].x == -CUDART_INF_F) ? 0.f : fast_exp2(ml[s][d].x - M);
+      wt[s][d] = w;
+      W += w * ml[s][d].y;
+    }
+    winv[d] = (W > 0.f && !bad) ? 1.0f / W : 0.f;
+  } else if (d < kHPG + kSel) {
+    const int s = d - kHPG;
+    int a = 0;
+    for (int h = 0; h < kHPG; ++h) a |= ml[s][h].x != -CUDART_INF_F;
+    any[s] = a && !bad;
+  }
+  __syncthreads();
+  float acc[kHPG];
+#pragma unroll
+  for (int h = 0; h < kHPG; ++h) acc[h] = 0.f;
+  for (int s = 0; s < kSel; ++s) {
+    if (!any[s]) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(p.part_o + ((base + s) * kD + d) * (kHPG / 2));
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float2 o = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+      acc[2 * u] = fmaf(wt[s][2 * u], o.x, acc[2 * u]);
+      acc[2 * u + 1] = fmaf(wt[s][2 * u + 1], o.y, acc[2 * u + 1]);
     }
   }
-  const float inv = W > 0.f ? 1.0f / W : 0.f;
-  *reinterpret_cast<uint2*>(p.out + row * kD + 4 * lane) =
-      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  uint16_t* dst = p.out + (static_cast<int64_t>(t) * kQHeads + g * kHPG) * kD + d;
+#pragma unroll
+  for (int h = 0; h < kHPG; ++h) dst[h * kD] = static_cast<uint16_t>(pack_bf16x2(acc[h] * winv[h], 0.f) & 0xFFFFu);
 }
 
 struct PfLayout {
-  size_t count, offset, entries, tg_bad, part_o, part_lse, total;
+  size_t hdr, hkeys, hcnt, rowh, ehash, entries, chunks, tg_bad, part_o, part_ml, total;
+  uint32_t hslots;
+  int hbits;
 };
 
-PfLayout pf_layout(int B, int T, int maxb) {
+PfLayout pf_layout(int T) {
   using msa_host::align256;
   PfLayout l;
-  const size_t rows = static_cast<size_t>(B) * 4 * maxb;
   const size_t ent = static_cast<size_t>(T) * 4 * kSel;
-  l.count = 0;
-  l.offset = l.count + align256(rows * 4);
-  l.entries = l.offset + align256((rows + 1) * 4);
-  l.tg_bad = l.entries + align256(ent * 4);
+  l.hbits = 10;
+  while ((size_t{1} << l.hbits) < 2 * ent) ++l.hbits;
+  l.hslots = static_cast<uint32_t>(size_t{1} << l.hbits);
+  l.hdr = 0;
+  l.hkeys = l.hdr + 256;
+  l.hcnt = l.hkeys + align256(static_cast<size_t>(l.hslots) * 8);
+  l.rowh = l.hcnt + align256(static_cast<size_t>(l.hslots) * 4);
+  l.ehash = l.rowh + align256(ent * 4);
+  l.entries = l.ehash + align256(ent * 4);
+  l.chunks = l.entries + align256(ent * 8);
+  l.tg_bad = l.chunks + align256((ent + static_cast<size_t>(T)) * 16);
   l.part_o = l.tg_bad + align256(static_cast<size_t>(T) * 4 * 4);
-  l.part_lse = l.part_o + align256(ent * kHPG * kD * 2);
-  l.total = l.part_lse + align256(ent * kHPG * 4);
+  l.part_ml = l.part_o + align256(ent * kHPG * kD * 2);
+  l.total = l.part_ml + align256(ent * kHPG * 8);
   return l;
 }
 
@@ -329,7 +768,7 @@ extern "C" size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B,
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || T > kMaxT || max_blocks_per_seq < 1 ||
       max_blocks_per_seq > (1 << 20))
     return 0;
-  return pf_layout(B, T, max_blocks_per_seq).total;
+  return pf_layout(T).total;
 }
 
 extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
@@ -342,7 +781,6 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   if (batch->B < 0 || batch->T < 0 || batch->B > kMaxB || batch->T > kMaxT) return MSA_ERR_INVALID_ARG;
   if (batch->max_q_len < 1 || batch->max_q_len > kMaxQ) return MSA_ERR_INVALID_ARG;
   if (batch->max_blocks_per_seq < 1 || batch->max_blocks_per_seq > (1 << 20)) return MSA_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(batch->B) * batch->max_blocks_per_seq * 4 > (int64_t{1} << 31) - 2) return MSA_ERR_UNSUPPORTED;
   if (batch->B > 0 && (batch->query_start_loc == nullptr || batch->seq_lens == nullptr || batch->block_table == nullptr))
     return MSA_ERR_INVALID_ARG;
   if ((st = check_cache(cache, false, true)) != MSA_OK) return st;
@@ -350,7 +788,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
     return MSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const PfLayout lay = pf_layout(batch->B, batch->T, batch->max_blocks_per_seq);
+  const PfLayout lay = pf_layout(batch->T);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < lay.total) return MSA_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PfParams p;
@@ -365,31 +803,44 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   p.sel = sel;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.out = out;
-  p.count = reinterpret_cast<int32_t*>(ws + lay.count);
-  p.offset = reinterpret_cast<int32_t*>(ws + lay.offset);
-  p.entries = reinterpret_cast<int32_t*>(ws + lay.entries);
+  p.hdr = reinterpret_cast<int32_t*>(ws + lay.hdr);
+  p.hkeys = reinterpret_cast<uint64_t*>(ws + lay.hkeys);
+  p.hcnt = reinterpret_cast<int32_t*>(ws + lay.hcnt);
+  p.rowh = reinterpret_cast<int32_t*>(ws + lay.rowh);
+  p.ehash = reinterpret_cast<int32_t*>(ws + lay.ehash);
+  p.entries = reinterpret_cast<int2*>(ws + lay.entries);
+  p.chunks = reinterpret_cast<int4*>(ws + lay.chunks);
   p.tg_bad = reinterpret_cast<int32_t*>(ws + lay.tg_bad);
   p.part_o = reinterpret_cast<uint32_t*>(ws + lay.part_o);
-  p.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  p.part_ml = reinterpret_cast<float2*>(ws + lay.part_ml);
+  p.hmask = lay.hslots - 1;
+  p.hbits = lay.hbits;
   p.status = status;
-  const int64_t rows = static_cast<int64_t>(p.B) * 4 * p.maxb;
-  if (cudaMemsetAsync(p.count, 0, static_cast<size_t>(rows) * 4, stream) != cudaSuccess ||
+  if (cudaMemsetAsync(p.hdr, 0, 16, stream) != cudaSuccess ||
+      cudaMemsetAsync(p.hkeys, 0xFF, static_cast<size_t>(lay.hslots) * 8, stream) != cudaSuccess ||
+      cudaMemsetAsync(p.hcnt, 0, static_cast<size_t>(lay.hslots) * 4, stream) != cudaSuccess ||
       cudaMemsetAsync(p.tg_bad, 0, static_cast<size_t>(p.T) * 16, stream) != cudaSuccess)
     return MSA_ERR_CUDA;
   const int64_t ent = static_cast<int64_t>(p.T) * 4 * kSel;
   const int eb = static_cast<int>((ent + 255) / 256);
   k_map_count<<<eb, 256, 0, stream>>>(p);
-  k_map_scan<<<1, 1024, 0, stream>>>(p, rows);
+  k_map_alloc<<<eb, 256, 0, stream>>>(p);
   k_map_fill<<<eb, 256, 0, stream>>>(p);
   if ((st = launch_status()) != MSA_OK) return st;
-  alignas(64) CUtensorMap tmap;
-  if (!kv_tensor_map(&tmap, cache->kv_pages, static_cast<uint64_t>(cache->num_pages > 0 ? cache->num_pages : 1)))
+  alignas(64) CUtensorMap kv_map;
+  alignas(64) CUtensorMap q_map;
+  if (!kv_tensor_map(&kv_map, cache->kv_pages, static_cast<uint64_t>(cache->num_pages > 0 ? cache->num_pages : 1)) ||
+      !rows128_tensor_map(&q_map, q, static_cast<uint64_t>(p.T) * kQHeads, kHPG))
     return MSA_ERR_CUDA;
-  if (cudaFuncSetAttribute(k_prefill_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PfSmem::kBytes)) !=
+  if (cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Smem::kBytes)) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
-  if (rows > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
-  k_prefill_attn<<<static_cast<unsigned>(rows), kPfThreads, PfSmem::kBytes, stream>>>(p, tmap);
-  k_prefill_merge<<<static_cast<unsigned>((static_cast<int64_t>(p.T) * kQHeads + 7) / 8), 256, 0, stream>>>(p);
+  const int sms = num_sms();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  // never more CTAs than chunks can exist: at most T + 64 T (each row adds at most one chunk)
+  const int64_t max_chunks = ent + p.T;
+  const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
+  k_prefill_tc<<<grid, kThreads, Smem::kBytes, stream>>>(p, kv_map, q_map);
+  k_prefill_merge<<<static_cast<unsigned>(static_cast<int64_t>(p.T) * 4), 128, 0, stream>>>(p);
   return launch_status();
 }

@@ -135,3 +135,88 @@ def test_prefill_faults_zero_fill_and_report(msa):
                 assert (rows == 0).all()
             else:
                 assert torch.equal(rows, good[100 + i, 16 * g:16 * (g + 1)])
+
+
+def map_counts(w: W.Workload, sel: np.ndarray):
+    """The key-block -> query map's counts from the batch alone: the valid first-occurrence
+    selections, grouped by (physical page, group) and by (sequence, group, block)."""
+    qsl = w.query_start_loc()
+    by_page, by_seq = {}, {}
+    for b in range(w.B):
+        for t in range(qsl[b], qsl[b] + w.q_lens[b]):
+            for g in range(4):
+                seen = set()
+                for v in sel[t, g]:
+                    if v < 0 or v in seen:
+                        continue
+                    seen.add(int(v))
+                    ph = int(w.block_table[b, v])
+                    by_page[(ph, g)] = by_page.get((ph, g), 0) + 1
+                    by_seq[(b, g, int(v))] = by_seq.get((b, g, int(v)), 0) + 1
+    return by_page, by_seq
+
+
+def test_shared_prefix_pages_are_dequantised_once(msa):
+    """Four sequences with mixed q_len share the physical pages of a 1,024-token prefix: every
+    token selects prefix blocks, and each (page, group) the sequences share is one row of the map,
+    dequantised once per 64 selections of all the sequences together, with the oracle's result."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("shared_prefix", [3000, 2200 + 5, 1500, 4000 + 77, 900], [90, 3, 1, 8, 17], seed=67,
+                prefix_len=1024, prefix_seqs=4)
+    assert w.prefix_seqs == 4 and (w.block_table[1:4, :8] == w.block_table[0, :8]).all()
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 9)
+    rng = np.random.default_rng(10)
+    qsl = w.query_start_loc()
+    for b in range(4):  # slot 1: prefix block 0; slot 2: another prefix block
+        for t in range(qsl[b], qsl[b] + w.q_lens[b]):
+            sel[t, :, 1] = 0
+            sel[t, :, 2] = rng.integers(1, 8, size=4)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seln = torch.from_numpy(sel).cuda()
+    out = torch.full((w.T, 64, 128), 0x7FC0, dtype=torch.uint16, device="cuda")
+    ws = torch.empty(msa.msa_prefill_workspace_size(w.B, w.T, dl.batch.max_blocks), dtype=torch.uint8, device="cuda")
+    msa.msa_prefill_attn(dl.batch, dl.cache, dl.q8, seln, dl.softmax_scale, out, ws, st)
+    torch.cuda.synchronize()
+    assert msa.status_bits(st) == 0
+    rows, chunks, entries, _ = ws[:16].view(torch.int32).cpu().tolist()
+    by_page, by_seq = map_counts(w, sel)
+    assert rows == len(by_page)
+    assert entries == sum(by_page.values())
+    assert chunks == sum((c + 63) // 64 for c in by_page.values())
+    shared = {k: c for k, c in by_page.items() if k[0] in set(w.block_table[0, :8].tolist())}
+    assert len(shared) == 32 and min(c for (ph, g), c in shared.items() if ph == w.block_table[0, 0]) > 64
+    assert rows < len(by_seq)  # keyed by sequence, every sharing sequence would dequantise them again
+    got = bf16_to_f32(out).cpu().numpy()
+    for b in range(w.B):
+        rows_b = slice(qsl[b], qsl[b] + w.q_lens[b])
+        s = sel[rows_b]
+        ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(s[s >= 0])).attention(s, dl.softmax_scale)
+        check_attention(got[rows_b], ref, f"shared prefix seq {b}")
+
+
+def test_prefill_large_rows_split_into_chunks(msa):
+    """One long prompt whose every token selects the same few blocks: rows of hundreds of
+    selections are cut into chunks of 64, each served by its own CTA turn, same result."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("hot_rows", [6000 + 3], [700], seed=68)
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 11)
+    sel[:, :, 1:4] = np.array([0, 1, 2], dtype=np.int32)
+    sel[:, :, 4:] = np.where(sel[:, :, 4:] <= 2, -1, sel[:, :, 4:])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seln = torch.from_numpy(sel).cuda()
+    out = torch.empty((w.T, 64, 128), dtype=torch.uint16, device="cuda")
+    ws = torch.empty(msa.msa_prefill_workspace_size(w.B, w.T, dl.batch.max_blocks), dtype=torch.uint8, device="cuda")
+    msa.msa_prefill_attn(dl.batch, dl.cache, dl.q8, seln, dl.softmax_scale, out, ws, st)
+    torch.cuda.synchronize()
+    assert msa.status_bits(st) == 0
+    rows, chunks, entries, _ = ws[:16].view(torch.int32).cpu().tolist()
+    by_page, _ = map_counts(w, sel)
+    assert (rows, entries, chunks) == (len(by_page), sum(by_page.values()),
+                                       sum((c + 63) // 64 for c in by_page.values()))
+    assert max(by_page.values()) >= 600
+    ref = OracleSeq(w, 0, 0, "cuda", kv_blocks=np.unique(sel[sel >= 0])).attention(sel, dl.softmax_scale)
+    check_attention(bf16_to_f32(out).cpu().numpy(), ref, "hot rows")

@@ -619,12 +619,24 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the lines of the other configurations")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time the prefill attention alone (its 2,048-token prompt) and print its record")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.prefill_only:
+        import torch
+
+        import nvfp4_kv_cache_gb300 as msa
+
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        print(json.dumps({"prefill_attn": time_prefill(msa, args.steps, args.warmup, flush, dev)}), flush=True)
+        return
     w = W.CONFIGS[args.config]()
     if args.impl == "reference":
         run_reference(args, w, rank)

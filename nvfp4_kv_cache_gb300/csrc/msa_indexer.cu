@@ -52,7 +52,7 @@ constexpr int kMmaWarps = 3;                     // MMA-issuing warps (pages in 
 constexpr int kWarpDq = 1 + kMmaWarps;           // first dequant warp
 constexpr int kWarpEp = kWarpDq + 4 * kDqGroups; // first max-pool warp
 constexpr int kIdxThreads = 32 * (kWarpEp + 4 * kEpGroups);
-constexpr int kDTiles = 6;                       // TMEM accumulators (32 columns each)
+constexpr int kDTiles = 9;                       // TMEM accumulators (32 columns each)
 constexpr int kTmemCols = 512;
 // The exact-score variant (NVFP4 keys to f16 with no E4M3 re-rounding, f16 score MMA): an
 // internal index kind next to MSA_INDEX_NVFP4 and MSA_INDEX_FP8.
@@ -276,11 +276,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);  // NVFP4: the dequant group's 4 warps; FP8: the max-pool group's
+      mbar_init(&empty[i], kNv ? 4 : 1);  // NVFP4: the dequant group's 4 warps; FP8: the page's MMAs
     }
     for (int i = 0; i < kATiles; ++i) {
       mbar_init(&a_full[i], 4);
-      mbar_init(&a_empty[i], 4);  // the max-pool group's 4 warps, once the MMAs are done
+      mbar_init(&a_empty[i], 1);  // the page's MMAs have completed (a commit)
     }
     for (int i = 0; i < kDTiles; ++i) {
       mbar_init(&d_full[i], 1);
@@ -450,9 +450,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
                           idesc, s > 0 ? 1u : 0u);
             }
           }
-          tc_commit(&d_full[d]);  // also tells the max-pool group the key tile (and FP8 stage) is free
+          tc_commit(&d_full[d]);
+          tc_commit(&a_empty[a]);  // the key tile and query tile (and an FP8 stage) may be refilled
+          if constexpr (!kNv) tc_commit(&empty[n % kStages]);
         } else {
           mbar_arrive(&d_full[d]);
+          mbar_arrive(&a_empty[a]);
+          if constexpr (!kNv) mbar_arrive(&empty[n % kStages]);
         }
       }
       __syncwarp();
@@ -579,10 +583,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         break;
       }
       tc_fence_after();
-      if (lane == 0) {  // the MMAs are done: their key tile (and FP8 stage) may be refilled
-        mbar_arrive(&a_empty[n % kATiles]);
-        if constexpr (!kNv) mbar_arrive(&empty[n % kStages]);
-      }
       float pm = -CUDART_INF_F;  // this lane's column maximum over the quarter's 32 keys
       int col = 0;
       {

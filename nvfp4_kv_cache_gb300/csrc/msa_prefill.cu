@@ -17,12 +17,12 @@
 //     in one row. Each row's selections are cut into chunks of at most 64;
 //  2. k_prefill_tc: one persistent CTA per SM takes chunks in turn. A chunk's K and V regions are
 //     copied (one 3-D tensor copy) and dequantised once, K to an E4M3 K-major tile and V to an
-//     E4M3 tile in place of the MN-major operand; then each tile of 8 selections (8 x 16 query
-//     heads = M 128) runs S = Q K^T (tcgen05.mma kind::f8f6f4, both operands in shared memory,
-//     N = 128 keys), a softmax over the block's 128 keys (one thread per query-head row), and
-//     O^T = V^T P^T with P split into hi = E4M3(P) and lo = E4M3(16 (P - hi)) (N = 256: the hi
-//     and the lo rows of all 128 heads). The (m, l) of every row and its unnormalised o go to
-//     the selection's slot;
+//     f16 tile read as the MN-major operand (E4M3 -> f16 is exact); then each tile of 8
+//     selections (8 x 16 query heads = M 128) runs S = Q K^T (tcgen05.mma kind::f8f6f4, both
+//     operands in shared memory, N = 128 keys), a softmax over the block's 128 keys (one thread
+//     per query-head row) that writes P in f16, and O^T = V^T P^T (kind::f16, M = 128 dims,
+//     N = 128 query-head rows). The (m, l) of every row and its unnormalised o go to the
+//     selection's slot;
 //  3. k_prefill_merge: per (token, group), the log-sum-exp merge of its up to 16 partials.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -44,28 +44,31 @@ constexpr int kTileSel = 8;            // selections per MMA tile: 8 x 16 query 
 constexpr int kMaxQ = 1 << 20;         // query tokens per sequence
 constexpr int kMaxT = 1 << 22;         // query tokens per call (entries pack t << 4 | slot)
 constexpr uint64_t kNoKey = ~0ull;     // an empty hash slot
-constexpr float kLoScale = 16.0f;      // the lo rows of P hold kLoScale (P - hi)
-constexpr uint32_t kLoScale2 = 0x4C004C00u;  // f16x2 {16, 16}
 
 // Warp roles of k_prefill_tc. A warp reads the TMEM lanes 32 (warp % 4) .. + 31, so the softmax
 // and epilogue groups are aligned sets of four warps.
-constexpr int kWarpProd = 0;   // chunk fetch, entry lists, tensor copies (lane 0)
-constexpr int kWarpIss = 1;    // MMA issue (lane 0); allocates TMEM
-constexpr int kWarpDq = 2;     // two dequant warps
-constexpr int kDqWarps = 2;
+constexpr int kWarpProd = 0;   // chunk fetch, entry lists, query-tile copies
+constexpr int kWarpIss = 1;    // S = Q K^T issue (lane 0) for every tile; allocates TMEM
+constexpr int kWarpPv = 2;     // two O^T = V^T P^T issuers (warps 2, 3): even and odd tiles
 constexpr int kWarpSm = 4;     // two softmax warpgroups (warps 4-7, 8-11): even and odd tiles
-constexpr int kWarpEp = 12;    // two epilogue warpgroups (warps 12-15, 16-19): heads 0-63, 64-127
-constexpr int kThreads = 640;
+constexpr int kWarpEp = 12;    // two epilogue warpgroups (warps 12-15, 16-19): even and odd tiles
+constexpr int kWarpDq = 20;    // two dequant warps
+constexpr int kDqWarps = 2;
+constexpr int kThreads = 32 * (kWarpDq + kDqWarps);
 constexpr int kMetaSlots = 4;
 // Arrivals that release a chunk's entry list: every dequant, softmax and epilogue warp and the
-// issuer, each after its last use of it.
-constexpr int kMetaUsers = kDqWarps + 8 + 8 + 1;
+// three issuers, each after its last use of it.
+constexpr int kMetaUsers = kDqWarps + 8 + 8 + 3;
 
-constexpr int kStage = 2 * kRegion;      // K region then V region of one (page, group), raw
+constexpr int kQBufs = 3;                // query tiles in flight (their copies take ~5,000 cycles)
 constexpr int kKTile = kBS * kD;         // 128 keys x 128 E4M3, K-major, 128-byte swizzle
+constexpr int kVTile = kBS * kD * 2;     // 128 keys x 128 f16, MN-major: two 64-dim atom columns
+constexpr uint32_t kVLbo = 16384;        //   V tile: the two 64-dim atom columns
+constexpr uint32_t kVSbo = 1024;         //           8-key groups
 constexpr int kQTile = kTileSel * kHPG * kD;  // 128 query-head rows x 128 E4M3
-constexpr int kPTile = 2 * 128 * kBS;    // 256 rows (hi heads, then lo heads) x 128 keys E4M3
-constexpr uint32_t kTmemCols = 512;      // S double buffer (2 x 128) + O^T (256)
+constexpr int kPTile = 128 * kBS * 2;    // 128 query-head rows x 128 keys f16: two 64-key K atoms
+constexpr int kPAtom = 128 * 128;        //   16 KB each
+constexpr uint32_t kTmemCols = 512;      // S (2 x 128) and O^T (2 x 128), both double-buffered
 constexpr uint32_t kColO = 256;
 
 struct PfParams {
@@ -73,6 +76,7 @@ struct PfParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
   const int32_t* block_table;
+  const uint8_t* kv;
   const uint8_t* q;
   const int32_t* sel;
   float scale_log2;
@@ -213,30 +217,27 @@ struct ChunkMeta {
 };
 
 struct Smem {
-  static constexpr size_t kOffStage = 0;                                  // [2] raw K+V regions
-  static constexpr size_t kOffK = kOffStage + 2 * static_cast<size_t>(kStage);  // [2] K tiles
+  static constexpr size_t kOffK = 0;                                            // [2] K tiles
   static constexpr size_t kOffV = kOffK + 2 * static_cast<size_t>(kKTile);      // [2] V tiles
-  static constexpr size_t kOffQ = kOffV + 2 * static_cast<size_t>(kKTile);      // [2] Q tiles
-  static constexpr size_t kOffP = kOffQ + 2 * static_cast<size_t>(kQTile);      // [2] P tiles
+  static constexpr size_t kOffQ = kOffV + 2 * static_cast<size_t>(kVTile);      // [kQBufs] Q tiles
+  static constexpr size_t kOffP = kOffQ + kQBufs * static_cast<size_t>(kQTile); // [2] P tiles
   static constexpr size_t kOffLut = kOffP + 2 * static_cast<size_t>(kPTile);
   static constexpr size_t kOffMeta = kOffLut + 256 * 8;
   static constexpr size_t kOffBar = kOffMeta + kMetaSlots * sizeof(ChunkMeta);
-  // barriers: meta full/empty, stage full/empty, tile full/empty, q full/empty, s full/free,
-  // p full/empty (two of each but the meta ring), o full/free, fin
-  static constexpr int kNumBars = 2 * kMetaSlots + 2 * 2 * 5 + 3;
+  // barriers: meta full/empty, q full/empty, then two each of tile full/empty, s full/free,
+  // p full/empty, o full/free, and one fin per issuer
+  static constexpr int kNumBars = 2 * kMetaSlots + 2 * kQBufs + 2 * 2 * 4 + 3;
   static constexpr size_t kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr size_t kBytes = 1024 + kOffMisc + 16;
 };
-static_assert(Smem::kOffK % 1024 == 0 && Smem::kOffQ % 1024 == 0 && Smem::kOffP % 1024 == 0 &&
-                  kRegion % 1024 == 0,
+static_assert(Smem::kOffK % 1024 == 0 && Smem::kOffV % 1024 == 0 && Smem::kOffQ % 1024 == 0 &&
+                  Smem::kOffP % 1024 == 0 && kRegion % 1024 == 0,
               "swizzled tiles and copies start on 1024-B boundaries");
 static_assert(Smem::kOffBar % 8 == 0 && Smem::kBytes <= 232448, "shared memory budget");
 
 struct Bars {
   uint64_t* meta_full;
   uint64_t* meta_empty;
-  uint64_t* kv_full;
-  uint64_t* kv_empty;
   uint64_t* kt_full;
   uint64_t* kt_empty;
   uint64_t* q_full;
@@ -253,38 +254,46 @@ struct Bars {
     meta_full = b;
     meta_empty = b + kMetaSlots;
     b += 2 * kMetaSlots;
-    kv_full = b;
-    kv_empty = b + 2;
-    kt_full = b + 4;
-    kt_empty = b + 6;
-    q_full = b + 8;
-    q_empty = b + 10;
-    s_full = b + 12;
-    s_free = b + 14;
-    p_full = b + 16;
-    p_empty = b + 18;
-    o_full = b + 20;
-    o_free = b + 21;
-    fin = b + 22;
-    static_assert(2 * kMetaSlots + 23 == Smem::kNumBars, "barrier area");
+    q_full = b;
+    q_empty = b + kQBufs;
+    b += 2 * kQBufs;
+    kt_full = b;
+    kt_empty = b + 2;
+    s_full = b + 4;
+    s_free = b + 6;
+    p_full = b + 8;
+    p_empty = b + 10;
+    o_full = b + 12;
+    o_free = b + 14;
+    fin = b + 16;
+    static_assert(2 * kMetaSlots + 2 * kQBufs + 19 == Smem::kNumBars, "barrier area");
   }
 };
 
 __device__ __forceinline__ int ntiles_of(int n) { return (n + kTileSel - 1) / kTileSel; }
 
+// Key row r of an NVFP4 K or V region in the cache (no swizzle: rows of 64 code bytes, then
+// the 8 scale bytes of each row), read-only loads.
+__device__ __forceinline__ void load_row_global(const uint8_t* region, int r, RawRow& raw) {
+  const uint4* c = reinterpret_cast<const uint4*>(region + r * kRowCodes);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) raw.c[q] = __ldg(c + q);
+  raw.sc = __ldg(reinterpret_cast<const uint2*>(region + kScaleOff + r * kRowScales));
+}
+
 // Persistent: one CTA per SM takes chunks in turn (a global counter). Warp roles:
 //  producer — the chunk's entry list into the meta ring, one tensor copy of its K and V regions,
 //             and per tile one 2 KB tensor copy per selection of its token's 16 query heads;
-//  dequant  — the K rows to an E4M3 K-major tile, the V rows to an E4M3 tile read as the
-//             MN-major A operand of O^T (rows of 128 dims, 128-byte swizzle);
-//  issuer   — S(i) = Q K^T (M 128 heads x N 128 keys) one tile ahead of O^T(i - 1) = V^T P^T
-//             (M 128 dims x N 256 hi/lo head rows);
-//  softmax  — thread = query-head row: the row's max and sum over the block's unmasked keys, P as
-//             hi and lo E4M3 rows, and the row's (m, l) to its slot;
-//  epilogue — thread = dim: o = hi + lo / 16 of every head to its slot, f16.
+//  dequant  — the K rows to an E4M3 K-major tile, the V rows to an f16 tile read as the MN-major
+//             A operand of O^T (two 64-dim atom columns, 8-key groups, 128-byte swizzle);
+//  issuer   — S(i) = Q K^T (M 128 heads x N 128 keys, E4M3) one tile ahead of O^T(i - 1) =
+//             V^T P^T (M 128 dims x N 128 head rows x K 128 keys, f16);
+//  softmax  — thread = query-head row: the row's max and sum over the block's unmasked keys, P in
+//             f16, and the row's (m, l) to its slot (two warpgroups, alternate tiles);
+//  epilogue — thread = dim: o of every head to its slot, f16 (two warpgroups, alternate tiles).
 // Every wait is bounded (MSA_ERR_TIMEOUT, then every role leaves); nothing traps.
 __global__ void __launch_bounds__(kThreads, 1)
-    k_prefill_tc(const PfParams p, const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map) {
+    k_prefill_tc(const PfParams p, const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const Bars bars(smem);
@@ -300,28 +309,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.meta_full[i], 1);
       mbar_init(&bars.meta_empty[i], kMetaUsers);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], kDqWarps);
-      mbar_init(&bars.kt_full[i], kDqWarps);
-      mbar_init(&bars.kt_empty[i], 1);
+    for (int i = 0; i < kQBufs; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.kt_full[i], kDqWarps);
+      mbar_init(&bars.kt_empty[i], 2);  // both O^T issuers, after their last MMA of the chunk
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.s_free[i], 4);  // the four warps of the tile's softmax warpgroup
       mbar_init(&bars.p_full[i], 4);
       mbar_init(&bars.p_empty[i], 1);
+      mbar_init(&bars.o_full[i], 1);
+      mbar_init(&bars.o_free[i], 4);  // the four warps of the tile's epilogue warpgroup
     }
-    mbar_init(bars.o_full, 1);
-    mbar_init(bars.o_free, 8);  // both epilogue warpgroups
-    mbar_init(bars.fin, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars.fin[i], 1);
     fence_mbar_init();
     *abort_flag = 0;
   }
   {
     // Q tiles start as zeros: rows of a short tile's missing selections then hold finite values
     uint4* qz = reinterpret_cast<uint4*>(smem + Smem::kOffQ);
-    for (int i = tid; i < 2 * kQTile / 16; i += kThreads) qz[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < kQBufs * kQTile / 16; i += kThreads) qz[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   if (warp == kWarpIss) tmem_alloc(tmem_slot, kTmemCols);
   build_dequant_lut(lut, tid, kThreads);
@@ -343,12 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProd) {
     // ---- producer ---------------------------------------------------------------------------
-    if (lane == 0) {
-      prefetch_tensormap(&kv_map);
-      prefetch_tensormap(&q_map);
-    }
+    if (lane == 0) prefetch_tensormap(&q_map);
     const uint64_t pol = policy_evict_last();  // a token's query heads serve up to 16 chunks
-    int k = 0, i = 0, kvn = 0;  // chunks taken, query tiles and K/V copies issued
+    int k = 0, i = 0;  // chunks taken, query tiles issued
     for (;; ++k) {
       int c = 0;
       if (lane == 0) c = atomicAdd(&p.hdr[3], 1);
@@ -371,124 +377,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         m.g = ch.w;
       }
       __syncwarp();
-      bool ok = true;
       if (lane == 0) {
         __threadfence_block();
         mbar_arrive(&bars.meta_full[ms]);
-        const int s = k & 1;
-        ok = mbar_wait(&bars.kv_empty[s], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u, abort_flag);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars.kv_full[s], kStage);
-          tma_load_3d(smem + Smem::kOffStage + static_cast<size_t>(s) * kStage, &kv_map, 0, 2 * ch.w * (kRegion / kD),
-                      ch.z, &bars.kv_full[s]);
-          ++kvn;
-        }
-        for (int j = 0; ok && j < ntiles_of(ch.y); ++j, ++i) {
-          ok = mbar_wait(&bars.q_empty[i & 1], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag);
-          if (!ok) break;
-          const int ne = min(kTileSel, ch.y - kTileSel * j);
-          mbar_arrive_expect_tx(&bars.q_full[i & 1], static_cast<uint32_t>(ne) * kHPG * kD);
-          uint8_t* qt = smem + Smem::kOffQ + static_cast<size_t>(i & 1) * kQTile;
-          for (int e = 0; e < ne; ++e) {
-            const int t = m.e[kTileSel * j + e].x >> 4;
-            tma_load_2d(qt + e * kHPG * kD, &q_map, 0, t * kQHeads + ch.w * kHPG, &bars.q_full[i & 1], pol);
-          }
-        }
-        if (!ok) {
-          if (!*abort_flag) set_status(p.status, MSA_ERR_TIMEOUT);
-          *abort_flag = 1;
+      }
+      // the chunk's query tiles: 8 lanes copy one selection's 16 query rows each
+      bool ok = true;
+      for (int j = 0; j < ntiles_of(ch.y); ++j, ++i) {
+        const int qb = i % kQBufs;
+        if (!(ok = wwait(&bars.q_empty[qb], (static_cast<uint32_t>(i / kQBufs) & 1u) ^ 1u))) break;
+        const int ne = min(kTileSel, ch.y - kTileSel * j);
+        if (lane == 0) mbar_arrive_expect_tx(&bars.q_full[qb], static_cast<uint32_t>(ne) * kHPG * kD);
+        __syncwarp();
+        if (lane < ne) {
+          const int t = m.e[kTileSel * j + lane].x >> 4;
+          tma_load_2d(smem + Smem::kOffQ + static_cast<size_t>(qb) * kQTile + lane * kHPG * kD, &q_map, 0,
+                      t * kQHeads + ch.w * kHPG, &bars.q_full[qb], pol);
         }
       }
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+      if (!ok) break;
     }
     // never leave while a copy into this CTA's shared memory may still be in flight
     if (lane == 0) {
-      for (int j = kvn > 2 ? kvn - 2 : 0; j < kvn; ++j)
-        if (!mbar_wait_bounded(&bars.kv_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
-          set_status(p.status, MSA_ERR_TIMEOUT);
-      for (int j = i > 2 ? i - 2 : 0; j < i; ++j)
-        if (!mbar_wait_bounded(&bars.q_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs, nullptr))
+      for (int j = i > kQBufs ? i - kQBufs : 0; j < i; ++j)
+        if (!mbar_wait_bounded(&bars.q_full[j % kQBufs], static_cast<uint32_t>(j / kQBufs) & 1u, kWaitLimitNs, nullptr))
           set_status(p.status, MSA_ERR_TIMEOUT);
     }
   } else if (warp == kWarpIss) {
-    // ---- MMA issuer: S one tile ahead of O^T ----------------------------------------------------
+    // ---- S = Q K^T for every tile, in order ---------------------------------------------------
     constexpr uint32_t idesc_s = idesc_e4m3_f32(128, 128);
-    constexpr uint32_t idesc_o = idesc_e4m3_f32_amn(128, 256);
-    struct Tile {
-      int k, j, nt, i;
-    };
-    bool ok = true, issued = false;
-    // the next tile after `t` (t.nt == 0: before the first chunk); false at the end or on abort
-    auto next = [&](Tile& t) -> bool {
-      if (t.nt > 0 && t.j + 1 < t.nt) {
-        ++t.j;
-        ++t.i;
-        return true;
-      }
-      const int k = t.nt > 0 ? t.k + 1 : 0;
-      if (!wwait(&bars.meta_full[k % kMetaSlots], static_cast<uint32_t>(k / kMetaSlots) & 1u)) {
-        ok = false;
-        return false;
-      }
-      const int n = meta[k % kMetaSlots].n;
-      if (n < 0) return false;
-      t.i = t.nt > 0 ? t.i + 1 : 0;
-      t.k = k;
-      t.j = 0;
-      t.nt = ntiles_of(n);
-      return true;
-    };
-    auto issue_s = [&](const Tile& t) -> bool {
-      if (t.j == 0 && !wwait(&bars.kt_full[t.k & 1], static_cast<uint32_t>(t.k >> 1) & 1u)) return false;
-      if (!wwait(&bars.q_full[t.i & 1], static_cast<uint32_t>(t.i >> 1) & 1u)) return false;
-      if (!wwait(&bars.s_free[t.i & 1], (static_cast<uint32_t>(t.i >> 1) & 1u) ^ 1u)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + Smem::kOffQ + static_cast<size_t>(t.i & 1) * kQTile));
-        const uint64_t dk = sw128_kmajor_desc(smem_u32(smem + Smem::kOffK + static_cast<size_t>(t.k & 1) * kKTile));
+    bool issued = false;
+    int i = 0;
+    for (int k = 0;; ++k) {
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_full[ms], static_cast<uint32_t>(k / kMetaSlots) & 1u)) break;
+      const int n = meta[ms].n;
+      if (n < 0) break;
+      if (!wwait(&bars.kt_full[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) break;
+      bool ok = true;
+      for (int j = 0; j < ntiles_of(n); ++j, ++i) {
+        if (!(ok = wwait(&bars.q_full[i % kQBufs], static_cast<uint32_t>(i / kQBufs) & 1u))) break;
+        if (!(ok = wwait(&bars.s_free[i & 1], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dq = sw128_kmajor_desc(smem_u32(smem + Smem::kOffQ + static_cast<size_t>(i % kQBufs) * kQTile));
+          const uint64_t dk = sw128_kmajor_desc(smem_u32(smem + Smem::kOffK + static_cast<size_t>(k & 1) * kKTile));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // K = 32 dims per MMA: +32 B in both operands' atoms
-          tc_mma_f8(tmem + 128u * static_cast<uint32_t>(t.i & 1), dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
-        tc_commit(&bars.s_full[t.i & 1]);
-        tc_commit(&bars.q_empty[t.i & 1]);
+          for (int kk = 0; kk < 4; ++kk)  // K = 32 dims per MMA: +32 B in both operands' atoms
+            tc_mma_f8(tmem + 128u * static_cast<uint32_t>(i & 1), dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+          tc_commit(&bars.s_full[i & 1]);
+          tc_commit(&bars.q_empty[i % kQBufs]);
+        }
+        __syncwarp();
+        issued = true;
       }
-      __syncwarp();
-      issued = true;
-      return true;
-    };
-    auto issue_o = [&](const Tile& t) -> bool {
-      if (!wwait(&bars.p_full[t.i & 1], static_cast<uint32_t>(t.i >> 1) & 1u)) return false;
-      if (!wwait(bars.o_free, (static_cast<uint32_t>(t.i) & 1u) ^ 1u)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t va = smem_u32(smem + Smem::kOffV + static_cast<size_t>(t.k & 1) * kKTile);
-        const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + Smem::kOffP + static_cast<size_t>(t.i & 1) * kPTile));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // K = 32 keys per MMA: 32 rows (4 KB) of V, +32 B of P
-          tc_mma_f8(tmem + kColO, sw128_mnmajor8_desc(va + 4096 * kk), dp + 2 * kk, idesc_o, kk > 0 ? 1u : 0u);
-        tc_commit(bars.o_full);
-        tc_commit(&bars.p_empty[t.i & 1]);
-        if (t.j + 1 == t.nt) tc_commit(&bars.kt_empty[t.k & 1]);  // the chunk's tiles are free
-      }
-      __syncwarp();
-      if (t.j + 1 == t.nt && lane == 0) mbar_arrive(&bars.meta_empty[t.k % kMetaSlots]);
-      return true;
-    };
-    Tile cur = {0, 0, 0, 0};
-    bool have = next(cur);
-    if (have) ok = issue_s(cur);
-    while (have && ok) {
-      Tile prev = cur;
-      have = next(cur);
-      if (have && ok) ok = issue_s(cur);
-      if (ok) ok = issue_o(prev);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bars.meta_empty[ms]);
     }
     // nothing of this thread's is in flight when the CTA ends
     if (lane == 0 && issued) {
-      tc_commit(bars.fin);
-      if (!mbar_wait_bounded(bars.fin, 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+      tc_commit(&bars.fin[0]);
+      if (!mbar_wait_bounded(&bars.fin[0], 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
     }
   } else if (warp < kWarpSm) {
+    // ---- O^T = V^T P^T for the tiles of parity x ------------------------------------------------
+    constexpr uint32_t idesc_o = idesc_f16_f32_amn(128, 128);
+    const int x = warp - kWarpPv;
+    bool issued = false;
+    int i = 0;
+    for (int k = 0;; ++k) {
+      const int ms = k % kMetaSlots;
+      if (!wwait(&bars.meta_full[ms], static_cast<uint32_t>(k / kMetaSlots) & 1u)) break;
+      const int n = meta[ms].n;
+      if (n < 0) break;
+      bool ok = true;
+      for (int j = 0; j < ntiles_of(n); ++j, ++i) {
+        if ((i & 1) != x) continue;
+        if (!(ok = wwait(&bars.p_full[x], static_cast<uint32_t>(i >> 1) & 1u))) break;
+        if (!(ok = wwait(&bars.o_free[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dv =
+              sw128_mnmajor_desc(smem_u32(smem + Smem::kOffV + static_cast<size_t>(k & 1) * kVTile), kVLbo, kVSbo);
+          const uint64_t dp = sw128_kmajor_desc(smem_u32(smem + Smem::kOffP + static_cast<size_t>(x) * kPTile));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // K = 16 keys per MMA: two 8-key groups of V; 32 B (or the next atom) of P
+            tc_mma_f16(tmem + kColO + 128u * static_cast<uint32_t>(x), dv + ((2 * kVSbo) >> 4) * kk,
+                       dp + (((kk >> 2) * kPAtom + (kk & 3) * 32) >> 4), idesc_o, kk > 0 ? 1u : 0u);
+          tc_commit(&bars.o_full[x]);
+          tc_commit(&bars.p_empty[x]);
+        }
+        __syncwarp();
+        issued = true;
+      }
+      if (!ok) break;
+      // this issuer's MMAs on the chunk's K and V tiles (if any) are done: the tiles may be refilled
+      if (lane == 0) {
+        tc_commit(&bars.kt_empty[k & 1]);
+        mbar_arrive(&bars.meta_empty[ms]);
+      }
+    }
+    if (lane == 0 && issued) {
+      tc_commit(&bars.fin[1 + x]);
+      if (!mbar_wait_bounded(&bars.fin[1 + x], 0u, kWaitLimitNs, nullptr)) set_status(p.status, MSA_ERR_TIMEOUT);
+    }
+  } else if (warp >= kWarpDq) {
     // ---- dequant warps: K rows to the K tile, V rows to the V tile ---------------------------------
     const int dt = tid - 32 * kWarpDq;
     for (int k = 0;; ++k) {
@@ -497,26 +490,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = meta[ms].n;
       if (n < 0) break;
       const int s = k & 1;
-      if (!wwait(&bars.kv_full[s], static_cast<uint32_t>(k >> 1) & 1u)) break;
       if (!wwait(&bars.kt_empty[s], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u)) break;
-      const uint8_t* stage = smem + Smem::kOffStage + static_cast<size_t>(s) * kStage;
-      for (int r = dt; r < 2 * kBS; r += 32 * kDqWarps) {  // 4 rows a thread
-        const int rr = r & (kBS - 1);
-        RawRow raw;
-        load_row(stage + (r < kBS ? 0 : kRegion), rr, raw);
-        uint8_t* tile = smem + (r < kBS ? Smem::kOffK : Smem::kOffV) + static_cast<size_t>(s) * kKTile;
+      // the block's K and V regions straight from the cache (read once per chunk)
+      const uint8_t* kreg = p.kv + static_cast<int64_t>(meta[ms].ph) * kKvPage + 2 * meta[ms].g * kRegion;
+      uint8_t* kt = smem + Smem::kOffK + static_cast<size_t>(s) * kKTile;
+      uint8_t* vt = smem + Smem::kOffV + static_cast<size_t>(s) * kVTile;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {  // this thread's K rows and V rows (keys) dt and dt + 64
+        const int kr = dt + 64 * h;
+        RawRow rk, rv;
+        load_row_global(kreg, kr, rk);
+        load_row_global(kreg + kRegion, kr, rv);
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
           uint32_t w[8];
-          dequant_quarter(raw, qd, lut, w);
-          *reinterpret_cast<uint4*>(tile + sw128_chunk_off(rr, 2 * qd)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(tile + sw128_chunk_off(rr, 2 * qd + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+          dequant_quarter(rk, qd, lut, w);
+          *reinterpret_cast<uint4*>(kt + sw128_chunk_off(kr, 2 * qd)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(kt + sw128_chunk_off(kr, 2 * qd + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        uint8_t* vrow = vt + (kr >> 3) * kVSbo + (kr & 7) * 128;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          uint32_t w[8];
+          dequant_quarter(rv, qd, lut, w);
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {  // dims 32 qd + 8 hh .. +7 = chunk cc = 4 qd + hh
+            const int cc = 4 * qd + hh;
+            const uint4 v4 = make_uint4(cvt_f16x2_e4m3x2(w[2 * hh]), cvt_f16x2_e4m3x2(w[2 * hh] >> 16),
+                                        cvt_f16x2_e4m3x2(w[2 * hh + 1]), cvt_f16x2_e4m3x2(w[2 * hh + 1] >> 16));
+            *reinterpret_cast<uint4*>(vrow + (cc >> 3) * kVLbo + (((cc & 7) ^ (kr & 7)) << 4)) = v4;
+          }
         }
       }
       fence_proxy_async_smem();  // the tiles are read by the tensor core
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars.kv_empty[s]);
         mbar_arrive(&bars.kt_full[s]);
         mbar_arrive(&bars.meta_empty[ms]);
       }
@@ -547,23 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = __all_sync(0xffffffffu, rel >= kBS - 1);  // no key of the warp's rows masked
         float mr = -CUDART_INF_F;  // the row's max raw score over its unmasked keys
 #pragma unroll 1
-        for (int cc = 0; cc < 4; cc += 2) {  // two loads in flight per wait
-          uint32_t r[2][32];
-          tmem_ld32(ts + 32 * cc, r[0]);
-          tmem_ld32(ts + 32 * cc + 32, r[1]);
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(ts + 32 * cc, r);
           tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (full) {
+            for (int u = 0; u < 32; u += 4)
+              mr = fmaxf(mr, max3f(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
+                                   fmaxf(__uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]))));
+          } else {
 #pragma unroll
-              for (int u = 0; u < 32; u += 4)
-                mr = fmaxf(mr, max3f(__uint_as_float(r[h][u]), __uint_as_float(r[h][u + 1]),
-                                     fmaxf(__uint_as_float(r[h][u + 2]), __uint_as_float(r[h][u + 3]))));
-            } else {
-#pragma unroll
-              for (int u = 0; u < 32; ++u)
-                if (32 * (cc + h) + u <= rel) mr = fmaxf(mr, __uint_as_float(r[h][u]));
-            }
+            for (int u = 0; u < 32; ++u)
+              if (32 * cc + u <= rel) mr = fmaxf(mr, __uint_as_float(r[u]));
           }
         }
         const float mx = mr * c;  // c > 0: the max of the scaled scores
@@ -573,34 +577,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l = 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t r[1][32];
-          tmem_ld32(ts + 32 * cc, r[0]);
+          uint32_t r[32];
+          tmem_ld32(ts + 32 * cc, r);
           tmem_wait_ld();
           {
-            constexpr int h = 0;
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {  // 16 keys: one 16-byte chunk of the hi row and of the lo row
-              uint32_t hw[4], lw[4];
+            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
+              uint32_t pw[4];
 #pragma unroll
-              for (int u4 = 0; u4 < 4; ++u4) {
-                const int u = 16 * hq + 4 * u4;
-                float pv[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  pv[v] = fast_exp2(fmaf(__uint_as_float(r[h][u + v]), c, -mu));
-                  if (!full && 32 * cc + u + v > rel) pv[v] = 0.f;
-                }
-                l += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-                const uint32_t h01 = cvt_e4m3x2(pv[0], pv[1]), h23 = cvt_e4m3x2(pv[2], pv[3]);
-                const uint32_t r01 = sub_f16x2(pack_f16x2(pv[0], pv[1]), cvt_f16x2_e4m3x2(h01));
-                const uint32_t r23 = sub_f16x2(pack_f16x2(pv[2], pv[3]), cvt_f16x2_e4m3x2(h23));
-                const uint32_t l01 = cvt_e4m3x2_f16x2(mul_f16x2(r01, kLoScale2));
-                const uint32_t l23 = cvt_e4m3x2_f16x2(mul_f16x2(r23, kLoScale2));
-                hw[u4] = h01 | (h23 << 16);
-                lw[u4] = l01 | (l23 << 16);
+              for (int u2 = 0; u2 < 4; ++u2) {
+                const int u = 8 * q8 + 2 * u2;
+                float p0 = fast_exp2(fmaf(__uint_as_float(r[u]), c, -mu));
+                float p1 = fast_exp2(fmaf(__uint_as_float(r[u + 1]), c, -mu));
+                if (!full && 32 * cc + u > rel) p0 = 0.f;
+                if (!full && 32 * cc + u + 1 > rel) p1 = 0.f;
+                l += p0 + p1;
+                pw[u2] = pack_f16x2(p0, p1);
               }
-              *reinterpret_cast<uint4*>(pt + sw128_chunk_off(row, 2 * cc + hq)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint4*>(pt + sw128_chunk_off(128 + row, 2 * cc + hq)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
+                  make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
           }
         }
@@ -621,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.meta_empty[ms]);
     }
   } else {
-    // ---- epilogue warpgroup y (heads 64 y .. 64 y + 63): thread = dim 32 q + lane, o = hi + lo / 16
+    // ---- epilogue warpgroup y (tiles i with i % 2 == y): thread = dim 32 q + lane ---------------
     const int y = (warp - kWarpEp) >> 2, qw = warp & 3;
     const int d = 32 * qw + lane;
     const uint32_t lanes = static_cast<uint32_t>(32 * qw) << 16;
@@ -634,19 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n < 0) break;
       bool ok = true;
       for (int j = 0; j < ntiles_of(n); ++j, ++i) {
-        if (!(ok = wwait(bars.o_full, static_cast<uint32_t>(i) & 1u))) break;
+        if ((i & 1) != y) continue;
+        if (!(ok = wwait(&bars.o_full[y], static_cast<uint32_t>(i >> 1) & 1u))) break;
         tc_fence_after();
+        const uint32_t to = tmem + kColO + 128u * static_cast<uint32_t>(y) + lanes;
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {  // heads 32 hc .. 32 hc + 31: selections 2 hc, 2 hc + 1
-          const int hc = 2 * y + hh;
-          uint32_t hi[32], lo[32];
-          tmem_ld32(tmem + kColO + 32 * hc + lanes, hi);
-          tmem_ld32(tmem + kColO + 128 + 32 * hc + lanes, lo);
+        for (int hc = 0; hc < 4; ++hc) {  // heads 32 hc .. 32 hc + 31: selections 2 hc, 2 hc + 1
+          uint32_t o[32];
+          tmem_ld32(to + 32 * hc, o);
           tmem_wait_ld();
-          if (hh == 1) {
+          if (hc == 3) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.o_free);
+            if (lane == 0) mbar_arrive(&bars.o_free[y]);
           }
 #pragma unroll
           for (int ee = 0; ee < 2; ++ee) {
@@ -657,12 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t base = (static_cast<int64_t>(t) * 4 + m.g) * kSel + slot;
             uint32_t w[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float o0 = fmaf(__uint_as_float(lo[16 * ee + 2 * u]), 1.0f / kLoScale, __uint_as_float(hi[16 * ee + 2 * u]));
-              const float o1 =
-                  fmaf(__uint_as_float(lo[16 * ee + 2 * u + 1]), 1.0f / kLoScale, __uint_as_float(hi[16 * ee + 2 * u + 1]));
-              w[u] = pack_f16x2(o0, o1);
-            }
+            for (int u = 0; u < 8; ++u)
+              w[u] = pack_f16x2(__uint_as_float(o[16 * ee + 2 * u]), __uint_as_float(o[16 * ee + 2 * u + 1]));
             uint4* dst = reinterpret_cast<uint4*>(p.part_o + (base * kD + d) * (kHPG / 2));
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -799,6 +790,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   p.qsl = batch->query_start_loc;
   p.seq_lens = batch->seq_lens;
   p.block_table = batch->block_table;
+  p.kv = cache->kv_pages;
   p.q = q;
   p.sel = sel;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -827,11 +819,8 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   k_map_alloc<<<eb, 256, 0, stream>>>(p);
   k_map_fill<<<eb, 256, 0, stream>>>(p);
   if ((st = launch_status()) != MSA_OK) return st;
-  alignas(64) CUtensorMap kv_map;
   alignas(64) CUtensorMap q_map;
-  if (!kv_tensor_map(&kv_map, cache->kv_pages, static_cast<uint64_t>(cache->num_pages > 0 ? cache->num_pages : 1)) ||
-      !rows128_tensor_map(&q_map, q, static_cast<uint64_t>(p.T) * kQHeads, kHPG))
-    return MSA_ERR_CUDA;
+  if (!rows128_tensor_map(&q_map, q, static_cast<uint64_t>(p.T) * kQHeads, kHPG)) return MSA_ERR_CUDA;
   if (cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Smem::kBytes)) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
@@ -840,7 +829,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   // never more CTAs than chunks can exist: at most T + 64 T (each row adds at most one chunk)
   const int64_t max_chunks = ent + p.T;
   const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
-  k_prefill_tc<<<grid, kThreads, Smem::kBytes, stream>>>(p, kv_map, q_map);
+  k_prefill_tc<<<grid, kThreads, Smem::kBytes, stream>>>(p, q_map);
   k_prefill_merge<<<static_cast<unsigned>(static_cast<int64_t>(p.T) * 4), 128, 0, stream>>>(p);
   return launch_status();
 }

@@ -29,7 +29,7 @@ def check_layer(msa, w, layer, seqs):
     msa.msa_decode_step(dl.batch, dl.cache, dl.q8, dl.iq8, dl.softmax_scale, ws, o["out"], o["scores"], o["sel"])
     assert msa.msa_read_device_status(ws) == msa.MSA_OK
     qsl = w.query_start_loc()
-    compared = 0
+    compared = total = 0
     for b in seqs:
         ql, L = w.q_lens[b], w.seq_lens[b]
         rows = slice(int(qsl[b]), int(qsl[b]) + ql)
@@ -40,21 +40,26 @@ def check_layer(msa, w, layer, seqs):
         rs = ref.scores()
         check_scores(gs, rs, f"{w.name} layer {layer} seq {b}")
         compared += check_selection(gsel, gs, rs, L, ql, f"{w.name} layer {layer} seq {b}")
+        total += 4 * ql
         ro = ref.attention(gsel, dl.softmax_scale)
         check_attention(bf16_to_f32(o["out"][rows]).cpu().numpy(), ro, f"{w.name} layer {layer} seq {b}")
     del dl
     torch.cuda.empty_cache()
-    return compared
+    # (token, group) rows whose selection was compared with the oracle's own (the others have a
+    # gap of at most 1e-3 between the 15th and 16th candidates, where both orders are right)
+    print(f"{w.name} layer {layer}: selection compared with the oracle's on {compared} of {total} (token, group) rows")
+    return compared, total
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "spec", "long"])
 def test_fullsize_config(msa, name):
     w = W.CONFIGS[name]()
-    compared = check_layer(msa, w, 0, SAMPLES[name])
-    assert compared > 0
+    compared, total = check_layer(msa, w, 0, SAMPLES[name])
+    assert compared >= total // 2, f"only {compared} of {total} rows compared"
 
 
 @pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_fullsize_ragged_layer(msa, layer):
     w = W.ragged()
-    check_layer(msa, w, layer, SAMPLES["ragged"])
+    compared, total = check_layer(msa, w, layer, SAMPLES["ragged"])
+    assert compared >= total // 2, f"only {compared} of {total} rows compared"

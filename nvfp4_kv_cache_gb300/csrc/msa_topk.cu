@@ -6,7 +6,8 @@
 // twice): local = p_t / 128 is slot 0, slots 1..15 are the 15 best of blocks 0 .. local-1 in
 // descending score order, equal scores ordered by lower block id, -1 when fewer exist.
 //
-// Design: one warp per (token, group) row. Each score becomes a unique 64-bit key
+// Design: one warp per (token, group) row (a CTA per row, each warp a slice, for batches of few
+// rows longer than one warp holds in registers). Each score becomes a unique 64-bit key
 // (order-preserving fp32 bits << 32 | ~block id), so "descending score, then lower id" is one
 // integer order and ties need no special case. Rows of up to 64 candidates are sorted in
 // registers (warp bitonic network, two keys per lane). Longer rows are first filtered: the
@@ -251,6 +252,38 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
   if (lane < kCand) out[1 + lane] = res[warp][lane] ? key_id(res[warp][lane]) : -1;
 }
 
+// The same selection for a batch of few rows, some longer than one warp holds in registers
+// (32 x kRegKeys keys): a CTA per row, so that the rows spread over the SMs; each of its warps
+// takes the 15 best of one slice of the row, then one warp the 15 best of the slices'
+// candidates (keys are unique, so the 15 best of the union are the row's 15 best).
+constexpr int kSplitWarps = 8;
+
+__global__ void __launch_bounds__(32 * kSplitWarps) k_topk_split(const TopkParams p) {
+  __shared__ uint64_t buf[kSplitWarps][kSurvivors];
+  __shared__ uint64_t res[kSplitWarps][kCand];
+  __shared__ uint64_t top[kCand];
+  grid_dependency_wait();  // the indexer's scores (this kernel may launch while it finishes)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x;  // t * 4 + g
+  int32_t* out = p.sel + static_cast<int64_t>(row) * kSel;
+  const int local = row_local(p, row >> 2);  // the same for every warp of the CTA
+  if (local < 0) {
+    if (warp == 0 && lane == 0) set_status(p.status, MSA_ERR_INVALID_ARG);
+    if (warp == 0 && lane < kSel) out[lane] = -1;
+    return;
+  }
+  const float* s = p.scores + static_cast<int64_t>(row) * p.maxb;
+  const int per = ceil_div(local, kSplitWarps);
+  const int lo = min(local, warp * per), n = min(local, lo + per) - lo;
+  top15_keys([&](int i) { return score_key(s[lo + i], lo + i); }, n, buf[warp], res[warp], lane);
+  __syncthreads();
+  if (warp == 0) {
+    top15_keys([&](int i) { return res[i / kCand][i % kCand]; }, kSplitWarps * kCand, buf[0], top, lane);
+    if (lane == 0) out[0] = local;
+    if (lane < kCand) out[1 + lane] = top[lane] ? key_id(top[lane]) : -1;
+  }
+}
+
 struct CandParams {
   TopkParams t;
   int32_t kb, ke;        // this shard's block range
@@ -330,9 +363,14 @@ extern "C" msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* 
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
-  if (launch_after_previous(k_topk, dim3(ceil_div(batch->T * 4, kRowsPerCta)), dim3(32 * kRowsPerCta), 0, stream, p) !=
-      cudaSuccess)
-    return MSA_ERR_CUDA;
+  // a warp per row; a CTA per row when rows may be longer than a warp holds and so few that a
+  // CTA each fits in one wave (two per SM of the part the choice is tuned for)
+  const int rows = batch->T * 4;
+  const cudaError_t e =
+      (batch->max_blocks_per_seq > 32 * kRegKeys && rows <= 2 * kTunedSms)
+          ? launch_after_previous(k_topk_split, dim3(rows), dim3(32 * kSplitWarps), 0, stream, p)
+          : launch_after_previous(k_topk, dim3(ceil_div(rows, kRowsPerCta)), dim3(32 * kRowsPerCta), 0, stream, p);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
   return launch_status();
 }
 

@@ -157,11 +157,14 @@ def test_sharp_softmax(msa, case):
         assert moves > 0, "the case does not exercise the reference move"
 
 
-def test_topk_on_crafted_scores(msa):
-    """Ties, NaN, -inf, -0/+0, fewer than 15 candidates: GPU == the oracle's stable sort."""
+@pytest.mark.parametrize("pad", [0, 80])
+def test_topk_on_crafted_scores(msa, pad):
+    """Ties, NaN, -inf, -0/+0, fewer than 15 candidates: GPU == the oracle's stable sort. With
+    few rows (pad = 0) the rows longer than a warp holds take a CTA each; 80 more sequences push
+    the batch past that threshold, so the same rows run one warp each."""
     rng = np.random.default_rng(5)
-    seq_lens = [128 * 700 + 3, 128 * 3 + 1, 128 * 16, 5, 128 * 4096]
-    q_lens = [3, 1, 2, 1, 1]
+    seq_lens = [128 * 700 + 3, 128 * 3 + 1, 128 * 16, 5, 128 * 4096] + [128 * 2000 + 7] * pad
+    q_lens = [3, 1, 2, 1, 1] + [1] * pad
     B = len(seq_lens)
     maxb = 4096
     qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)

@@ -91,7 +91,7 @@ struct PfParams {
   int4* chunks;        // [T * 65] {first entry, count, page, group}
   int32_t* tg_bad;     // [T * 4] the (token, group) saw a bad selection or page: zero output
   uint32_t* part_o;    // [T * 64 slots][128 dims][16 heads] unnormalised partial o, f16 pairs
-  float2* part_ml;     // [T * 64 slots][16 heads] {m (log2 domain), l} of the slots with ehash >= 0
+  float2* part_ml;     // [T * 64 slots][16 heads] {m (log2 domain), l}; m = -inf: no partial
   uint32_t hmask;      // H - 1 (H a power of two)
   int32_t hbits;       // log2 H
   uint32_t* status;
@@ -113,7 +113,8 @@ __device__ __forceinline__ bool token_seq(const PfParams& p, int t, int* b_out, 
 }
 
 // One thread per (token, group, slot): validate the selection, and file the first occurrence of
-// each valid block under its (page, group) row (ehash = -1 marks a slot that gets no partial).
+// each valid block under its (page, group) row (ehash = -1 marks a slot that gets no partial;
+// k_map_fill gives those m = -inf, and the kernel writes every other slot's (m, l)).
 __global__ void __launch_bounds__(256) k_map_count(const PfParams p) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
@@ -201,7 +202,12 @@ __global__ void __launch_bounds__(256) k_map_fill(const PfParams p) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
   const int h = p.ehash[e];
-  if (h < 0) return;
+  if (h < 0) {  // a slot with no partial: m = -inf for the merge
+    float2* ml = p.part_ml + e * kHPG;
+#pragma unroll
+    for (int x = 0; x < kHPG; ++x) ml[x] = make_float2(-CUDART_INF_F, 0.f);
+    return;
+  }
   const int t = static_cast<int>(e / (4 * kSel)), g = static_cast<int>((e / kSel) % 4), slot = static_cast<int>(e % kSel);
   int b, p_tok, nb;
   token_seq(p, t, &b, &p_tok, &nb);
@@ -681,11 +687,7 @@ __global__ void __launch_bounds__(128) k_prefill_merge(const PfParams p) {
   __shared__ int any[kSel];
   const int tg = blockIdx.x, t = tg >> 2, g = tg & 3, d = threadIdx.x;
   const int64_t base = static_cast<int64_t>(tg) * kSel;
-  for (int x = d; x < kSel * kHPG; x += 128) {  // slots that got no partial count as m = -inf
-    const float2 v = p.part_ml[base * kHPG + x];  // both loads in flight; unserved slots: unused bytes
-    const bool served = p.ehash[base + x / kHPG] >= 0;
-    ml[x / kHPG][x % kHPG] = served ? v : make_float2(-CUDART_INF_F, 0.f);
-  }
+  for (int x = d; x < kSel * kHPG; x += 128) ml[x / kHPG][x % kHPG] = p.part_ml[base * kHPG + x];
   __syncthreads();
   const bool bad = p.tg_bad[tg] != 0;
   if (d < kHPG) {

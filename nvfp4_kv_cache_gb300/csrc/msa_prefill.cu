@@ -31,6 +31,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "msa.h"
 #include "msa_attn_tile.cuh"
 #include "msa_device.cuh"
@@ -112,10 +114,26 @@ __device__ __forceinline__ bool token_seq(const PfParams& p, int t, int* b_out, 
   return t - q0 >= 0 && t - q0 < ql && L >= ql && L <= p.maxb * kBS;
 }
 
+// The map's state for a new call: an empty hash table, zero counts and flags.
+__global__ void __launch_bounds__(256) k_map_init(const PfParams p) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t x = i; x <= static_cast<int64_t>(p.hmask); x += stride) {
+    p.hkeys[x] = kNoKey;
+    p.hcnt[x] = 0;
+  }
+  for (int64_t x = i; x < static_cast<int64_t>(p.T) * 4; x += stride) p.tg_bad[x] = 0;
+  if (i < 4) p.hdr[i] = 0;
+}
+
+// The kernels after k_map_init are launched as programmatic dependents of the kernel before them:
+// each waits (griddepcontrol.wait) before it touches anything that kernel writes or reads.
+
 // One thread per (token, group, slot): validate the selection, and file the first occurrence of
 // each valid block under its (page, group) row (ehash = -1 marks a slot that gets no partial;
 // k_map_fill gives those m = -inf, and the kernel writes every other slot's (m, l)).
 __global__ void __launch_bounds__(256) k_map_count(const PfParams p) {
+  grid_dependency_wait();
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
   const int t = static_cast<int>(e / (4 * kSel)), g = static_cast<int>((e / kSel) % 4), slot = static_cast<int>(e % kSel);
@@ -164,6 +182,7 @@ __global__ void __launch_bounds__(256) k_map_count(const PfParams p) {
 // One thread per row: the row's place in the entry list and its chunks, allocated with one
 // atomic per warp (rows and chunks land in arbitrary order; only their grouping matters).
 __global__ void __launch_bounds__(256) k_map_alloc(const PfParams p) {
+  grid_dependency_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const int nrows = p.hdr[0];
@@ -199,6 +218,7 @@ __global__ void __launch_bounds__(256) k_map_alloc(const PfParams p) {
 // The same threads as k_map_count place their selection in its row: the token and slot, and
 // the query position relative to the block's first key (the mask of the block's keys).
 __global__ void __launch_bounds__(256) k_map_fill(const PfParams p) {
+  grid_dependency_wait();
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(p.T) * 4 * kSel) return;
   const int h = p.ehash[e];
@@ -307,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::kOffMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nchunks = p.hdr[1];
 
   if (tid == 0) {
     for (int i = 0; i < kMetaSlots; ++i) {
@@ -340,6 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpIss) tmem_alloc(tmem_slot, kTmemCols);
   build_dequant_lut(lut, tid, kThreads);
   fence_proxy_async_smem();
+  grid_dependency_wait();  // the map (the prologue above ran while it finished)
+  const int nchunks = p.hdr[1];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -681,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sum_s 2^(m_s - M) l_s per head over the selection's partials; zero when the (token, group) is
 // bad or has none.
 __global__ void __launch_bounds__(128) k_prefill_merge(const PfParams p) {
+  grid_dependency_wait();
   __shared__ float2 ml[kSel][kHPG];
   __shared__ float wt[kSel][kHPG];
   __shared__ float winv[kHPG];
@@ -733,8 +755,13 @@ struct PfLayout {
   int hbits;
 };
 
-PfLayout pf_layout(int T) {
+// The hash table has at least twice as many slots as there are selections (sized by the
+// selections even when fewer distinct rows can exist: the keys' counters then spread over many
+// cache lines, which their atomics need).
+PfLayout pf_layout(int B, int T, int maxb) {
   using msa_host::align256;
+  (void)B;
+  (void)maxb;
   PfLayout l;
   const size_t ent = static_cast<size_t>(T) * 4 * kSel;
   l.hbits = 10;
@@ -764,7 +791,7 @@ extern "C" size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B,
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || T > kMaxT || max_blocks_per_seq < 1 ||
       max_blocks_per_seq > (1 << 20))
     return 0;
-  return pf_layout(T).total;
+  return pf_layout(B, T, max_blocks_per_seq).total;
 }
 
 extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
@@ -784,7 +811,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
     return MSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const PfLayout lay = pf_layout(batch->T);
+  const PfLayout lay = pf_layout(batch->B, batch->T, batch->max_blocks_per_seq);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < lay.total) return MSA_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PfParams p;
@@ -813,16 +840,17 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   p.hmask = lay.hslots - 1;
   p.hbits = lay.hbits;
   p.status = status;
-  if (cudaMemsetAsync(p.hdr, 0, 16, stream) != cudaSuccess ||
-      cudaMemsetAsync(p.hkeys, 0xFF, static_cast<size_t>(lay.hslots) * 8, stream) != cudaSuccess ||
-      cudaMemsetAsync(p.hcnt, 0, static_cast<size_t>(lay.hslots) * 4, stream) != cudaSuccess ||
-      cudaMemsetAsync(p.tg_bad, 0, static_cast<size_t>(p.T) * 16, stream) != cudaSuccess)
-    return MSA_ERR_CUDA;
+  {
+    const int64_t n = std::max<int64_t>(lay.hslots, static_cast<int64_t>(p.T) * 4);
+    const int ib = static_cast<int>(std::min<int64_t>((n + 255) / 256, 8 * kTunedSms));
+    k_map_init<<<ib, 256, 0, stream>>>(p);
+  }
   const int64_t ent = static_cast<int64_t>(p.T) * 4 * kSel;
   const int eb = static_cast<int>((ent + 255) / 256);
-  k_map_count<<<eb, 256, 0, stream>>>(p);
-  k_map_alloc<<<eb, 256, 0, stream>>>(p);
-  k_map_fill<<<eb, 256, 0, stream>>>(p);
+  if (launch_after_previous(k_map_count, dim3(eb), dim3(256), 0, stream, p) != cudaSuccess ||
+      launch_after_previous(k_map_alloc, dim3(eb), dim3(256), 0, stream, p) != cudaSuccess ||
+      launch_after_previous(k_map_fill, dim3(eb), dim3(256), 0, stream, p) != cudaSuccess)
+    return MSA_ERR_CUDA;
   if ((st = launch_status()) != MSA_OK) return st;
   alignas(64) CUtensorMap q_map;
   if (!rows128_tensor_map(&q_map, q, static_cast<uint64_t>(p.T) * kQHeads, kHPG)) return MSA_ERR_CUDA;
@@ -834,7 +862,9 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   // never more CTAs than chunks can exist: at most T + 64 T (each row adds at most one chunk)
   const int64_t max_chunks = ent + p.T;
   const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
-  k_prefill_tc<<<grid, kThreads, Smem::kBytes, stream>>>(p, q_map);
-  k_prefill_merge<<<static_cast<unsigned>(static_cast<int64_t>(p.T) * 4), 128, 0, stream>>>(p);
+  if (launch_after_previous(k_prefill_tc, dim3(grid), dim3(kThreads), Smem::kBytes, stream, p, q_map) != cudaSuccess ||
+      launch_after_previous(k_prefill_merge, dim3(static_cast<unsigned>(static_cast<int64_t>(p.T) * 4)), dim3(128), 0,
+                            stream, p) != cudaSuccess)
+    return MSA_ERR_CUDA;
   return launch_status();
 }

@@ -163,8 +163,9 @@ def test_topk_on_crafted_scores(msa, pad):
     few rows (pad = 0) the rows longer than a warp holds take a CTA each; 80 more sequences push
     the batch past that threshold, so the same rows run one warp each."""
     rng = np.random.default_rng(5)
-    seq_lens = [128 * 700 + 3, 128 * 3 + 1, 128 * 16, 5, 128 * 4096] + [128 * 2000 + 7] * pad
-    q_lens = [3, 1, 2, 1, 1] + [1] * pad
+    # rows of 1,024 and 1,025 candidates sit on the boundary of the in-register path
+    seq_lens = [128 * 700 + 3, 128 * 3 + 1, 128 * 16, 5, 128 * 4096, 128 * 1024 + 1, 128 * 1025 + 1] + [128 * 2000 + 7] * pad
+    q_lens = [3, 1, 2, 1, 1, 1, 1] + [1] * pad
     B = len(seq_lens)
     maxb = 4096
     qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)

@@ -220,3 +220,30 @@ def test_prefill_large_rows_split_into_chunks(msa):
     assert max(by_page.values()) >= 600
     ref = OracleSeq(w, 0, 0, "cuda", kv_blocks=np.unique(sel[sel >= 0])).attention(sel, dl.softmax_scale)
     check_attention(bf16_to_f32(out).cpu().numpy(), ref, "hot rows")
+
+
+def test_prefill_rows_with_no_key(msa):
+    """(token, group) rows that list no block, and rows whose only blocks lie after the token's
+    position (every key masked): their output is zero, as the oracle's; the other rows of the same
+    tokens are unaffected."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("no_key", [3000, 1800 + 9], [120, 40], seed=69)
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 12)
+    sel[3, 1, :] = -1            # no block listed
+    sel[50, 2, :] = -1
+    qsl = w.query_start_loc()
+    t_early = int(qsl[0])        # the first prompt token of sequence 0: position 2880, block 22
+    sel[t_early, 0, :] = -1
+    sel[t_early, 0, 0] = 23      # a later block of the sequence only: all its keys are masked
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = bf16_to_f32(run_prefill(msa, dl, w, sel, st)).cpu().numpy()
+    assert msa.status_bits(st) == 0
+    for rows_t, g in [(3, 1), (50, 2), (t_early, 0)]:
+        assert (out[rows_t, 16 * g:16 * (g + 1)] == 0).all(), (rows_t, g)
+    for b in range(w.B):
+        rows = slice(qsl[b], qsl[b] + w.q_lens[b])
+        s = sel[rows]
+        ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(s[s >= 0])).attention(s, dl.softmax_scale)
+        check_attention(out[rows], ref, f"no-key rows, seq {b}")

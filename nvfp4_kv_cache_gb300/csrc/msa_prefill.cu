@@ -758,10 +758,8 @@ struct PfLayout {
 // The hash table has at least twice as many slots as there are selections (sized by the
 // selections even when fewer distinct rows can exist: the keys' counters then spread over many
 // cache lines, which their atomics need).
-PfLayout pf_layout(int B, int T, int maxb) {
+PfLayout pf_layout(int T) {
   using msa_host::align256;
-  (void)B;
-  (void)maxb;
   PfLayout l;
   const size_t ent = static_cast<size_t>(T) * 4 * kSel;
   l.hbits = 10;
@@ -791,7 +789,7 @@ extern "C" size_t msa_prefill_workspace_size(const msa_geometry* geo, int32_t B,
   if (check_geometry(geo) != MSA_OK || B < 0 || T < 0 || T > kMaxT || max_blocks_per_seq < 1 ||
       max_blocks_per_seq > (1 << 20))
     return 0;
-  return pf_layout(B, T, max_blocks_per_seq).total;
+  return pf_layout(T).total;
 }
 
 extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch* batch, const msa_cache* cache,
@@ -811,7 +809,7 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))
     return MSA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale != softmax_scale) return MSA_ERR_INVALID_ARG;
-  const PfLayout lay = pf_layout(batch->B, batch->T, batch->max_blocks_per_seq);
+  const PfLayout lay = pf_layout(batch->T);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < lay.total) return MSA_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PfParams p;

@@ -708,15 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waitw(&st_full[jb % kStages], static_cast<uint32_t>(jb / kStages) & 1u)) return;
       RawRow rk;
       load_row(wgb + static_cast<size_t>(jb % kStages) * kStageBytes, key_k, rk);
-      uint32_t wk[32];
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
+      for (int qq = 0; qq < 4; ++qq) {  // each quarter goes to TMEM while the next is dequantised
         uint32_t uu[8];
         dequant_quarter(rk, qq, lut, uu);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) wk[8 * qq + e] = uu[e];
+        tmem_st8(tw + lanes + kColK + 8 * qq, uu);
       }
-      tmem_st32(tw + lanes + kColK, wk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

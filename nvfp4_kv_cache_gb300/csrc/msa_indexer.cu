@@ -182,18 +182,22 @@ __device__ __forceinline__ int page_seq(const int* prefix, int B, int gp) {
 }
 
 // Dequantise key row r of a staged NVFP4 page (written by a 128-byte-swizzled copy) to 128
-// E4M3 bytes: w[c] holds elements 4c .. 4c+3, the TMEM A-operand layout of one row.
-__device__ __forceinline__ void dequant_row_nvfp4(const uint8_t* pg, int r, const uint2* lut, uint32_t (&w)[32]) {
+// E4M3 bytes straight into the TMEM key tile at taddr (this thread's lane, 32 columns: column c
+// holds elements 4c .. 4c+3): each quarter of the row is stored while the next is dequantised.
+// Completes at tmem_wait_st().
+__device__ __forceinline__ void dequant_row_nvfp4_tmem(const uint8_t* pg, int r, const uint2* lut, uint32_t taddr) {
   const uint2 sc = lds64(pg + sw128_phys(static_cast<uint32_t>(kScaleOff + r * kRowScales)));
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // 32 elements: 32q .. 32q+31, scales 2q and 2q+1
+  for (int q = 0; q < 4; ++q) {
     const uint4 c = lds128(pg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * q)));
     const uint32_t s2 = ((q < 2) ? sc.x : sc.y) >> (16 * (q & 1));
     const uint2 e0 = lut[s2 & 0xFFu], e1 = lut[(s2 >> 8) & 0xFFu];
-    dq8(c.x, e0, w[8 * q + 0], w[8 * q + 1]);
-    dq8(c.y, e0, w[8 * q + 2], w[8 * q + 3]);
-    dq8(c.z, e1, w[8 * q + 4], w[8 * q + 5]);
-    dq8(c.w, e1, w[8 * q + 6], w[8 * q + 7]);
+    uint32_t w[8];
+    dq8(c.x, e0, w[0], w[1]);
+    dq8(c.y, e0, w[2], w[3]);
+    dq8(c.z, e1, w[4], w[5]);
+    dq8(c.w, e1, w[6], w[7]);
+    tmem_st8(taddr + 8 * q, w);
   }
 }
 
@@ -478,14 +482,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
       const int s = n % kStages, a = n % kATiles;
       if (!warp_wait(&full[s], static_cast<uint32_t>(n / kStages) & 1u, abort_flag)) break;
       const SlotInfo si = info[s];
-      uint32_t w[32];
+      if (!warp_wait(&a_empty[a], (static_cast<uint32_t>(n / kATiles) & 1u) ^ 1u, abort_flag)) break;
+      tc_fence_after();
       if constexpr (kNv && !kExact) {
-        if (si.valid) dequant_row_nvfp4(stages + static_cast<size_t>(s) * S::kPage, i, lut, w);
+        if (si.valid) dequant_row_nvfp4_tmem(stages + static_cast<size_t>(s) * S::kPage, i, lut, t_a + kACols * a + lane_base);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the warp's reads of the stage are done
       }
-      if (!warp_wait(&a_empty[a], (static_cast<uint32_t>(n / kATiles) & 1u) ^ 1u, abort_flag)) break;
-      tc_fence_after();
       if (si.b != cur_b) {
         cur_b = si.b;
         q0 = p.qsl[cur_b];
@@ -525,6 +528,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         if (lane == 0) *tag = cur_b;
       }
       if constexpr (kExact) {  // two halves of the f16 row, then the stage is free
+        uint32_t w[32];
         const uint8_t* pg = stages + static_cast<size_t>(s) * S::kPage;
         if (si.valid) dequant_half_exact(pg, i, 0, lut16, w);
         if (si.valid) tmem_st32(t_a + kACols * a + lane_base, w);
@@ -534,7 +538,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       } else if constexpr (kNv) {
-        if (si.valid) tmem_st32(t_a + kACols * a + lane_base, w);
         tmem_wait_st();
       }
       tc_fence_before();

@@ -346,6 +346,24 @@ msa_status msa_sparse_attn_decode_noalloc(const msa_geometry* geo, const msa_bat
 /* Size in bytes of the device array msa_sparse_attn_decode_noalloc uses. */
 size_t msa_noalloc_scratch_bytes(void);
 
+/* The indexer for prompts (the prefill / many-query path: "MiniMax M3 in vLLM ...",
+ * "MiniMax 稀疏注意力后端" lists prefill indexer scoring as its own kernel, and "预填充执行" scores a
+ * prompt's blocks before selecting them). The same scores as msa_indexer_decode (block_scores
+ * [t][g][k] = max over the cache positions j <= p_t of block k of index_q[t][g] . ik(j), -inf
+ * for a block with no such j; entries k >= the sequence's block count are not written) for a
+ * batch of any number of query tokens per sequence (max_q_len up to 2^20, T up to 2^22, B up to
+ * 4096). Each index page is read and dequantised once for up to 128 query tokens (512 index-query
+ * rows) of its sequence. Arguments, layouts and errors as msa_indexer_decode. */
+msa_status msa_indexer_prefill(const msa_geometry* geo, const msa_batch* batch,
+                               const msa_cache* cache, const uint8_t* index_q,
+                               float* block_scores, uint32_t* status, cudaStream_t stream);
+
+/* msa_topk_blocks for a prefill batch (max_q_len up to 2^20, T up to 2^22): the same rule,
+ * layouts and errors for every (token, group) row. */
+msa_status msa_topk_prefill(const msa_geometry* geo, const msa_batch* batch,
+                            const float* block_scores, int32_t* sel, uint32_t* status,
+                            cudaStream_t stream);
+
 /* Workspace bytes msa_prefill_attn needs: a hash table and the selection lists of the key-block
  * -> query map, and the per-(token, group, slot) partial results (4 KB of unnormalised output and
  * 128 B of (max, sum) per slot): about 300 KB a query token, a function of T alone (T up to

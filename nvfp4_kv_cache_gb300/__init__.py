@@ -83,6 +83,8 @@ _SIGS = {
     "msa_topk_blocks": (_I32, [_GP, _BP, _P, _P, _P, _P]),
     "msa_indexer_decode_range": (_I32, [_GP, _BP, _CP, _P, _I32, _I32, _P, _P, _P]),
     "msa_indexer_decode_exact": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
+    "msa_indexer_prefill": (_I32, [_GP, _BP, _CP, _P, _P, _P, _P]),
+    "msa_topk_prefill": (_I32, [_GP, _BP, _P, _P, _P, _P]),
     "msa_prefill_workspace_size": (_SZ, [_GP, _I32, _I32, _I32]),
     "msa_prefill_attn": (_I32, [_GP, _BP, _CP, _P, _P, ctypes.c_float, _P, _SZ, _P, _P, _P]),
     "msa_topk_candidates": (_I32, [_GP, _BP, _P, _I32, _I32, _P, _P, _P]),
@@ -240,6 +242,21 @@ def msa_indexer_decode_exact(batch: Batch, cache: Cache, index_q: torch.Tensor, 
 
 def msa_prefill_workspace_size(B: int, T: int, max_blocks_per_seq: int) -> int:
     return int(_lib.msa_prefill_workspace_size(ctypes.byref(GEOMETRY), B, T, max_blocks_per_seq))
+
+
+def msa_indexer_prefill(batch: Batch, cache: Cache, index_q: torch.Tensor, block_scores: torch.Tensor,
+                        status: Optional[torch.Tensor] = None) -> None:
+    """The indexer for a prefill batch (any number of query tokens per sequence)."""
+    _check(_lib.msa_indexer_prefill(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), ctypes.byref(cache.c),
+                                    _ptr(index_q), _ptr(block_scores), _ptr(status), _stream()),
+           "msa_indexer_prefill")
+
+
+def msa_topk_prefill(batch: Batch, block_scores: torch.Tensor, sel: torch.Tensor,
+                     status: Optional[torch.Tensor] = None) -> None:
+    """The block selection for a prefill batch (any number of query tokens per sequence)."""
+    _check(_lib.msa_topk_prefill(ctypes.byref(GEOMETRY), ctypes.byref(batch.c), _ptr(block_scores), _ptr(sel),
+                                 _ptr(status), _stream()), "msa_topk_prefill")
 
 
 def msa_prefill_attn(batch: Batch, cache: Cache, q: torch.Tensor, sel: torch.Tensor, softmax_scale: float,

@@ -57,6 +57,20 @@ inline msa_status check_batch(const msa_batch* b) {
   return MSA_OK;
 }
 
+// A prefill / many-query batch: any number of query tokens per sequence (max_q_len up to 2^20),
+// up to 2^22 in all (T); the rest as check_batch.
+inline msa_status check_prefill_batch(const msa_batch* b) {
+  if (b == nullptr) return MSA_ERR_INVALID_ARG;
+  if (b->B < 0 || b->T < 0 || b->B > 4096 || b->T > (1 << 22)) return MSA_ERR_INVALID_ARG;
+  if (b->max_q_len < 1 || b->max_q_len > (1 << 20)) return MSA_ERR_INVALID_ARG;
+  if (b->max_blocks_per_seq < 1 || b->max_blocks_per_seq > (1 << 20)) return MSA_ERR_INVALID_ARG;
+  if (b->B > 0 && (b->query_start_loc == nullptr || b->seq_lens == nullptr || b->block_table == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned(b->query_start_loc, 4) || !aligned(b->seq_lens, 4) || !aligned(b->block_table, 4))
+    return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
 inline msa_status check_cache(const msa_cache* c, bool need_index, bool need_kv) {
   if (c == nullptr) return MSA_ERR_INVALID_ARG;
   if (c->num_pages < 0) return MSA_ERR_INVALID_ARG;

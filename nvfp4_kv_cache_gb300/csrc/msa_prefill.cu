@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kChunk = 64;             // selections served by one dequantised (page, group) block
 constexpr int kTileSel = 8;            // selections per MMA tile: 8 x 16 query heads = M 128
-constexpr int kMaxQ = 1 << 20;         // query tokens per sequence
 constexpr int kMaxT = 1 << 22;         // query tokens per call (entries pack t << 4 | slot)
 constexpr uint64_t kNoKey = ~0ull;     // an empty hash slot
 
@@ -797,13 +796,8 @@ extern "C" msa_status msa_prefill_attn(const msa_geometry* geo, const msa_batch*
                                        size_t workspace_bytes, uint16_t* out, uint32_t* status, cudaStream_t stream) {
   msa_status st = check_geometry(geo);
   if (st != MSA_OK) return st;
-  if (batch == nullptr) return MSA_ERR_INVALID_ARG;
   // a prefill batch: any number of query tokens per sequence (max_q_len up to 2^20)
-  if (batch->B < 0 || batch->T < 0 || batch->B > kMaxB || batch->T > kMaxT) return MSA_ERR_INVALID_ARG;
-  if (batch->max_q_len < 1 || batch->max_q_len > kMaxQ) return MSA_ERR_INVALID_ARG;
-  if (batch->max_blocks_per_seq < 1 || batch->max_blocks_per_seq > (1 << 20)) return MSA_ERR_INVALID_ARG;
-  if (batch->B > 0 && (batch->query_start_loc == nullptr || batch->seq_lens == nullptr || batch->block_table == nullptr))
-    return MSA_ERR_INVALID_ARG;
+  if ((st = check_prefill_batch(batch)) != MSA_OK) return st;
   if ((st = check_cache(cache, false, true)) != MSA_OK) return st;
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (q == nullptr || sel == nullptr || out == nullptr || !aligned(q, 16) || !aligned(sel, 4) || !aligned(out, 16))

@@ -352,14 +352,30 @@ using namespace msa_host;
 
 namespace {
 msa_status topk_setup(const msa_geometry* geo, const msa_batch* batch, const float* block_scores, int32_t* sel,
-                      uint32_t* status, TopkParams* p);
+                      uint32_t* status, TopkParams* p, bool prefill = false);
+msa_status topk_launch(const msa_batch* batch, const TopkParams& p, const float* block_scores, int32_t* sel,
+                       cudaStream_t stream);
 }  // namespace
 
 extern "C" msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* batch, const float* block_scores,
                                       int32_t* sel, uint32_t* status, cudaStream_t stream) {
   TopkParams p;
-  msa_status st = topk_setup(geo, batch, block_scores, sel, status, &p);
+  const msa_status st = topk_setup(geo, batch, block_scores, sel, status, &p);
   if (st != MSA_OK) return st;
+  return topk_launch(batch, p, block_scores, sel, stream);
+}
+
+extern "C" msa_status msa_topk_prefill(const msa_geometry* geo, const msa_batch* batch, const float* block_scores,
+                                       int32_t* sel, uint32_t* status, cudaStream_t stream) {
+  TopkParams p;
+  const msa_status st = topk_setup(geo, batch, block_scores, sel, status, &p, true);
+  if (st != MSA_OK) return st;
+  return topk_launch(batch, p, block_scores, sel, stream);
+}
+
+namespace {
+msa_status topk_launch(const msa_batch* batch, const TopkParams& p, const float* block_scores, int32_t* sel,
+                       cudaStream_t stream) {
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
@@ -374,12 +390,11 @@ extern "C" msa_status msa_topk_blocks(const msa_geometry* geo, const msa_batch* 
   return launch_status();
 }
 
-namespace {
 msa_status topk_setup(const msa_geometry* geo, const msa_batch* batch, const float* block_scores, int32_t* sel,
-                      uint32_t* status, TopkParams* p) {
+                      uint32_t* status, TopkParams* p, bool prefill) {
   msa_status st = check_geometry(geo);
   if (st != MSA_OK) return st;
-  if ((st = check_batch(batch)) != MSA_OK) return st;
+  if ((st = prefill ? check_prefill_batch(batch) : check_batch(batch)) != MSA_OK) return st;
   p->B = batch->B;
   p->T = batch->T;
   p->maxb = batch->max_blocks_per_seq;

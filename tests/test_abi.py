@@ -105,3 +105,53 @@ def test_host_step_checks_without_gpu(lib):
     assert f(*args(good, ctypes.byref(batch), ctypes.byref(cache), None, 0)) == 1         # no host description
     io = (ctypes.c_void_p * 6)(*([0x2000] * 6))
     assert f(*args(good, ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(io), 4)) == 1  # unknown flag
+
+
+def test_prefill_indexer_and_selection_checks_without_gpu(lib):
+    """msa_indexer_prefill and msa_topk_prefill take prefill batches (more than 8 query tokens a
+    sequence) and reject bad geometry, batches and caches before any CUDA call; an empty batch
+    is a successful no-op."""
+
+    class Geo(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int32) for n in "abcdefgh"]
+
+    class Batch(ctypes.Structure):
+        _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("qsl", ctypes.c_void_p),
+                    ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("maxb", ctypes.c_int32),
+                    ("max_q_len", ctypes.c_int32)]
+
+    class Cache(ctypes.Structure):
+        _fields_ = [("kv", ctypes.c_void_p), ("ix", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                    ("pages", ctypes.c_int32)]
+
+    ix = lib.msa_indexer_prefill
+    ix.restype = ctypes.c_int32
+    ix.argtypes = [ctypes.c_void_p] * 7
+    tk = lib.msa_topk_prefill
+    tk.restype = ctypes.c_int32
+    tk.argtypes = [ctypes.c_void_p] * 6
+    good = Geo(64, 4, 128, 128, 128, 16, 1, 0)
+    bad = Geo(64, 4, 128, 128, 64, 16, 1, 0)  # 64-token blocks
+    dummy = 0x1000  # never dereferenced: the checks stop before any access
+    cache = Cache(0x10000, 0x10000, 0, 8)
+    no_index = Cache(0x10000, None, 0, 8)
+    empty = Batch(0, 0, dummy, dummy, dummy, 16, 1)
+    long_prompt = Batch(1, 0, dummy, dummy, dummy, 16, 1 << 20)  # up to 2^20 tokens a sequence: accepted
+    too_long = Batch(1, 4, dummy, dummy, dummy, 16, (1 << 20) + 1)
+    too_many = Batch(1, (1 << 22) + 1, dummy, dummy, dummy, 16, 1 << 20)
+    r = lambda p: ctypes.byref(p)
+    assert ix(r(bad), r(empty), r(cache), None, None, None, None) == 2
+    assert ix(r(good), None, r(cache), None, None, None, None) == 1
+    assert ix(r(good), r(too_long), r(cache), None, None, None, None) == 1
+    assert ix(r(good), r(too_many), r(cache), None, None, None, None) == 1
+    assert ix(r(good), r(empty), r(no_index), None, None, None, None) == 1
+    assert ix(r(good), r(empty), r(cache), None, None, None, None) == 0
+    assert ix(r(good), r(long_prompt), r(cache), None, None, None, None) == 0  # T = 0: nothing to do
+    assert tk(r(bad), r(empty), None, None, None, None) == 2
+    assert tk(r(good), r(too_long), None, None, None, None) == 1
+    assert tk(r(good), r(long_prompt), None, None, None, None) == 0
+    # the decode selection keeps its own limit of 8 query tokens a sequence
+    dk = lib.msa_topk_blocks
+    dk.restype = ctypes.c_int32
+    dk.argtypes = [ctypes.c_void_p] * 6
+    assert dk(r(good), r(long_prompt), None, None, None, None) == 1

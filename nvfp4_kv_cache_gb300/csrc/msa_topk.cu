@@ -132,6 +132,7 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t k, int lane) {
 constexpr int kRowsPerCta = 8;
 constexpr int kSurvivors = 64;
 constexpr int kRegKeys = 32;  // rows of up to 32 x 32 keys are held in registers (one load each)
+constexpr int kRegKeysShort = 4;  // the same for rows of up to 128 keys (fewer registers, more warps per SM)
 constexpr int kCand = kSel - 1;  // candidates per (token, group) and shard: the 15 best non-local blocks
 
 // The 15 largest of the n keys key_at(0 .. n-1) (unique; 0 = none), descending, into res[0..14]
@@ -139,7 +140,7 @@ constexpr int kCand = kSel - 1;  // candidates per (token, group) and shard: the
 // (15 distinct elements reach it), so only keys at or above it survive (typically a few
 // dozen) and those are sorted in registers; more than 64 survivors (adversarial ties across
 // lanes) fall back to repeated warp argmax.
-template <class KeyAt>
+template <int KR = kRegKeys, class KeyAt>
 __device__ void top15_keys(KeyAt key_at, int n, uint64_t* buf, uint64_t* res, int lane) {
   uint64_t k0 = 0, k1 = 0;
   bool sorted = false;
@@ -147,18 +148,18 @@ __device__ void top15_keys(KeyAt key_at, int n, uint64_t* buf, uint64_t* res, in
     k0 = 2 * lane < n ? key_at(2 * lane) : 0ull;
     k1 = 2 * lane + 1 < n ? key_at(2 * lane + 1) : 0ull;
     sorted = true;
-  } else if (n <= 32 * kRegKeys) {
+  } else if (n <= 32 * KR) {
     // the same filter with the row's keys loaded once, all loads in flight together
-    uint64_t kk[kRegKeys];
+    uint64_t kk[KR];
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) kk[j] = 32 * j + lane < n ? key_at(32 * j + lane) : 0ull;
+    for (int j = 0; j < KR; ++j) kk[j] = 32 * j + lane < n ? key_at(32 * j + lane) : 0ull;
     uint64_t best = 0;
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) best = kk[j] > best ? kk[j] : best;
+    for (int j = 0; j < KR; ++j) best = kk[j] > best ? kk[j] : best;
     const uint64_t tau = __shfl_sync(0xffffffffu, warp_sort32_desc(best, lane), 14);
     int count = 0;
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < KR; ++j) {
       const bool keep = kk[j] >= tau && kk[j] != 0ull;
       const uint32_t m = __ballot_sync(0xffffffffu, keep);
       const int pos = count + __popc(m & ((1u << lane) - 1u));
@@ -231,7 +232,9 @@ __device__ __forceinline__ int row_local(const TopkParams& p, int t) {
   return (L - ql + (t - q0)) / kBS;
 }
 
-// One warp per (token, group) row: sel = [local, the 15 best of blocks 0 .. local-1].
+// One warp per (token, group) row: sel = [local, the 15 best of blocks 0 .. local-1]; rows of up
+// to 32 x KR keys are loaded into registers at once.
+template <int KR>
 __global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
   __shared__ uint64_t buf[kRowsPerCta][kSurvivors];
   __shared__ uint64_t res[kRowsPerCta][kCand];
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) k_topk(const TopkParams p) {
     return;
   }
   const float* s = p.scores + static_cast<int64_t>(row) * p.maxb;
-  top15_keys([&](int i) { return score_key(s[i], i); }, local, buf[warp], res[warp], lane);
+  top15_keys<KR>([&](int i) { return score_key(s[i], i); }, local, buf[warp], res[warp], lane);
   if (lane == 0) out[0] = local;
   if (lane < kCand) out[1 + lane] = res[warp][lane] ? key_id(res[warp][lane]) : -1;
 }
@@ -379,13 +382,17 @@ msa_status topk_launch(const msa_batch* batch, const TopkParams& p, const float*
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
-  // a warp per row; a CTA per row when rows may be longer than a warp holds and so few that a
-  // CTA each fits in one wave (two per SM of the part the choice is tuned for)
+  // a warp per row (with fewer registers, so more warps per SM, when no row can exceed 128
+  // blocks); a CTA per row when rows may be longer than a warp holds and so few that a CTA each
+  // fits in one wave (two per SM of the part the choice is tuned for)
   const int rows = batch->T * 4;
+  const dim3 grid(ceil_div(rows, kRowsPerCta)), block(32 * kRowsPerCta);
   const cudaError_t e =
       (batch->max_blocks_per_seq > 32 * kRegKeys && rows <= 2 * kTunedSms)
           ? launch_after_previous(k_topk_split, dim3(rows), dim3(32 * kSplitWarps), 0, stream, p)
-          : launch_after_previous(k_topk, dim3(ceil_div(rows, kRowsPerCta)), dim3(32 * kRowsPerCta), 0, stream, p);
+      : batch->max_blocks_per_seq <= 32 * kRegKeysShort
+          ? launch_after_previous(k_topk<kRegKeysShort>, grid, block, 0, stream, p)
+          : launch_after_previous(k_topk<kRegKeys>, grid, block, 0, stream, p);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   return launch_status();
 }

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kPiThreads, 1)
     }
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 1);  // the epilogue warpgroup that read the tile's accumulator
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
@@ -342,8 +342,7 @@ __global__ void __launch_bounds__(kPiThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 32 E4M3 a step: +32 B in both operands
             tc_mma_f8(tmem + 128u * e, qdesc + 2 * kk, kdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-          tc_commit(&d_full[e]);
-          tc_commit(&q_empty[qs]);
+          tc_commit(&d_full[e]);  // the epilogue frees the query tile once it has seen this
           issued = true;
           ++dn[e];
           ++qc;
@@ -387,16 +386,21 @@ __global__ void __launch_bounds__(kPiThreads, 1)
     const int wq = warp & 3;  // TMEM lane quarter
     const int r = 32 * wq + lane;
     const uint32_t taddr = tmem + 128u * e + (static_cast<uint32_t>(32 * wq) << 16);
-    int gt = 0, dn = 0;
+    int gt = 0, dn = 0, qc = 0;  // all tiles, this warpgroup's live tiles, all live tiles
     for (int x = blockIdx.x; x < items; x += gridDim.x) {
       const PiItem it = pi_item(p, prefix, x);
       for (int i = it.i0; i < it.i1; ++i, ++gt) {
+        const bool live = it.active && pi_tile_live(it, i);
+        const int qs = qc % kQStages;
+        qc += live ? 1 : 0;
         if ((gt & 1) != e) continue;
         const int rr = kTileRows * i + r;  // the row within the sequence's rows
         const bool mine = rr < 4 * it.ql;
         float m = -CUDART_INF_F;
-        if (it.active && pi_tile_live(it, i)) {
+        if (live) {
           const bool got = waitw(&d_full[e], static_cast<uint32_t>(dn) & 1u);
+          // the tile's MMAs have landed: its query tile may be refilled
+          if (wq == 0 && lane == 0) mbar_arrive(&q_empty[qs]);
           if (got) {
             tc_fence_after();
             // keys 0 .. nvis-1 of the block are at or before the row's position

@@ -52,6 +52,31 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def fp8_tensor_peak():
+    """Dense E4M3 tensor peak (TFLOP/s) for a kernel timed alone: the measured bf16 burst figure
+    x 2, the nominal FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return 2.0 * float(json.load(open(p))["bf16_tflops"]), "measured bf16 burst x 2"
+    return 2.0 * 1900.0, "fallback bf16 x 2"
+
+
+def prefill_live_pairs(w: W.Workload) -> int:
+    """(tile of 128 index-query rows, index page) pairs the prefill indexer scores with an MMA:
+    the pages each tile's last token reaches."""
+    qsl = w.query_start_loc()
+    n = 0
+    for b in range(w.B):
+        L, ql = w.seq_lens[b], w.q_lens[b]
+        if ql == 0:
+            continue
+        nb = (L + 127) // 128
+        for i in range((4 * ql + 127) // 128):
+            last = L - ql + min(ql - 1, (128 * (i + 1) - 1) // 4)
+            n += min(nb, last // 128 + 1)
+    return n
+
+
 def index_bytes(w: W.Workload, layer: int) -> int:
     """Algorithmic bytes of the index scan: every valid token's index key once (shared pages
     once), plus the index queries."""
@@ -310,6 +335,65 @@ def time_prefill(msa, steps: int, warmup: int, flush, dev):
             "selections": "local block + 15 distinct earlier blocks drawn uniformly per (token, group)"}
 
 
+def time_prefill_path(msa, steps: int, warmup: int, flush, dev):
+    """The whole prefill path on the same 2,048-token prompt chunk at 16K context: the prefill
+    indexer, the selection and the block-major attention on the selection the indexer makes,
+    each stage timed with events between the calls."""
+    import torch
+
+    from workloads.device import DeviceLayer
+
+    wp = W.make("prefill B=1 L=16384 q_len=2048", [16384], [2048], seed=5)
+    dlp = DeviceLayer(wp, 0, device=dev)
+    maxb = dlp.batch.max_blocks
+    scores = torch.empty((wp.T, 4, maxb), dtype=torch.float32, device=dev)
+    sel = torch.empty((wp.T, 4, 16), dtype=torch.int32, device=dev)
+    out = torch.empty((wp.T, 64, 128), dtype=torch.uint16, device=dev)
+    wsp = torch.empty(msa.msa_prefill_workspace_size(wp.B, wp.T, maxb), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(ev=None):
+        if ev:
+            ev[0].record()
+        msa.msa_indexer_prefill(dlp.batch, dlp.cache, dlp.iq8, scores, st)
+        if ev:
+            ev[1].record()
+        msa.msa_topk_prefill(dlp.batch, scores, sel, st)
+        if ev:
+            ev[2].record()
+        msa.msa_prefill_attn(dlp.batch, dlp.cache, dlp.q8, sel, dlp.softmax_scale, out, wsp, st)
+        if ev:
+            ev[3].record()
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        run(evs[i])
+    torch.cuda.synchronize()
+    assert msa.status_bits(st) == 0
+    stage = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) * 1e3 for j in range(3)]
+    total = statistics.mean(e[0].elapsed_time(e[3]) for e in evs) * 1e3
+    rows, chunks, entries, _ = wsp[:16].view(torch.int32).cpu().tolist()
+    pairs = prefill_live_pairs(wp)
+    flops = pairs * 2 * 128 * 128 * 128
+    peak, kind = fp8_tensor_peak()
+    tflops = flops / (stage[0] * 1e-6) / 1e12
+    nb = (wp.seq_lens[0] + 127) // 128
+    idx_bytes = nb * 9216 + wp.T * 512 + wp.T * 4 * nb * 4  # pages once, index queries, scores
+    return {"workload": wp.name, "us_per_call": total, "tokens_per_s": wp.T / total * 1e6,
+            "stages_us": {"indexer": stage[0], "topk": stage[1], "attention": stage[2]},
+            "indexer_roofline": {"kernel": "k_indexer_prefill (msa_indexer_prefill)", "bound": "tensor",
+                                 "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                                 "peak_kind": kind, "mma_pairs": pairs, "flops": flops,
+                                 "algorithmic_bytes": idx_bytes},
+            "attention_distinct_blocks_read": rows, "attention_kv_dequantisations": chunks,
+            "attention_selections_served": entries,
+            "selections": "the prefill indexer's own (msa_topk_prefill of its scores)"}
+
+
 PER_CONFIG_STEPS, PER_CONFIG_WARMUP = 8, 3
 
 
@@ -488,6 +572,8 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
 
     # ---- the prefill (many-query) attention path, rank 0 alone, on its own synthetic prompt
     prefill = time_prefill(msa, args.steps, args.warmup, flush, dev) if rank == 0 and args.config == "spec" else None
+    prefill_path = (time_prefill_path(msa, args.steps, args.warmup, flush, dev)
+                    if rank == 0 and args.config == "spec" else None)
 
     # ---- end to end through host buffers: the library's host-buffer step (pinned H2D of the
     # step's inputs and D2H of its output on a copy stream, overlapped with the kernels), and
@@ -594,6 +680,7 @@ def run_ours(args, w: W.Workload, rank: int, world: int, local_rank: int):
         "stages_us": {"indexer": stage_ms[0] * 1e3, "topk": stage_ms[1] * 1e3, "attention": stage_ms[2] * 1e3},
         "indexer_exact_us": None if exact_ms is None else exact_ms * 1e3,
         "prefill_attn": prefill,
+        "prefill_path": prefill_path,
         "roofline": roof[dominant],
         "roofline_stages": roof,
         "e2e": {"value": e2e_ms * 1e3, "unit": "us/layer-step", "h2d_bytes_per_step": int(h2d),
@@ -620,7 +707,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the lines of the other configurations")
     ap.add_argument("--prefill-only", action="store_true",
-                    help="time the prefill attention alone (its 2,048-token prompt) and print its record")
+                    help="time the prefill attention (its 2,048-token prompt) and the prefill path "
+                         "(indexer, selection, attention) and print their records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -635,7 +723,8 @@ def main():
         dev = torch.device("cuda", local_rank)
         torch.cuda.set_device(dev)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        print(json.dumps({"prefill_attn": time_prefill(msa, args.steps, args.warmup, flush, dev)}), flush=True)
+        print(json.dumps({"prefill_attn": time_prefill(msa, args.steps, args.warmup, flush, dev),
+                          "prefill_path": time_prefill_path(msa, args.steps, args.warmup, flush, dev)}), flush=True)
         return
     w = W.CONFIGS[args.config]()
     if args.impl == "reference":

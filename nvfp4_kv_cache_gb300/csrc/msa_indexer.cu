@@ -201,30 +201,31 @@ __device__ __forceinline__ void dequant_row_nvfp4_tmem(const uint8_t* pg, int r,
   }
 }
 
-// Dims 64 h .. 64 h + 63 of key row r of a staged NVFP4 page as exact f16 (table entries of
-// build_exact_lut): w[c] holds elements 64 h + 2c, +1, the TMEM A-operand layout of half a row.
-__device__ __forceinline__ void dequant_half_exact(const uint8_t* pg, int r, int h, const uint4* lut,
-                                                   uint32_t (&w)[32]) {
+// Key row r of a staged NVFP4 page as exact f16 (table entries of build_exact_lut) straight into
+// the TMEM key tile at taddr (this thread's lane, 64 columns: column c holds elements 2c, 2c+1):
+// each 32 elements are stored while the next are dequantised. Completes at tmem_wait_st().
+__device__ __forceinline__ void dequant_row_exact_tmem(const uint8_t* pg, int r, const uint4* lut, uint32_t taddr) {
   const uint2 sc2 = lds64(pg + sw128_phys(static_cast<uint32_t>(kScaleOff + r * kRowScales)));
-  const uint32_t sh = h ? sc2.y : sc2.x;  // the four scales of dims 64 h .. 64 h + 63
 #pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {  // 32 elements: 64 h + 32 qq .. +31, scales 2 qq and 2 qq + 1 of sh
-    const uint4 c = lds128(pg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * (2 * h + qq))));
-    const uint32_t s2 = sh >> (16 * qq);
+  for (int q = 0; q < 4; ++q) {  // 32 elements: 32 q .. +31, scales 2 q and 2 q + 1 of the row
+    const uint4 c = lds128(pg + sw128_phys(static_cast<uint32_t>(r * kRowCodes + 16 * q)));
+    const uint32_t s2 = ((q < 2) ? sc2.x : sc2.y) >> (16 * (q & 1));
     const uint4 t0 = lut[s2 & 0xFFu], t1 = lut[(s2 >> 8) & 0xFFu];
+    uint32_t w[16];
     uint32_t o[4];
     dq8_f16(c.x, t0, o);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[16 * qq + e] = o[e];
+    for (int e = 0; e < 4; ++e) w[e] = o[e];
     dq8_f16(c.y, t0, o);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[16 * qq + 4 + e] = o[e];
+    for (int e = 0; e < 4; ++e) w[4 + e] = o[e];
     dq8_f16(c.z, t1, o);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[16 * qq + 8 + e] = o[e];
+    for (int e = 0; e < 4; ++e) w[8 + e] = o[e];
     dq8_f16(c.w, t1, o);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[16 * qq + 12 + e] = o[e];
+    for (int e = 0; e < 4; ++e) w[12 + e] = o[e];
+    tmem_st16(taddr + 16 * q, w);
   }
 }
 
@@ -527,13 +528,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, c
         __syncwarp();
         if (lane == 0) *tag = cur_b;
       }
-      if constexpr (kExact) {  // two halves of the f16 row, then the stage is free
-        uint32_t w[32];
+      if constexpr (kExact) {  // the f16 row, then the stage is free
         const uint8_t* pg = stages + static_cast<size_t>(s) * S::kPage;
-        if (si.valid) dequant_half_exact(pg, i, 0, lut16, w);
-        if (si.valid) tmem_st32(t_a + kACols * a + lane_base, w);
-        if (si.valid) dequant_half_exact(pg, i, 1, lut16, w);
-        if (si.valid) tmem_st32(t_a + kACols * a + 32 + lane_base, w);
+        if (si.valid) dequant_row_exact_tmem(pg, i, lut16, t_a + kACols * a + lane_base);
         tmem_wait_st();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);

@@ -704,8 +704,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bar_vote = kBarVote + w, bar_x = kBarX + w;
     int jg = 0, nre = 0;  // blocks seen; rescale events (alternate the two reduction buffers)
 
-    auto do_k = [&](int jb) {  // K rows of block jb -> the TMEM K tile
-      if (!waitw(&st_full[jb % kStages], static_cast<uint32_t>(jb / kStages) & 1u)) return;
+    // K rows of block jb -> the TMEM K tile; with `finish`, the stores are waited for and the
+    // tile announced here, else by k_finish() once the caller has other work in flight
+    auto k_finish = [&]() {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ka_full);
+    };
+    auto do_k = [&](int jb, bool finish) {
+      if (!waitw(&st_full[jb % kStages], static_cast<uint32_t>(jb / kStages) & 1u)) return false;
       RawRow rk;
       load_row(wgb + static_cast<size_t>(jb % kStages) * kStageBytes, key_k, rk);
 #pragma unroll
@@ -714,10 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dequant_quarter(rk, qq, lut, uu);
         tmem_st8(tw + lanes + kColK + 8 * qq, uu);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ka_full);
+      if (finish) k_finish();
+      return true;
     };
 
     for (int k = 0;; ++k) {
@@ -731,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref[4], l[4];
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) m_ref[hh] = l[hh] = 0.f;
-      do_k(jg);
+      do_k(jg, true);
       bool quit = false;
       for (int j = 0; j < n; ++j, ++jg) {
         uint8_t* stg = wgb + static_cast<size_t>(jg % kStages) * kStageBytes;
@@ -842,8 +848,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
           }
         }
-        // ---- K of the next block (its S MMA runs while this block's V and P are made)
-        if (j + 1 < n) do_k(jg + 1);
+        // ---- K of the next block (its S MMA runs while this block's V and P are made); its
+        // stores are waited for halfway through the V rows
+        const bool k_pending = j + 1 < n && do_k(jg + 1, false);
         // ---- V rows -> the E4M3 V tile over the stage: row vrow = key position, MN-major
         if (ok) {
           uint8_t* vt = stg + (vrow >> 3) * 1024 + (vrow & 7) * 128;
@@ -853,7 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dequant_quarter(rv, qq, lut, uu);
             *reinterpret_cast<uint4*>(vt + (((2 * qq) ^ (vrow & 7)) << 4)) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
             *reinterpret_cast<uint4*>(vt + (((2 * qq + 1) ^ (vrow & 7)) << 4)) = make_uint4(uu[4], uu[5], uu[6], uu[7]);
+            if (qq == 3 && k_pending) k_finish();
           }
+        } else if (k_pending) {
+          k_finish();
         }
         // ---- P = exp2(d) -> P^T hi / lo (the tile is free once PV(jg - 1) has landed)
         if (waitw(pv_done, static_cast<uint32_t>(jg - 1) & 1u)) {

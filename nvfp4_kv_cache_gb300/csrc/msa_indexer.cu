@@ -46,24 +46,39 @@
 namespace msa {
 namespace {
 
-constexpr int kDqGroups = 3;                     // dequant groups (4 warps each)
-constexpr int kEpGroups = 3;                     // max-pool groups (4 warps each)
-constexpr int kMmaWarps = 3;                     // MMA-issuing warps (pages in turn)
-constexpr int kWarpDq = 1 + kMmaWarps;           // first dequant warp
-constexpr int kWarpEp = kWarpDq + 4 * kDqGroups; // first max-pool warp
-constexpr int kIdxThreads = 32 * (kWarpEp + 4 * kEpGroups);
-constexpr int kDTiles = 9;                       // TMEM accumulators (32 columns each)
 constexpr int kTmemCols = 512;
 // The exact-score variant (NVFP4 keys to f16 with no E4M3 re-rounding, f16 score MMA): an
 // internal index kind next to MSA_INDEX_NVFP4 and MSA_INDEX_FP8.
 constexpr int kIdxNvExact = 2;
-// Partial-maximum slots of the max-pool quarters: page n uses slot n % kPartSlots. A slot is
-// written again only by page n + kPartSlots, whose MMA needed its accumulator released by all
-// four quarters at page n + kPartSlots - kDTiles, which each quarter reaches after combining
-// page n (a warp takes its pages in order): 2 * kDTiles slots are enough.
-constexpr int kPartSlots = 2 * kDTiles;
-static_assert(kDTiles % kEpGroups == 0 && kDTiles % kMmaWarps == 0, "an accumulator serves one group");
-static_assert(kIdxThreads <= 1024, "one CTA");
+
+// Warp roles per index kind: a producer warp, kMmaWarps MMA-issuing warps (pages in turn),
+// kDqGroups dequant groups and three max-pool groups of four warps, and kDTiles TMEM
+// accumulators of 32 columns. The exact (f16) keys cost twice the dequant work of the E4M3 ones,
+// so that kind runs four dequant groups and two MMA warps (which have the slack) where the others
+// run three of each.
+template <int DT>
+struct RoleCfg {
+  static constexpr int kDqGroups = 3, kMmaWarps = 3, kDTiles = 9;
+};
+template <>
+struct RoleCfg<kIdxNvExact> {
+  static constexpr int kDqGroups = 4, kMmaWarps = 2, kDTiles = 6;
+};
+template <int DT>
+struct Roles : RoleCfg<DT> {
+  using C = RoleCfg<DT>;
+  static constexpr int kEpGroups = 3;
+  static constexpr int kWarpDq = 1 + C::kMmaWarps;           // first dequant warp
+  static constexpr int kWarpEp = kWarpDq + 4 * C::kDqGroups;  // first max-pool warp
+  static constexpr int kThreads = 32 * (kWarpEp + 4 * kEpGroups);
+  // Partial-maximum slots of the max-pool quarters: page n uses slot n % kPartSlots. A slot is
+  // written again only by page n + kPartSlots, whose MMA needed its accumulator released by all
+  // four quarters at page n + kPartSlots - kDTiles, which each quarter reaches after combining
+  // page n (a warp takes its pages in order): 2 * kDTiles slots are enough.
+  static constexpr int kPartSlots = 2 * C::kDTiles;
+  static_assert(C::kDTiles % kEpGroups == 0 && C::kDTiles % C::kMmaWarps == 0, "an accumulator serves one group");
+  static_assert(kThreads <= 1024, "one CTA");
+};
 
 // Key tiles and query tiles per index kind: E4M3 keys take 32 TMEM columns a tile and the
 // query tile is 32 rows x 128 E4M3; exact keys take 64 columns (f16) and the query tile is
@@ -77,15 +92,15 @@ struct TileCfg {
 };
 template <>
 struct TileCfg<kIdxNvExact> {
-  static constexpr int kATiles = 3;
+  static constexpr int kATiles = 4;
   static constexpr int kACols = 64;
   static constexpr int kBTile = 32 * kD * 2;
   static constexpr int kLutBytes = 256 * 16;
 };
 template <int DT>
 constexpr bool tiles_ok() {
-  return TileCfg<DT>::kATiles % kDqGroups == 0 && TileCfg<DT>::kATiles % kMmaWarps == 0 &&
-         TileCfg<DT>::kACols * TileCfg<DT>::kATiles + 32 * kDTiles <= kTmemCols;
+  return TileCfg<DT>::kATiles % Roles<DT>::kDqGroups == 0 && TileCfg<DT>::kATiles % Roles<DT>::kMmaWarps == 0 &&
+         TileCfg<DT>::kACols * TileCfg<DT>::kATiles + 32 * Roles<DT>::kDTiles <= kTmemCols;
 }
 static_assert(tiles_ok<MSA_INDEX_NVFP4>() && tiles_ok<MSA_INDEX_FP8>() && tiles_ok<kIdxNvExact>(),
               "a key tile serves one dequant group and one MMA warp; TMEM budget");
@@ -109,7 +124,7 @@ struct IdxCfg<MSA_INDEX_FP8> {
 template <>
 struct IdxCfg<kIdxNvExact> {
   static constexpr int kPage = kIdxPageNv;
-  static constexpr int kStages = 18;
+  static constexpr int kStages = 16;
 };
 
 struct IdxParams {
@@ -133,7 +148,8 @@ struct IdxSmem {
   static constexpr int kPage = IdxCfg<DT>::kPage;
   static constexpr int kATiles = TileCfg<DT>::kATiles;
   static constexpr int kBTile = TileCfg<DT>::kBTile;
-  static_assert(kStages % kDqGroups == 0, "a stage serves one dequant group");
+  static constexpr int kDTiles = Roles<DT>::kDTiles, kPartSlots = Roles<DT>::kPartSlots;
+  static_assert(kStages % Roles<DT>::kDqGroups == 0, "a stage serves one dequant group");
   // offsets from a 1024-byte aligned base (pages and query tiles are multiples of 1024 B)
   static constexpr size_t kOffStage = 0;
   static constexpr size_t kOffB = kOffStage + static_cast<size_t>(kStages) * kPage;
@@ -248,8 +264,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kIdxThreads, 1) k_indexer(const IdxParams p, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(Roles<DT>::kThreads, 1)
+    k_indexer(const IdxParams p, const __grid_constant__ CUtensorMap tmap) {
   using S = IdxSmem<DT>;
+  using R = Roles<DT>;
+  constexpr int kDqGroups = R::kDqGroups, kEpGroups = R::kEpGroups, kMmaWarps = R::kMmaWarps;
+  constexpr int kWarpDq = R::kWarpDq, kWarpEp = R::kWarpEp, kIdxThreads = R::kThreads;
+  constexpr int kDTiles = R::kDTiles, kPartSlots = R::kPartSlots;
   constexpr int kStages = S::kStages;
   constexpr int kATiles = TileCfg<DT>::kATiles, kACols = TileCfg<DT>::kACols, kBTile = TileCfg<DT>::kBTile;
   constexpr bool kExact = DT == kIdxNvExact;
@@ -671,7 +692,7 @@ msa_status launch_indexer(const IdxParams& p, const uint8_t* pages, cudaStream_t
   if (cudaFuncSetAttribute(k_indexer<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
-  k_indexer<DT><<<sms, kIdxThreads, smem, stream>>>(p, tmap);
+  k_indexer<DT><<<sms, Roles<DT>::kThreads, smem, stream>>>(p, tmap);
   return msa_host::launch_status();
 }
 

@@ -848,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
           }
         }
-        // ---- K of the next block (its S MMA runs while this block's V and P are made); its
-        // stores are waited for halfway through the V rows
+        // ---- K of the next block (its S MMA runs while this block's P is made); its stores are
+        // waited for, and the tile announced, after this block's V rows
         const bool k_pending = j + 1 < n && do_k(jg + 1, false);
         // ---- V rows -> the E4M3 V tile over the stage: row vrow = key position, MN-major
         if (ok) {

@@ -195,6 +195,45 @@ def test_topk_on_crafted_scores(msa, pad):
                 assert np.array_equal(got[t, g], want), (b, i, g)
 
 
+@pytest.mark.parametrize("maxb", [128, 129])
+@pytest.mark.parametrize("prefill", [False, True])
+def test_topk_short_rows(msa, maxb, prefill):
+    """Batches whose rows cannot exceed 128 blocks take the selection kernel's 4-key register
+    layout (max_blocks_per_seq <= 128), the others the 32-key one: the same crafted rows (ties,
+    NaN, -inf, -0/+0, 5 to 127 candidates) through both, and through the prefill entry point
+    with more than 8 query tokens a sequence, equal the oracle's stable sort."""
+    rng = np.random.default_rng(6 + maxb + prefill)
+    seq_lens = [128 * 128, 128 * 100 + 5, 128 * 65 + 1, 128 * 64 + 1, 128 * 6, 700]
+    q_lens = [12 if prefill else 8, 3, 1, 1, 2, 1]
+    B = len(seq_lens)
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(qsl[-1])
+    scores = rng.standard_normal((T, 4, maxb)).astype(np.float32)
+    scores[0, 0, rng.integers(0, 127, 20)] = np.nan
+    scores[0, 1, rng.integers(0, 127, 20)] = -np.inf
+    scores[1, 2, :] = 0.0
+    scores[1, 2, ::2] = -0.0
+    scores[2, 3, :] = rng.integers(-2, 3, maxb).astype(np.float32)  # heavy ties
+    scores[3, 0, :] = 3.0  # all equal
+    bt = torch.zeros((B, maxb), dtype=torch.int32, device="cuda")
+    batch = msa.Batch(torch.from_numpy(qsl).cuda(), torch.tensor(seq_lens, dtype=torch.int32, device="cuda"), bt,
+                      max_q_len=max(q_lens))
+    sd = torch.from_numpy(scores).cuda()
+    sel = torch.empty((T, 4, 16), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    (msa.msa_topk_prefill if prefill else msa.msa_topk_blocks)(batch, sd, sel, st)
+    got = sel.cpu().numpy()
+    assert msa.status_bits(st) == 0
+    for b in range(B):
+        L, ql = seq_lens[b], q_lens[b]
+        for i in range(ql):
+            t = qsl[b] + i
+            local = (L - ql + i) // 128
+            for g in range(4):
+                want = oracle.select_row(scores[t, g].astype(np.float64), local)
+                assert np.array_equal(got[t, g], want), (b, i, g)
+
+
 def test_paging_invariance(msa):
     """Identity vs permuted block tables: bit-identical scores, selection and output."""
     from workloads.device import DeviceLayer

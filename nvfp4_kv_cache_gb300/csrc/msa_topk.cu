@@ -132,7 +132,9 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t k, int lane) {
 constexpr int kRowsPerCta = 8;
 constexpr int kSurvivors = 64;
 constexpr int kRegKeys = 32;  // rows of up to 32 x 32 keys are held in registers (one load each)
-constexpr int kRegKeysShort = 4;  // the same for rows of up to 128 keys (fewer registers, more warps per SM)
+// The same for rows of up to 128, 256 and 512 keys: fewer registers (more warps per SM) and no
+// work on empty key slots.
+constexpr int kRegKeysShort = 4;
 constexpr int kCand = kSel - 1;  // candidates per (token, group) and shard: the 15 best non-local blocks
 
 // The 15 largest of the n keys key_at(0 .. n-1) (unique; 0 = none), descending, into res[0..14]
@@ -382,9 +384,9 @@ msa_status topk_launch(const msa_batch* batch, const TopkParams& p, const float*
   if (batch->B == 0 || batch->T == 0) return MSA_OK;
   if (block_scores == nullptr || sel == nullptr || !aligned(block_scores, 4) || !aligned(sel, 4))
     return MSA_ERR_INVALID_ARG;
-  // a warp per row (with fewer registers, so more warps per SM, when no row can exceed 128
-  // blocks); a CTA per row when rows may be longer than a warp holds and so few that a CTA each
-  // fits in one wave (two per SM of the part the choice is tuned for)
+  // a warp per row (with as many keys a lane in registers as the longest possible row needs:
+  // 4, 8, 16 or 32); a CTA per row when rows may be longer than a warp holds and so few that a
+  // CTA each fits in one wave (two per SM of the part the choice is tuned for)
   const int rows = batch->T * 4;
   const dim3 grid(ceil_div(rows, kRowsPerCta)), block(32 * kRowsPerCta);
   const cudaError_t e =
@@ -392,7 +394,9 @@ msa_status topk_launch(const msa_batch* batch, const TopkParams& p, const float*
           ? launch_after_previous(k_topk_split, dim3(rows), dim3(32 * kSplitWarps), 0, stream, p)
       : batch->max_blocks_per_seq <= 32 * kRegKeysShort
           ? launch_after_previous(k_topk<kRegKeysShort>, grid, block, 0, stream, p)
-          : launch_after_previous(k_topk<kRegKeys>, grid, block, 0, stream, p);
+      : batch->max_blocks_per_seq <= 32 * 8 ? launch_after_previous(k_topk<8>, grid, block, 0, stream, p)
+      : batch->max_blocks_per_seq <= 32 * 16 ? launch_after_previous(k_topk<16>, grid, block, 0, stream, p)
+                                             : launch_after_previous(k_topk<kRegKeys>, grid, block, 0, stream, p);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   return launch_status();
 }

@@ -195,15 +195,16 @@ def test_topk_on_crafted_scores(msa, pad):
                 assert np.array_equal(got[t, g], want), (b, i, g)
 
 
-@pytest.mark.parametrize("maxb", [128, 129])
+@pytest.mark.parametrize("maxb", [128, 129, 256, 257, 512, 513])
 @pytest.mark.parametrize("prefill", [False, True])
 def test_topk_short_rows(msa, maxb, prefill):
-    """Batches whose rows cannot exceed 128 blocks take the selection kernel's 4-key register
-    layout (max_blocks_per_seq <= 128), the others the 32-key one: the same crafted rows (ties,
-    NaN, -inf, -0/+0, 5 to 127 candidates) through both, and through the prefill entry point
-    with more than 8 query tokens a sequence, equal the oracle's stable sort."""
+    """The selection kernel holds 4, 8, 16 or 32 keys a lane in registers, by the longest row the
+    batch allows (max_blocks_per_seq <= 128, 256, 512, else): the same crafted rows (ties, NaN,
+    -inf, -0/+0, 5 to maxb - 1 candidates) on both sides of each threshold, through the decode
+    entry point and through the prefill one with more than 8 query tokens a sequence, equal the
+    oracle's stable sort."""
     rng = np.random.default_rng(6 + maxb + prefill)
-    seq_lens = [128 * 128, 128 * 100 + 5, 128 * 65 + 1, 128 * 64 + 1, 128 * 6, 700]
+    seq_lens = [128 * maxb, 128 * 100 + 5, 128 * 65 + 1, 128 * 64 + 1, 128 * 6, 700]
     q_lens = [12 if prefill else 8, 3, 1, 1, 2, 1]
     B = len(seq_lens)
     qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)

@@ -256,6 +256,35 @@ __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 2^x of both halves of an f16x2 (-inf gives +0).
+__device__ __forceinline__ uint32_t exp2_f16x2(uint32_t h2) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(h2));
+  return r;
+}
+
+// The two halves of an f16x2 added (in f16), as an fp32.
+__device__ __forceinline__ float sum_f16x2(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 lo, hi, s;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f16 s, lo, hi;\n\tcvt.f32.f16 %0, s;\n\t}"
+      : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// a * b + c on two fp32 lanes in one instruction (the packed fp32 FMA of sm_100 and later).
+__device__ __forceinline__ void fma_f32x2(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
+                                          float& d1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   const uint32_t h2 = cvt_f16x2_e4m3x2(byte & 0xFFu);
   float f;

@@ -599,30 +599,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = mx == -CUDART_INF_F ? 0.f : mx;
         if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
         uint8_t* pt = smem + Smem::kOffP + static_cast<size_t>(x) * kPTile;
+        // P = 2^(s c - mu) of two keys at a time: the exponent by a packed fp32 FMA, rounded to
+        // f16, the power by the f16x2 exp2 (a masked key's -inf gives 0); l sums the f16 P that
+        // the PV MMA reads, in f16 over 8 keys a half and 32 keys a chunk (values <= 1), in fp32
+        // across chunks
         float l = 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t r[32];
           tmem_ld32(ts + 32 * cc, r);
           tmem_wait_ld();
-          {
+          if (!full) {
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
-              uint32_t pw[4];
-#pragma unroll
-              for (int u2 = 0; u2 < 4; ++u2) {
-                const int u = 8 * q8 + 2 * u2;
-                float p0 = fast_exp2(fmaf(__uint_as_float(r[u]), c, -mu));
-                float p1 = fast_exp2(fmaf(__uint_as_float(r[u + 1]), c, -mu));
-                if (!full && 32 * cc + u > rel) p0 = 0.f;
-                if (!full && 32 * cc + u + 1 > rel) p1 = 0.f;
-                l += p0 + p1;
-                pw[u2] = pack_f16x2(p0, p1);
-              }
-              *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
-                  make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            }
+            for (int u = 0; u < 32; ++u)
+              r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
           }
+          uint32_t s8[4];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
+            uint32_t pw[4];
+#pragma unroll
+            for (int u2 = 0; u2 < 4; ++u2) {
+              const int u = 8 * q8 + 2 * u2;
+              float x0, x1;
+              fma_f32x2(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), c, c, -mu, -mu, x0, x1);
+              pw[u2] = exp2_f16x2(pack_f16x2(x0, x1));
+            }
+            s8[q8] = add_f16x2(add_f16x2(pw[0], pw[1]), add_f16x2(pw[2], pw[3]));
+            *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
+                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          }
+          l += sum_f16x2(add_f16x2(add_f16x2(s8[0], s8[1]), add_f16x2(s8[2], s8[3])));
         }
         tc_fence_before();
         fence_proxy_async_smem();  // P is read by the tensor core

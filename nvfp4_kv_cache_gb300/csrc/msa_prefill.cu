@@ -71,6 +71,7 @@ constexpr int kPTile = 128 * kBS * 2;    // 128 query-head rows x 128 keys f16: 
 constexpr int kPAtom = 128 * 128;        //   16 KB each
 constexpr uint32_t kTmemCols = 512;      // S (2 x 128) and O^T (2 x 128), both double-buffered
 constexpr uint32_t kColO = 256;
+constexpr float kLazyMax = 128.0f;      // the largest row sum l a first-chunk reference may keep
 
 struct PfParams {
   int32_t B, T, maxb, num_pages;
@@ -578,58 +579,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t ts = tmem + 128u * static_cast<uint32_t>(x) + lanes;
         const bool full = __all_sync(0xffffffffu, rel >= kBS - 1);  // no key of the warp's rows masked
-        float mr = -CUDART_INF_F;  // the row's max raw score over its unmasked keys
+        // the row's max raw score over the unmasked keys of its first `nc` 32-key chunks
+        auto row_max = [&](int nc) {
+          float mr = -CUDART_INF_F;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(ts + 32 * cc, r);
-          tmem_wait_ld();
-          if (full) {
+          for (int cc = 0; cc < nc; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(ts + 32 * cc, r);
+            tmem_wait_ld();
+            if (!full) {
+#pragma unroll
+              for (int u = 0; u < 32; ++u)
+                r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
+            }
 #pragma unroll
             for (int u = 0; u < 32; u += 4)
               mr = fmaxf(mr, max3f(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
                                    fmaxf(__uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]))));
-          } else {
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-              if (32 * cc + u <= rel) mr = fmaxf(mr, __uint_as_float(r[u]));
           }
-        }
-        const float mx = mr * c;  // c > 0: the max of the scaled scores
-        const float mu = mx == -CUDART_INF_F ? 0.f : mx;
-        if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+          return mr * c;  // c > 0: the max of the scaled scores
+        };
         uint8_t* pt = smem + Smem::kOffP + static_cast<size_t>(x) * kPTile;
-        // P = 2^(s c - mu) of two keys at a time: the exponent by a packed fp32 FMA, rounded to
-        // f16, the power by the f16x2 exp2 (a masked key's -inf gives 0); l sums the f16 P that
-        // the PV MMA reads, in f16 over 8 keys a half and 32 keys a chunk (values <= 1), in fp32
+        // P = 2^(s c - mx) of two keys at a time: the exponent by a packed fp32 FMA, rounded to
+        // f16, the power by the f16x2 exp2 (a masked key's -inf gives 0); returns l, the sum of
+        // the f16 P that the PV MMA reads, in f16 over 8 keys a half and 32 keys a chunk, in fp32
         // across chunks
-        float l = 0.f;
+        auto write_p = [&](float mx) {
+          const float mu = mx == -CUDART_INF_F ? 0.f : mx;
+          float l = 0.f;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(ts + 32 * cc, r);
-          tmem_wait_ld();
-          if (!full) {
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(ts + 32 * cc, r);
+            tmem_wait_ld();
+            if (!full) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-              r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
-          }
-          uint32_t s8[4];
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
-            uint32_t pw[4];
-#pragma unroll
-            for (int u2 = 0; u2 < 4; ++u2) {
-              const int u = 8 * q8 + 2 * u2;
-              float x0, x1;
-              fma_f32x2(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), c, c, -mu, -mu, x0, x1);
-              pw[u2] = exp2_f16x2(pack_f16x2(x0, x1));
+              for (int u = 0; u < 32; ++u)
+                r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
             }
-            s8[q8] = add_f16x2(add_f16x2(pw[0], pw[1]), add_f16x2(pw[2], pw[3]));
-            *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
-                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            uint32_t s8[4];
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
+              uint32_t pw[4];
+#pragma unroll
+              for (int u2 = 0; u2 < 4; ++u2) {
+                const int u = 8 * q8 + 2 * u2;
+                float x0, x1;
+                fma_f32x2(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), c, c, -mu, -mu, x0, x1);
+                pw[u2] = exp2_f16x2(pack_f16x2(x0, x1));
+              }
+              s8[q8] = add_f16x2(add_f16x2(pw[0], pw[1]), add_f16x2(pw[2], pw[3]));
+              *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
+                  make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            }
+            l += sum_f16x2(add_f16x2(add_f16x2(s8[0], s8[1]), add_f16x2(s8[2], s8[3])));
           }
-          l += sum_f16x2(add_f16x2(add_f16x2(s8[0], s8[1]), add_f16x2(s8[2], s8[3])));
+          return l;
+        };
+        // The reference is the maximum over the first 32 keys only (key 0 is never masked in a
+        // valid row), so a P may exceed 1. A row whose l stays within kLazyMax (the bound that
+        // the row's own maximum gives: 128 keys of P <= 1) keeps that reference, the same bound
+        // on its unnormalised o; any other row (P or a sum beyond f16, or a key far above the
+        // first 32) is written again from the maximum over all its keys. The warp runs the
+        // second pass if any of its rows needs it; the rows that kept their reference write the
+        // same P again, so a row's result never depends on the rows it shares a tile with.
+        float mx = row_max(1);
+        if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+        float l = write_p(mx);
+        if (__any_sync(0xffffffffu, !(l <= kLazyMax))) {
+          const float m_all = row_max(4);
+          if (!(l <= kLazyMax)) mx = m_all;
+          l = write_p(mx);
         }
         tc_fence_before();
         fence_proxy_async_smem();  // P is read by the tensor core

@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from parity import OracleSeq, check_attention
 
@@ -40,12 +41,13 @@ def random_selection(w: W.Workload, seed: int, dup: bool = False) -> np.ndarray:
     return sel
 
 
-def run_prefill(msa, dl, w, sel_np, status=None):
+def run_prefill(msa, dl, w, sel_np, status=None, scale=None):
     sel = torch.from_numpy(sel_np).cuda()
     out = torch.full((w.T, 64, 128), 0x7FC0, dtype=torch.uint16, device="cuda")  # NaN fill
     n = msa.msa_prefill_workspace_size(w.B, w.T, dl.batch.max_blocks)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
-    msa.msa_prefill_attn(dl.batch, dl.cache, dl.q8, sel, dl.softmax_scale, out, ws, status)
+    msa.msa_prefill_attn(dl.batch, dl.cache, dl.q8, sel, dl.softmax_scale if scale is None else scale, out, ws,
+                         status)
     torch.cuda.synchronize()
     return out
 
@@ -247,3 +249,46 @@ def test_prefill_rows_with_no_key(msa):
         s = sel[rows]
         ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(s[s >= 0])).attention(s, dl.softmax_scale)
         check_attention(out[rows], ref, f"no-key rows, seq {b}")
+
+
+@pytest.mark.parametrize("sharp", [False, True])
+def test_prefill_first_chunk_reference(msa, sharp):
+    """The prefill softmax takes each (token, head, block) row's reference maximum from the
+    block's first 32 keys and writes the row again from the maximum over all its keys when the
+    row sum passes 128. Against the oracle at the default scale and at softmax_scale 1.0 (logits
+    about 11x wider); at 1.0 the oracle's own scores must show rows of both kinds (those that
+    keep the first-chunk reference and those that cannot), so both paths run."""
+    from workloads.device import DeviceLayer, bf16_to_f32
+
+    w = W.small("first_chunk", [3000, 700], [120, 33], seed=65)
+    dl = DeviceLayer(w, 0)
+    sel = random_selection(w, 166)
+    scale = 1.0 if sharp else dl.softmax_scale
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = bf16_to_f32(run_prefill(msa, dl, w, sel, st, scale=scale)).cpu().numpy()
+    assert msa.status_bits(st) == 0
+    qsl = w.query_start_loc()
+    keep = redo = 0
+    for b in range(w.B):
+        ql, L = w.q_lens[b], w.seq_lens[b]
+        rows = slice(qsl[b], qsl[b] + ql)
+        s = sel[rows]
+        ref = OracleSeq(w, 0, b, "cuda", kv_blocks=np.unique(s[s >= 0]))
+        check_attention(out[rows], ref.attention(s, scale), f"seq {b} at scale {scale}")
+        if not sharp:
+            continue
+        q = oracle.e4m3_decode(ref.q8).reshape(ql, 64, 128)
+        kvals, kscales = ref.kv[0], ref.kv[1]
+        for t in range(ql):
+            p_tok = L - ql + t
+            for g in range(4):
+                for k in dict.fromkeys(int(x) for x in s[t, g] if x >= 0):
+                    keys = np.arange(128 * k, min(128 * k + 128, p_tok + 1))
+                    kd = oracle.e4m3_decode(oracle.dequant_nvfp4(kvals[keys, g], kscales[keys, g]))
+                    z = q[t, 16 * g:16 * g + 16] @ kd.T * scale * np.log2(np.e)
+                    lazy = np.exp2(z - z[:, :32].max(axis=1, keepdims=True)).sum(axis=1)
+                    redo += int((lazy > 128.0).sum())
+                    keep += int((lazy <= 128.0).sum())
+    if sharp:
+        print(f"scale {scale}: {keep} rows keep the first-chunk reference, {redo} exceed it")
+        assert keep > 0 and redo > 0

@@ -579,62 +579,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t ts = tmem + 128u * static_cast<uint32_t>(x) + lanes;
         const bool full = __all_sync(0xffffffffu, rel >= kBS - 1);  // no key of the warp's rows masked
-        // the row's max raw score over the unmasked keys of its first `nc` 32-key chunks
-        auto row_max = [&](int nc) {
-          float mr = -CUDART_INF_F;
-#pragma unroll 1
-          for (int cc = 0; cc < nc; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(ts + 32 * cc, r);
-            tmem_wait_ld();
-            if (!full) {
+        // chunk cc (keys 32 cc .. 32 cc + 31) of the row's raw scores, masked keys set to -inf
+        auto load_chunk = [&](int cc, uint32_t (&r)[32]) {
+          tmem_ld32(ts + 32 * cc, r);
+          tmem_wait_ld();
+          if (!full) {
 #pragma unroll
-              for (int u = 0; u < 32; ++u)
-                r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
-            }
-#pragma unroll
-            for (int u = 0; u < 32; u += 4)
-              mr = fmaxf(mr, max3f(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
-                                   fmaxf(__uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]))));
+            for (int u = 0; u < 32; ++u)
+              r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
           }
+        };
+        auto chunk_max = [&](const uint32_t (&r)[32]) {
+          float mr = -CUDART_INF_F;
+#pragma unroll
+          for (int u = 0; u < 32; u += 4)
+            mr = fmaxf(mr, max3f(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
+                                 fmaxf(__uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]))));
           return mr * c;  // c > 0: the max of the scaled scores
         };
         uint8_t* pt = smem + Smem::kOffP + static_cast<size_t>(x) * kPTile;
-        // P = 2^(s c - mx) of two keys at a time: the exponent by a packed fp32 FMA, rounded to
-        // f16, the power by the f16x2 exp2 (a masked key's -inf gives 0); returns l, the sum of
-        // the f16 P that the PV MMA reads, in f16 over 8 keys a half and 32 keys a chunk, in fp32
-        // across chunks
-        auto write_p = [&](float mx) {
+        // P = 2^(s c - mx) of chunk cc, two keys at a time: the exponent by a packed fp32 FMA,
+        // rounded to f16, the power by the f16x2 exp2 (a masked key's -inf gives 0); returns the
+        // chunk's share of l, the sum of the f16 P that the PV MMA reads (in f16 over 8 keys a
+        // half, then over the chunk)
+        auto write_chunk = [&](int cc, const uint32_t (&r)[32], float mx) {
           const float mu = mx == -CUDART_INF_F ? 0.f : mx;
-          float l = 0.f;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(ts + 32 * cc, r);
-            tmem_wait_ld();
-            if (!full) {
+          uint32_t s8[4];
 #pragma unroll
-              for (int u = 0; u < 32; ++u)
-                r[u] = 32 * cc + u > rel ? __float_as_uint(-CUDART_INF_F) : r[u];
+          for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
+            uint32_t pw[4];
+#pragma unroll
+            for (int u2 = 0; u2 < 4; ++u2) {
+              const int u = 8 * q8 + 2 * u2;
+              float x0, x1;
+              fma_f32x2(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), c, c, -mu, -mu, x0, x1);
+              pw[u2] = exp2_f16x2(pack_f16x2(x0, x1));
             }
-            uint32_t s8[4];
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of the row's f16 P
-              uint32_t pw[4];
-#pragma unroll
-              for (int u2 = 0; u2 < 4; ++u2) {
-                const int u = 8 * q8 + 2 * u2;
-                float x0, x1;
-                fma_f32x2(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), c, c, -mu, -mu, x0, x1);
-                pw[u2] = exp2_f16x2(pack_f16x2(x0, x1));
-              }
-              s8[q8] = add_f16x2(add_f16x2(pw[0], pw[1]), add_f16x2(pw[2], pw[3]));
-              *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
-                  make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            }
-            l += sum_f16x2(add_f16x2(add_f16x2(s8[0], s8[1]), add_f16x2(s8[2], s8[3])));
+            s8[q8] = add_f16x2(add_f16x2(pw[0], pw[1]), add_f16x2(pw[2], pw[3]));
+            *reinterpret_cast<uint4*>(pt + (cc >> 1) * kPAtom + sw128_chunk_off(row, 4 * (cc & 1) + q8)) =
+                make_uint4(pw[0], pw[1], pw[2], pw[3]);
           }
-          return l;
+          return sum_f16x2(add_f16x2(add_f16x2(s8[0], s8[1]), add_f16x2(s8[2], s8[3])));
         };
         // The reference is the maximum over the first 32 keys only (key 0 is never masked in a
         // valid row), so a P may exceed 1. A row whose l stays within kLazyMax (the bound that
@@ -643,13 +628,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first 32) is written again from the maximum over all its keys. The warp runs the
         // second pass if any of its rows needs it; the rows that kept their reference write the
         // same P again, so a row's result never depends on the rows it shares a tile with.
-        float mx = row_max(1);
-        if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
-        float l = write_p(mx);
+        float mx, l;
+        {
+          uint32_t r[32];
+          load_chunk(0, r);
+          mx = chunk_max(r);
+          if (!(ok = wwait(&bars.p_empty[x], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u))) break;
+          l = write_chunk(0, r, mx);
+        }
+#pragma unroll 1
+        for (int cc = 1; cc < 4; ++cc) {
+          uint32_t r[32];
+          load_chunk(cc, r);
+          l += write_chunk(cc, r, mx);
+        }
         if (__any_sync(0xffffffffu, !(l <= kLazyMax))) {
-          const float m_all = row_max(4);
+          float m_all = -CUDART_INF_F;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r[32];
+            load_chunk(cc, r);
+            m_all = fmaxf(m_all, chunk_max(r));
+          }
           if (!(l <= kLazyMax)) mx = m_all;
-          l = write_p(mx);
+          l = 0.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r[32];
+            load_chunk(cc, r);
+            l += write_chunk(cc, r, mx);
+          }
         }
         tc_fence_before();
         fence_proxy_async_smem();  // P is read by the tensor core

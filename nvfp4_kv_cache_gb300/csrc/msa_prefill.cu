@@ -380,20 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- producer ---------------------------------------------------------------------------
     if (lane == 0) prefetch_tensormap(&q_map);
     const uint64_t pol = policy_evict_last();  // a token's query heads serve up to 16 chunks
-    int k = 0, i = 0;  // chunks taken, query tiles issued
-    for (;; ++k) {
+    int i = 0;  // query tiles issued
+    // Takes the next chunk and publishes its entry list in meta slot kk % kMetaSlots: its count,
+    // or -1 when no chunk is left (the slot then carries the end mark), -2 on a give-up.
+    auto fetch_meta = [&](int kk) -> int {
       int c = 0;
       if (lane == 0) c = atomicAdd(&p.hdr[3], 1);
       c = __shfl_sync(0xffffffffu, c, 0);
-      const int ms = k % kMetaSlots;
-      if (!wwait(&bars.meta_empty[ms], (static_cast<uint32_t>(k / kMetaSlots) & 1u) ^ 1u)) break;
+      const int ms = kk % kMetaSlots;
+      if (!wwait(&bars.meta_empty[ms], (static_cast<uint32_t>(kk / kMetaSlots) & 1u) ^ 1u)) return -2;
       ChunkMeta& m = meta[ms];
       if (c >= nchunks) {
         if (lane == 0) {
           m.n = -1;
           mbar_arrive(&bars.meta_full[ms]);
         }
-        break;
+        return -1;
       }
       const int4 ch = p.chunks[c];
       for (int e = lane; e < ch.y; e += 32) m.e[e] = p.entries[ch.x + e];
@@ -407,18 +409,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence_block();
         mbar_arrive(&bars.meta_full[ms]);
       }
+      return ch.y;
+    };
+    // The entry list of chunk k + 1 is published before chunk k's query tiles are issued, so that
+    // the dequant warps turn its K and V rows into tiles while chunk k's tiles run.
+    int n_next = fetch_meta(0);
+    for (int k = 0; n_next >= 0; ++k) {
+      const int n = n_next;
+      const ChunkMeta& m = meta[k % kMetaSlots];  // not refilled before chunk k + kMetaSlots
+      n_next = fetch_meta(k + 1);
+      if (n_next == -2) break;
       // the chunk's query tiles: 8 lanes copy one selection's 16 query rows each
       bool ok = true;
-      for (int j = 0; j < ntiles_of(ch.y); ++j, ++i) {
+      for (int j = 0; j < ntiles_of(n); ++j, ++i) {
         const int qb = i % kQBufs;
         if (!(ok = wwait(&bars.q_empty[qb], (static_cast<uint32_t>(i / kQBufs) & 1u) ^ 1u))) break;
-        const int ne = min(kTileSel, ch.y - kTileSel * j);
+        const int ne = min(kTileSel, n - kTileSel * j);
         if (lane == 0) mbar_arrive_expect_tx(&bars.q_full[qb], static_cast<uint32_t>(ne) * kHPG * kD);
         __syncwarp();
         if (lane < ne) {
           const int t = m.e[kTileSel * j + lane].x >> 4;
           tma_load_2d(smem + Smem::kOffQ + static_cast<size_t>(qb) * kQTile + lane * kHPG * kD, &q_map, 0,
-                      t * kQHeads + ch.w * kHPG, &bars.q_full[qb], pol);
+                      t * kQHeads + m.g * kHPG, &bars.q_full[qb], pol);
         }
       }
       if (!ok) break;
